@@ -1,0 +1,189 @@
+"""Plain CPU oracle for the QoQ W4A8 g128 linear layer (test infrastructure).
+
+Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The CUDA product path never imports it.
+
+The arithmetic lives in ``qoq_oracle.c`` (plain C, one function per step of
+the method, each citing the page passage it follows).  This module compiles it
+with gcc on first use and wraps it with numpy-level functions; it adds no
+arithmetic of its own.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(_HERE, "qoq_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_LOCK = threading.Lock()
+
+GCC_FLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math"]
+
+
+def compile_source(src: str, out: str) -> str:
+    """gcc one C file into a shared library (portable C11, no target flags)."""
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    tmp = out + f".{os.getpid()}.tmp"
+    subprocess.check_call(["gcc", *GCC_FLAGS, src, "-o", tmp, "-lm"])
+    os.replace(tmp, out)
+    return out
+
+
+def build(force: bool = False) -> str:
+    """Compile qoq_oracle.c into oracle/_build/liboracle.so."""
+    if force or not os.path.exists(LIB_PATH) or os.path.getmtime(LIB_PATH) < os.path.getmtime(SRC):
+        compile_source(SRC, LIB_PATH)
+    return LIB_PATH
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def _check(rc, what):
+    if rc == 1:
+        raise OracleError(f"{what}: bad arguments")
+    return rc
+
+
+class Oracle:
+    """numpy-level wrapper around one build of qoq_oracle.c."""
+
+    def __init__(self, path: str):
+        lib = ctypes.CDLL(path)
+        P = ctypes.c_void_p
+        i32 = ctypes.c_int
+        lib.qoq_oracle_half_to_double.argtypes = [ctypes.c_uint16]
+        lib.qoq_oracle_half_to_double.restype = ctypes.c_double
+        lib.qoq_oracle_double_to_half.argtypes = [ctypes.c_double]
+        lib.qoq_oracle_double_to_half.restype = ctypes.c_uint16
+        lib.qoq_oracle_dequant_code.argtypes = [ctypes.c_int64] * 3
+        lib.qoq_oracle_dequant_code.restype = ctypes.c_int64
+        lib.qoq_oracle_dequant_real.argtypes = [ctypes.c_double] * 3
+        lib.qoq_oracle_dequant_real.restype = ctypes.c_double
+        lib.qoq_oracle_weight_quant.argtypes = [i32, i32, i32, P, P, P, P, P, P]
+        lib.qoq_oracle_weight_quant.restype = i32
+        lib.qoq_oracle_dequant_weights.argtypes = [i32, i32, i32, P, P, P, P]
+        lib.qoq_oracle_dequant_weights.restype = i32
+        lib.qoq_oracle_act_quant.argtypes = [i32, i32, P, P, P]
+        lib.qoq_oracle_act_quant.restype = i32
+        lib.qoq_oracle_gemm.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P, P]
+        lib.qoq_oracle_gemm.restype = i32
+        lib.qoq_oracle_gemm_entries.argtypes = [i32, P, P, i32, i32, P, P, P, P, P, P, P, P]
+        lib.qoq_oracle_gemm_entries.restype = i32
+        self.lib = lib
+        self.path = path
+
+    # ------------------------------------------------------------ scalars --
+    def half_to_double(self, b: int) -> float:
+        return self.lib.qoq_oracle_half_to_double(int(b) & 0xFFFF)
+
+    def double_to_half(self, x: float) -> int:
+        return int(self.lib.qoq_oracle_double_to_half(float(x)))
+
+    def dequant_code(self, q: int, zero: int, scale: int) -> int:
+        return int(self.lib.qoq_oracle_dequant_code(q, zero, scale))
+
+    def dequant_real(self, q: float, zero: float, scale: float) -> float:
+        return float(self.lib.qoq_oracle_dequant_real(q, zero, scale))
+
+    # ------------------------------------------------------------- arrays --
+    def weight_quant(self, W_bits: np.ndarray, g: int = 128) -> dict:
+        """Progressive group quantization of fp16 weights W [N][K] (uint16 bits).
+
+        Returns s1 [N] (fp16 bits), Q8 [N][K] int8, q4 [N][K] uint8 (one code
+        per byte), s2 [N][K/g] uint8 and z [N][K/g] uint8.
+        """
+        W = _c(W_bits, np.uint16)
+        N, K = W.shape
+        G = K // g if g > 0 else 0
+        s1 = np.empty(N, np.uint16)
+        Q8 = np.empty((N, K), np.int8)
+        q4 = np.empty((N, K), np.uint8)
+        s2 = np.empty((N, max(G, 1)), np.uint8)
+        z = np.empty((N, max(G, 1)), np.uint8)
+        _check(self.lib.qoq_oracle_weight_quant(N, K, g, _p(W), _p(s1), _p(Q8), _p(q4), _p(s2),
+                                                _p(z)), "weight_quant")
+        return {"s1": s1, "Q8": Q8, "q4": q4, "s2": np.ascontiguousarray(s2[:, :G]),
+                "z": np.ascontiguousarray(z[:, :G])}
+
+    def dequant_weights(self, q4, s2, z, g: int = 128) -> np.ndarray:
+        q4 = _c(q4, np.uint8)
+        N, K = q4.shape
+        w8 = np.empty((N, K), np.int16)
+        _check(self.lib.qoq_oracle_dequant_weights(N, K, g, _p(q4), _p(_c(s2, np.uint8)),
+                                                   _p(_c(z, np.uint8)), _p(w8)), "dequant_weights")
+        return w8
+
+    def act_quant(self, X_bits: np.ndarray):
+        """Per-token symmetric int8 quantization of fp16 X [M][K] -> (Xq, sx bits)."""
+        X = _c(X_bits, np.uint16)
+        M, K = X.shape
+        Xq = np.empty((M, K), np.int8)
+        sx = np.empty(M, np.uint16)
+        _check(self.lib.qoq_oracle_act_quant(M, K, _p(X), _p(Xq), _p(sx)), "act_quant")
+        return Xq, sx
+
+    def gemm(self, Xq, sx, q4, s2, z, s1, g: int = 128, want_acc: bool = True):
+        """acc [M][N] int64 (or None) and Y [M][N] fp16 bits."""
+        Xq = _c(Xq, np.int8)
+        q4 = _c(q4, np.uint8)
+        M, K = Xq.shape
+        N = q4.shape[0]
+        acc = np.empty((M, N), np.int64) if want_acc else None
+        Y = np.empty((M, N), np.uint16)
+        rc = _check(self.lib.qoq_oracle_gemm(M, N, K, g, _p(Xq), _p(_c(sx, np.uint16)), _p(q4),
+                                             _p(_c(s2, np.uint8)), _p(_c(z, np.uint8)),
+                                             _p(_c(s1, np.uint16)), _p(acc), _p(Y)), "gemm")
+        if rc == 2:
+            raise OracleError("gemm: |acc| reached 2^31")
+        return acc, Y
+
+    def gemm_entries(self, m_idx, n_idx, Xq, sx, q4, s2, z, s1, g: int = 128):
+        """acc and Y for the listed (m, n) entries only."""
+        m_idx = _c(m_idx, np.int32)
+        n_idx = _c(n_idx, np.int32)
+        Xq = _c(Xq, np.int8)
+        q4 = _c(q4, np.uint8)
+        K = Xq.shape[1]
+        cnt = int(m_idx.shape[0])
+        acc = np.empty(cnt, np.int64)
+        Y = np.empty(cnt, np.uint16)
+        _check(self.lib.qoq_oracle_gemm_entries(cnt, _p(m_idx), _p(n_idx), K, g, _p(Xq),
+                                                _p(_c(sx, np.uint16)), _p(q4), _p(_c(s2, np.uint8)),
+                                                _p(_c(z, np.uint8)), _p(_c(s1, np.uint16)), _p(acc),
+                                                _p(Y)), "gemm_entries")
+        return acc, Y
+
+
+_DEFAULT: Oracle | None = None
+
+
+def default() -> Oracle:
+    global _DEFAULT
+    with _LOCK:
+        if _DEFAULT is None:
+            _DEFAULT = Oracle(build())
+    return _DEFAULT
+
+
+def __getattr__(name):
+    # module-level shortcuts: oracle.weight_quant(...) etc. use the default build
+    if name in ("half_to_double", "double_to_half", "dequant_code", "dequant_real", "weight_quant",
+                "dequant_weights", "act_quant", "gemm", "gemm_entries"):
+        return getattr(default(), name)
+    raise AttributeError(name)

@@ -1,0 +1,335 @@
+"""Pins for the oracle: checks against what the pages and mathematics fix.
+
+Each check takes an ``oracle.Oracle`` instance and raises AssertionError on a
+mismatch, so the same checks run against the real build and against builds
+with a planted mistake (``test_oracle_mutants.py``).  None of them retypes the
+oracle's formulas: they use stored hand-worked values, brute-force searches,
+library routines (numpy matmul and float16 rounding), closed-form bounds and
+invariants.
+"""
+from __future__ import annotations
+
+import os
+from fractions import Fraction
+
+import numpy as np
+
+from w4a8_quantized_serving_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def load_golden(name: str) -> dict:
+    out = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            k, v = (t.strip() for t in line.split("=", 1))
+            vals = [int(t, 0) for t in v.split()]
+            out[k] = vals if len(vals) > 1 else vals[0]
+    return out
+
+
+def f16(values) -> np.ndarray:
+    return np.asarray(values, dtype=np.float64).astype(np.float16)
+
+
+def half_val(bits) -> np.ndarray:
+    return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float64)
+
+
+def nearest_int_half_even(x: Fraction) -> int:
+    """Brute-force nearest integer to x, ties to the even one."""
+    lo = x.numerator // x.denominator
+    best = None
+    for c in range(lo - 1, lo + 3):
+        d = abs(x - c)
+        if best is None or d < best[0] or (d == best[0] and c % 2 == 0):
+            best = (d, c)
+    return best[1]
+
+
+# --------------------------------------------------------------------------
+# binary16 conversions against numpy's IEEE float16
+# --------------------------------------------------------------------------
+
+def check_half_to_double(o) -> None:
+    allbits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = allbits.view(np.float16).astype(np.float64)
+    for b in range(0, 65536, 7):  # every 7th pattern covers all exponents
+        v = o.half_to_double(b)
+        r = ref[b]
+        if np.isnan(r):
+            assert np.isnan(v), b
+        else:
+            assert v == r, (hex(b), v, r)
+
+
+def check_double_to_half(o) -> None:
+    rng = np.random.default_rng(1234)
+    xs = np.concatenate([
+        rng.standard_normal(3000) * 10.0 ** rng.integers(-9, 6, 3000),
+        # exact ties between neighbouring fp16 values
+        (np.arange(2048, 4096, 3, dtype=np.float64) + 0.5) * 2.0 ** -11,
+        (np.arange(1, 1024, 5, dtype=np.float64) + 0.5) * 2.0 ** -24,  # subnormal ties
+        np.array([65504.0, 65519.99, 65520.0, 70000.0, 2.0 ** -25, 2.0 ** -26, 6.1e-5, 0.0, -0.0]),
+    ])
+    with np.errstate(over="ignore"):
+        wants = xs.astype(np.float16).view(np.uint16)
+    for x, want in zip(xs, wants):
+        got = o.double_to_half(float(x))
+        want = int(want)
+        assert got == want, (x, hex(got), hex(want))
+
+
+# --------------------------------------------------------------------------
+# the hand-worked example and the printed dequant literal
+# --------------------------------------------------------------------------
+
+def _appendix_inputs(gold: dict, K: int = 8, g: int = 4, embed: bool = False):
+    Q8 = np.array(gold["Q8"], np.int64)
+    Xq = np.array(gold["Xq"], np.int64)
+    if not embed:
+        W = f16(Q8 * 2.0 ** -7).reshape(1, K)
+        X = f16(Xq * 2.0 ** -6).reshape(1, K)
+        return W, X
+    # g = 128 embedding: group j of the example sits at k = 128 j + 0..3, zeros elsewhere
+    Wl = np.zeros(K, np.float64)
+    Xl = np.zeros(K, np.float64)
+    for j in range(2):
+        Wl[128 * j:128 * j + 4] = Q8[4 * j:4 * j + 4] * 2.0 ** -7
+        Xl[128 * j:128 * j + 4] = Xq[4 * j:4 * j + 4] * 2.0 ** -6
+    return f16(Wl).reshape(1, K), f16(Xl).reshape(1, K)
+
+
+def check_appendix_a(o) -> None:
+    gold = load_golden("appendix_a_g4.txt")
+    g = gold["g"]
+    W, X = _appendix_inputs(gold)
+    r = o.weight_quant(synth.bits(W), g)
+    assert int(r["s1"][0]) == gold["s1_bits"]
+    assert r["Q8"][0].tolist() == gold["Q8"]
+    assert r["s2"][0].tolist() == gold["s2"]
+    assert r["z"][0].tolist() == gold["z"]
+    assert r["q4"][0].tolist() == gold["q4"]
+    w8 = o.dequant_weights(r["q4"], r["s2"], r["z"], g)
+    assert w8[0].tolist() == gold["w8"]
+    Xq, sx = o.act_quant(synth.bits(X))
+    assert Xq[0].tolist() == gold["Xq"]
+    assert int(sx[0]) == gold["sx_bits"]
+    acc, Y = o.gemm(Xq, sx, r["q4"], r["s2"], r["z"], r["s1"], g)
+    assert int(acc[0, 0]) == gold["acc"] != gold["acc_half_away"]
+    assert int(Y[0, 0]) == gold["Y_bits"]
+
+
+def check_appendix_a_g128(o) -> None:
+    """The same example embedded at g = 128 (K = 256), rows replicated to N = 128."""
+    gold = load_golden("appendix_a_g4.txt")
+    W1, X = _appendix_inputs(gold, K=256, embed=True)
+    W = np.repeat(W1, 128, axis=0)
+    r = o.weight_quant(synth.bits(W), 128)
+    assert (r["s2"] == np.array(gold["s2"], np.uint8)).all()
+    assert (r["z"] == np.array(gold["z"], np.uint8)).all()
+    Xq, sx = o.act_quant(synth.bits(X))
+    acc, Y = o.gemm(Xq, sx, r["q4"], r["s2"], r["z"], r["s1"], 128)
+    assert (acc == gold["acc"]).all()
+    assert (Y == gold["Y_bits"]).all()
+
+
+def check_fig3_literal(o) -> None:
+    """QFactory notes, Fig. 3: (6 - 2) x (-0.4) = -1.6; the integer form of the same rule."""
+    assert o.dequant_real(6, 2, -0.4) == -1.6
+    assert o.dequant_code(6, 2, 4) == 16
+    assert o.dequant_code(2, 6, 4) == -16
+
+
+# --------------------------------------------------------------------------
+# brute force on tiny inputs
+# --------------------------------------------------------------------------
+
+def _tiny_rows(seed: int, n: int, k: int) -> np.ndarray:
+    rng = np.random.default_rng(seed)
+    W = rng.standard_normal((n, k)) * 0.05
+    W[:, rng.integers(0, k)] *= 8.0
+    W[0, :] = np.abs(W[0, :])  # an all-positive row
+    W[1, :] = -np.abs(W[1, :])  # an all-negative row
+    return f16(W)
+
+
+def check_level1_bruteforce(o) -> None:
+    W = _tiny_rows(7, 24, 16)
+    r = o.weight_quant(synth.bits(W), 8)
+    s1 = half_val(r["s1"])
+    for n in range(W.shape[0]):
+        amax = float(np.max(np.abs(W[n].astype(np.float64))))
+        # s1 is the fp16 nearest to amax/119 up to one fp16 half-ulp plus an fp32 rounding
+        assert abs(s1[n] - amax / 119) <= s1[n] * (2.0 ** -11 + 2.0 ** -23) + 1e-30
+        sf = Fraction(float(s1[n]))
+        for k in range(W.shape[1]):
+            w = Fraction(float(W[n, k]))
+            # nearest code in [-119, 119] to w/s1, ties to even
+            want = max(-119, min(119, nearest_int_half_even(w / sf)))
+            assert int(r["Q8"][n, k]) == want, (n, k)
+
+
+def check_level2_bruteforce(o) -> None:
+    W = _tiny_rows(11, 32, 16)
+    g = 4
+    r = o.weight_quant(synth.bits(W), g)
+    for n in range(W.shape[0]):
+        for j in range(W.shape[1] // g):
+            grp = [int(v) for v in r["Q8"][n, j * g:(j + 1) * g]]
+            lo, hi = min(0, min(grp)), max(0, max(grp))
+            # smallest integer scale >= 1 whose 16-level grid spans [lo, hi]
+            s2 = next(s for s in range(1, 64) if 15 * s >= hi - lo)
+            # zero point: the grid index of 0, nearest integer to -lo/s2, ties to even
+            zero = nearest_int_half_even(Fraction(-lo, s2))
+            assert int(r["s2"][n, j]) == s2, (n, j)
+            assert int(r["z"][n, j]) == zero, (n, j)
+            for t, q8 in enumerate(grp):
+                c = nearest_int_half_even(Fraction(q8, s2))
+                assert int(r["q4"][n, j * g + t]) == max(0, min(15, c + zero)), (n, j, t)
+
+
+# --------------------------------------------------------------------------
+# invariants and closed-form bounds
+# --------------------------------------------------------------------------
+
+def _adversarial_weights() -> np.ndarray:
+    rng = np.random.default_rng(5)
+    K = 256
+    rows = [
+        np.full(K, 0.5), np.full(K, -0.25), np.zeros(K),
+        np.where(np.arange(K) % 2 == 0, 1.0, -1.0),
+        np.linspace(-3, 3, K), rng.standard_normal(K) * 1e-3,
+        np.where(np.arange(K) % 128 == 5, 40.0, rng.standard_normal(K) * 0.01),
+        (rng.integers(-119, 120, K) * 2.0 ** -7),
+    ]
+    return f16(np.stack(rows + [rng.standard_normal(K) * 0.02 for _ in range(56)]))
+
+
+def check_invariants(o) -> None:
+    W = np.concatenate([_adversarial_weights(), synth.weights(64, 256, 99)])
+    g = 128
+    r = o.weight_quant(synth.bits(W), g)
+    Q8 = r["Q8"].astype(np.int64)
+    s2 = r["s2"].astype(np.int64)
+    z = r["z"].astype(np.int64)
+    q4 = r["q4"].astype(np.int64)
+    w8 = o.dequant_weights(r["q4"], r["s2"], r["z"], g).astype(np.int64)
+    s2e = np.repeat(s2, g, axis=1)
+    assert Q8.min() >= -119 and Q8.max() <= 119
+    assert s2.min() >= 1 and s2.max() <= 16
+    assert z.min() >= 0 and z.max() <= 15
+    assert q4.min() >= 0 and q4.max() <= 15
+    assert (2 * np.abs(w8 - Q8) <= s2e).all()  # group error at most s2/2
+    assert w8.min() >= -127 and w8.max() <= 127  # the protective range works
+    # w8 is the dequant of the stored codes with the stored parameters
+    assert (w8 == (q4 - np.repeat(z, g, axis=1)) * s2e).all()
+
+
+def check_error_bounds(o) -> None:
+    W = synth.weights(64, 512, 3)
+    X = synth.activations(16, 512, 3)
+    g = 128
+    r = o.weight_quant(synth.bits(W), g)
+    w8 = o.dequant_weights(r["q4"], r["s2"], r["z"], g).astype(np.float64)
+    s1 = half_val(r["s1"])[:, None]
+    s2e = np.repeat(r["s2"].astype(np.float64), g, axis=1)
+    Wd = W.astype(np.float64)
+    assert (np.abs(s1 * w8 - Wd) <= s1 * (0.5 + s2e / 2) * (1 + 1e-12)).all()
+    Xq, sx = o.act_quant(synth.bits(X))
+    sxv = half_val(sx)[:, None]
+    assert (np.abs(sxv * Xq - X.astype(np.float64)) <= sxv / 2 * (1 + 1e-12)).all()
+    assert np.abs(Xq).max() <= 127
+
+
+def check_lossless_grid(o) -> None:
+    """When a group already lies on its 16-level grid, level 2 loses nothing.
+
+    Group 0 holds multiples of 7 spanning exactly [-49, 56] (15 steps of 7), so
+    s2 = 7, z = 7 and every value is a grid point; group 2 spans [-7, 8]
+    (s2 = 1).  Group 1 holds the row maximum 119 * 2^-7, which pins s1 = 2^-7
+    so that the level-1 codes are the integers written here.
+    """
+    k = np.arange(128)
+    g0 = ((k % 16) - 7) * 7  # -49 .. 56
+    g1 = np.zeros(128, np.int64)
+    g1[17] = 119
+    g2 = (k % 16) - 7  # -7 .. 8
+    q8 = np.concatenate([g0, g1, g2]).astype(np.int64)
+    W = f16(q8 * 2.0 ** -7).reshape(1, -1)
+    r = o.weight_quant(synth.bits(W), 128)
+    assert int(r["s1"][0]) == 0x2000
+    assert (r["Q8"][0] == q8).all()
+    assert r["s2"][0].tolist() == [7, 8, 1] and r["z"][0].tolist() == [7, 0, 7]
+    w8 = o.dequant_weights(r["q4"], r["s2"], r["z"], 128)[0]
+    assert (w8[:128] == q8[:128]).all() and (w8[256:] == q8[256:]).all()
+
+
+def check_zero_and_underflow(o) -> None:
+    W = np.zeros((3, 256), np.float16)
+    W[1, 3] = np.float16(2.0 ** -24)  # amax/119 underflows fp16 -> treated as a zero row
+    W[2, :] = np.float16(1.0)
+    r = o.weight_quant(synth.bits(W), 128)
+    for n in (0, 1):
+        assert int(r["s1"][n]) == 0
+        assert (r["Q8"][n] == 0).all() and (r["q4"][n] == 0).all()
+        assert (r["s2"][n] == 1).all() and (r["z"][n] == 0).all()
+    X = np.zeros((2, 256), np.float16)
+    X[1, :] = np.float16(-3.0)
+    Xq, sx = o.act_quant(synth.bits(X))
+    assert int(sx[0]) == 0 and (Xq[0] == 0).all()
+    assert (Xq[1] == -127).all()
+
+
+# --------------------------------------------------------------------------
+# the GEMM against a library matmul
+# --------------------------------------------------------------------------
+
+def check_gemm_library(o) -> None:
+    M, N, K, g = 9, 40, 384, 128
+    W = synth.weights(N, K, 21)
+    X = synth.activations(M, K, 21)
+    r = o.weight_quant(synth.bits(W), g)
+    Xq, sx = o.act_quant(synth.bits(X))
+    acc, Y = o.gemm(Xq, sx, r["q4"], r["s2"], r["z"], r["s1"], g)
+    w8 = o.dequant_weights(r["q4"], r["s2"], r["z"], g).astype(np.int64)
+    assert (acc == Xq.astype(np.int64) @ w8.T).all()
+    # float dequant-then-matmul in float64 agrees with the scaled integer sum
+    Xf = half_val(sx)[:, None] * Xq
+    Wf = half_val(r["s1"])[:, None] * w8
+    Yf = Xf @ Wf.T
+    scaled = acc * half_val(sx)[:, None] * half_val(r["s1"])[None, :]
+    assert np.allclose(Yf, scaled, rtol=1e-12, atol=1e-300)
+    # the fp16 result is the library's round-to-nearest of the exact product
+    assert (Y == scaled.astype(np.float16).view(np.uint16)).all()
+    # sampled entries agree with the full product
+    mi = np.array([0, 3, 8, 8], np.int32)
+    ni = np.array([0, 39, 1, 17], np.int32)
+    a2, y2 = o.gemm_entries(mi, ni, Xq, sx, r["q4"], r["s2"], r["z"], r["s1"], g)
+    assert (a2 == acc[mi, ni]).all() and (y2 == Y[mi, ni]).all()
+    # an operand swap would be caught: W rows are output channels
+    assert acc.shape == (M, N)
+
+
+def check_acc_range(o) -> None:
+    """|acc| <= 127 * 127 * K stays below 2^31 for K <= 131072 (worst case)."""
+    K = 1024
+    W = np.full((1, K), np.float16(1.0))
+    X = np.full((1, K), np.float16(1.0))
+    r = o.weight_quant(synth.bits(W), 128)
+    Xq, sx = o.act_quant(synth.bits(X))
+    acc, _ = o.gemm(Xq, sx, r["q4"], r["s2"], r["z"], r["s1"], 128)
+    # Q8 = 119 everywhere: group range [0, 119] -> s2 = 8, z = 0, q4 = 15, w8 = 120
+    assert int(acc[0, 0]) == 127 * 120 * K
+
+
+ALL_CHECKS = [
+    check_half_to_double, check_double_to_half, check_appendix_a, check_appendix_a_g128,
+    check_fig3_literal, check_level1_bruteforce, check_level2_bruteforce, check_invariants,
+    check_error_bounds, check_lossless_grid, check_zero_and_underflow, check_gemm_library,
+    check_acc_range,
+]
