@@ -1,0 +1,399 @@
+"""Benchmark of the W4A8 g128 linear layer on GB300.
+
+One step = one pass of the hot path over one batch: per-token int8
+quantization of the activations (qoq_quant_act) and the W4A8 GEMM
+(qoq_w4a8_gemm), with the weights packed offline (qoq_pack_weights, timed
+separately).  Default workload: the 7B fused-QKV decode projection,
+M=16, N=12288, K=4096, g=128 (seed 1).
+
+Timing: W untimed warm-up steps, then K steps between CUDA events on the
+launching stream with a barrier and a device synchronize on both sides.  The
+inputs of consecutive steps rotate through a pool of independent buffer sets
+larger than 3x L2, so every step streams its weights from HBM.
+
+Output: one JSON line (rank 0).  Keys beyond the metric: roofline of the
+dominant kernel (the GEMM call), the oracle's CPU baseline, the end-to-end
+number through the public API with host buffers, clocks sampled during the
+timed region, and the count of kernel launches inside it.
+
+--impl reference times the oracle (the plain CPU implementation the tests
+check against) on the host cores instead: it is the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from w4a8_quantized_serving_gb300 import synth  # noqa: E402
+
+METRIC = "W4A8 g128 GEMM effective TOPS & HBM GB/s (% of roofline), M=1..4096"
+UNIT = "TOPS"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def algorithmic_bytes(M: int, N: int, K: int) -> dict:
+    """Bytes the GEMM call must move at least once: q4 nibbles, per-group s2 and
+    z, s1, Xq, s_x, and the fp16 output; plus the activation quantizer's."""
+    gemm = N * K // 2 + 2 * N * (K // 128) + 2 * N + M * K + 2 * M + 2 * M * N
+    act = 2 * M * K + M * K + 2 * M
+    return {"gemm": gemm, "act": act, "step": gemm + act}
+
+
+def load_peaks() -> tuple[dict, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env() -> tuple[int, int, int]:
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+# ------------------------------------------------------------------ clocks --
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "power_w_max": max(power), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------- CPU oracle --
+
+def oracle_step_timing(c: dict, budget_s: float, n_sample: int | None = None) -> dict:
+    """Time the oracle on a bounded sample of the workload: all M tokens
+    quantized, the GEMM over a sample of output channels (weights quantized
+    beforehand, outside the timing, as on the GPU)."""
+    import oracle
+
+    M, N, K = c["M"], c["N"], c["K"]
+    if n_sample is None:
+        n_sample = N
+    n_sample = min(N, n_sample)
+    W = synth.weights(n_sample, K, c["seed"])  # the first n_sample output channels
+    X = synth.activations(M, K, c["seed"])
+    wq = oracle.weight_quant(synth.bits(W), 128)
+    times = []
+    t_end = time.perf_counter() + budget_s
+    while True:
+        t0 = time.perf_counter()
+        Xq, sx = oracle.act_quant(synth.bits(X))
+        oracle.gemm(Xq, sx, wq["q4"], wq["s2"], wq["z"], wq["s1"], 128, want_acc=False)
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() >= t_end or len(times) >= 50:
+            break
+    t = statistics.median(times)
+    ops = 2.0 * M * n_sample * K
+    return {"value": ops / t / 1e12, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"act-quant of all {M} tokens + GEMM over {n_sample} of {N} output channels, "
+                      f"K={K}; median of {len(times)} runs of {t:.3f} s (single-threaded C)",
+            "seconds_per_sample": t}
+
+
+def run_reference(args, c: dict) -> None:
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    M, N, K = c["M"], c["N"], c["K"]
+    import oracle
+
+    n_sample = min(N, 512)
+    W = synth.weights(n_sample, K, c["seed"])
+    X = synth.activations(M, K, c["seed"])
+    wq = oracle.weight_quant(synth.bits(W), 128)
+
+    def step():
+        Xq, sx = oracle.act_quant(synth.bits(X))
+        oracle.gemm(Xq, sx, wq["q4"], wq["s2"], wq["z"], wq["s1"], 128, want_acc=False)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / max(1, args.steps)
+    value = 2.0 * M * n_sample * K / dt / 1e12
+    sample = f"per step: act-quant of {M} tokens + GEMM over {n_sample} of {N} output channels, K={K}"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int64", "data": "synthetic",
+        "config": config_dict(c),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_dict(c: dict, extra: dict | None = None) -> dict:
+    d = {"workload": c["name"], "M": c["M"], "N": c["N"], "K": c["K"], "g": 128, "seed": c["seed"]}
+    if extra:
+        d.update(extra)
+    return d
+
+
+# ------------------------------------------------------------------ GPU arm --
+
+def run_ours(args, c: dict) -> None:
+    import torch
+
+    import w4a8_quantized_serving_gb300 as q
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist  # noqa: F811
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    M, N, K = c["M"], c["N"], c["K"]
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+
+    # weights: generated once, packed on the GPU (timed separately), cloned into a pool
+    W = torch.from_numpy(synth.weights(N, K, c["seed"])).to(dev)
+    X = torch.from_numpy(synth.activations(M, K, c["seed"] + rank)).to(dev)
+    packed, s1 = q.qoq_pack_weights(W)
+    torch.cuda.synchronize()
+    pk_ev0, pk_ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    pk_ev0.record()
+    for _ in range(3):
+        q.qoq_pack_weights(W, packed=packed, s1=s1)
+    pk_ev1.record()
+    torch.cuda.synchronize()
+    pack_ms = pk_ev0.elapsed_time(pk_ev1) / 3
+    del W
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    ws_bytes = q.qoq_gemm_workspace_bytes(M, N, K)
+    set_bytes = packed.numel() + 2 * N + 2 * M * K + M * K + 2 * M + 2 * M * N + ws_bytes
+    nsets = max(2, int(np.ceil(3 * l2 / set_bytes)))
+    sets = []
+    for i in range(nsets):
+        sets.append(dict(
+            packed=packed.clone(), s1=s1.clone(), X=X.clone(),
+            Xq=torch.empty((M, K), dtype=torch.int8, device=dev),
+            sx=torch.empty(M, dtype=torch.float16, device=dev),
+            Y=torch.empty((M, N), dtype=torch.float16, device=dev),
+            ws=torch.empty(ws_bytes, dtype=torch.uint8, device=dev)))
+    del packed, s1
+
+    def step(i: int, ev=None):
+        s = sets[i % nsets]
+        q.qoq_quant_act(s["X"], Xq=s["Xq"], sx=s["sx"])
+        if ev is not None:
+            ev[0].record()
+        q.qoq_w4a8_gemm(s["Xq"], s["sx"], s["packed"], s["s1"], N, Y=s["Y"], workspace=s["ws"])
+        if ev is not None:
+            ev[1].record()
+
+    for i in range(max(3, args.warmup)):
+        step(i)
+    torch.cuda.synchronize()
+    st = q.qoq_last_device_status(sets[0]["ws"])
+    if st != 0:
+        raise SystemExit(f"device status after warm-up: {q.qoq_status_str(st)}")
+
+    # ---- timed region: K steps
+    sampler = ClockSampler(local)
+    sampler.start()
+    gemm_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(args.steps):
+        step(i, gemm_ev[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+    ms_total = t0.elapsed_time(t1)
+    gemm_ms = statistics.mean(a.elapsed_time(b) for a, b in gemm_ev)
+    for s in sets:
+        st = q.qoq_last_device_status(s["ws"])
+        if st != 0:
+            raise SystemExit(f"device status: {q.qoq_status_str(st)}")
+
+    # ---- end to end through the public API with host buffers
+    Xh = torch.empty((M, K), dtype=torch.float16, pin_memory=True)
+    Xh.copy_(X.cpu())
+    Yh = [torch.empty((M, N), dtype=torch.float16, pin_memory=True) for _ in range(2)]
+    e_steps = args.steps
+
+    def e2e_step(i: int):
+        s = sets[i % nsets]
+        s["X"].copy_(Xh, non_blocking=True)
+        q.qoq_quant_act(s["X"], Xq=s["Xq"], sx=s["sx"])
+        q.qoq_w4a8_gemm(s["Xq"], s["sx"], s["packed"], s["s1"], N, Y=s["Y"], workspace=s["ws"])
+        Yh[i % 2].copy_(s["Y"], non_blocking=True)
+
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(e_steps):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e_steps
+
+    ms_per_step = ms_total / args.steps
+    if dist:
+        tt = torch.tensor([ms_per_step, e2e_ms, gemm_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_per_step, e2e_ms, gemm_ms = (float(v) for v in tt.tolist())
+
+    ops = 2.0 * M * N * K
+    nbytes = algorithmic_bytes(M, N, K)
+    value = world * ops / (ms_per_step * 1e-3) / 1e12
+    peaks, peak_src = load_peaks()
+    intensity = ops / nbytes["gemm"]
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if intensity < ridge:
+        achieved = nbytes["gemm"] / (gemm_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": args.traffic,
+                "peak_source": f"{peak_src} hbm_gbs (copy bandwidth)"}
+    else:
+        achieved = ops / (gemm_ms * 1e-3) / 1e12
+        pk = peaks["bf16_tflops_sustained"] if args.steps * gemm_ms > 1000 else peaks["bf16_tflops"]
+        roof = {"bound": "tensor", "achieved": achieved, "peak": pk, "unit": "TFLOP/s",
+                "frac": achieved / pk, "traffic": args.traffic,
+                "peak_source": f"{peak_src} bf16 dense (fp16 operands run at the bf16 rate)"}
+    roof["kernel"] = "qoq_w4a8_gemm call (B-operand convert + GEMM kernel)"
+    roof["algorithmic_bytes_per_launch"] = nbytes["gemm"]
+    roof["ms_per_launch"] = gemm_ms
+    roof["gb_per_s_algorithmic"] = nbytes["gemm"] / (gemm_ms * 1e-3) / 1e9
+    roof["tops_effective"] = ops / (gemm_ms * 1e-3) / 1e12
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int8",
+        "data": "synthetic (seeded splitmix64 Gaussians with outlier channels)",
+        "config": config_dict(c, {
+            "parallelism": f"replicas{world}" if world > 1 else "single",
+            "l2_policy": f"rotating pool of {nsets} buffer sets, {nsets * set_bytes / 1e6:.0f} MB "
+                         f"(>= 3x L2 {l2 / 1e6:.0f} MB)",
+            "step": "qoq_quant_act + qoq_w4a8_gemm",
+            "mma": "tcgen05 kind::f16, exact integer operands, fp32 TMEM folded to int32"}),
+        "hbm_gb_per_s_step": world * nbytes["step"] / (ms_per_step * 1e-3) / 1e9,
+        "roofline": roof,
+        "e2e": {"value": world * ops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": 2 * M * K, "d2h_bytes_per_step": 2 * M * N,
+                "ms_per_step": e2e_ms},
+        "clocks": clocks,
+        "gpu_launches": 3 * args.steps,
+        "pack_ms": pack_ms,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = oracle_step_timing(c, budget_s=args.cpu_budget,
+                                                  n_sample=None if N * M * K <= 2 ** 31 else 2048)
+    elif rank == 0:
+        line["cpu_baseline"] = None
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main() -> None:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=1, help="workload index 0..4 (default 1)")
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle CPU timing")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per GEMM launch from an ncu capture of this build, if known")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    c = synth.WORKLOADS[args.config]
+    if args.impl == "reference":
+        run_reference(args, c)
+    else:
+        run_ours(args, c)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,179 @@
+/*
+ * qoq.h -- C ABI of the GB300 (sm_103a) W4A8 g128 linear layer of QServe's
+ * QoQ scheme: progressive group quantization of the weights, per-token int8
+ * activations, and the integer GEMM with an fp16 epilogue.
+ *
+ * Sources (web pages on W4A8 serving):
+ *  [QS]  QServe talk write-up (greptalks.ai, MLSys'25), "Technical Deep Dive":
+ *        sections "Progressive Group Quantization for W4A8 GEMM", "Precision
+ *        Data Flow and Activation Quantization Fusion", "Quantized Matrix
+ *        Multiplication (GEMM) Kernel on GPUs" and "Challenges and Design
+ *        Details of QServe GEMM Kernel".
+ *  [L15] Lecture 15 notes (cs2680), section 15.6 "QServe: W4A8KV4, and paying
+ *        for dequant once", and section 15.5 "The kernel trap".
+ *  [QF]  QFactory notes (papercache.org), section 2 (dequantization
+ *        w = (w_quant - zero) * scale) and Fig. 3.
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers on the current CUDA device; the
+ *    caller allocates and owns every buffer (including the workspace).  The
+ *    library allocates no device memory and keeps no state beyond a cached
+ *    per-device attribute lookup and the debug settings below.
+ *  - fp16 values cross the ABI as their IEEE binary16 bit patterns (uint16_t).
+ *  - Matrices are dense row-major.  W is [N][K] (row n = output channel),
+ *    X / Xq are [M][K] (row m = token), Y is [M][N]: Y = X * W^T.
+ *  - Every compute call is asynchronous on `stream` (a cudaStream_t; NULL is
+ *    the legacy default stream).  Only qoq_last_device_status synchronizes.
+ *  - Argument checks happen on the host before any launch and return an error
+ *    code without touching the device; launch failures return QOQ_ERR_CUDA.
+ *    The library never aborts, prints or throws across this boundary.
+ *  - Requirements shared by the compute calls: g == 128 (else
+ *    QOQ_ERR_UNSUPPORTED); N % 128 == 0 and K % 128 == 0 (else QOQ_ERR_SHAPE);
+ *    1 <= M <= 2^24, 128 <= N <= 2^24, 128 <= K <= 131072 (the int32
+ *    accumulator bound 127 * 127 * K < 2^31); pointers 16-byte aligned
+ *    (else QOQ_ERR_MISALIGNED); a compute capability 10.3 device (else
+ *    QOQ_ERR_ARCH).
+ */
+#ifndef QOQ_H
+#define QOQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* qoq_stream_t;
+
+typedef enum {
+  QOQ_OK = 0,
+  QOQ_ERR_NULL = 1,          /* a required pointer is NULL */
+  QOQ_ERR_SHAPE = 2,         /* M, N or K out of range or not a multiple of 128 */
+  QOQ_ERR_UNSUPPORTED = 3,   /* group size other than 128 */
+  QOQ_ERR_MISALIGNED = 4,    /* a pointer is not 16-byte aligned */
+  QOQ_ERR_WORKSPACE = 5,     /* workspace NULL or smaller than qoq_gemm_workspace_bytes */
+  QOQ_ERR_CUDA = 6,          /* a CUDA runtime call or kernel launch failed */
+  QOQ_ERR_DEVICE_TIMEOUT = 7, /* a device-side pipeline wait ran out (see qoq_last_device_status) */
+  QOQ_ERR_ARCH = 8           /* current device is not compute capability 10.3 (GB300) */
+} qoq_status;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* qoq_status_str(int status);
+
+/* ABI version of this library (major * 100 + minor). */
+int qoq_version(void);
+
+/*
+ * Bytes of the packed weight blob for an [N][K] weight at group size g
+ * (host-only, no device access).  Returns 0 for an unsupported shape.
+ *
+ * Layout ([QS] "compute-aware weight reordering": weights are stored in the
+ * order the GEMM consumes them, so one contiguous copy serves one pipeline
+ * stage): (N/128) x (K/128) tiles of 8448 bytes, tile (nt, j) at offset
+ * (nt * (K/128) + j) * 8448, each holding output rows 128*nt .. 128*nt+127
+ * and input channels 128*j .. 128*j+127:
+ *   bytes    0..127 : s2[r], the level-2 integer scale of row r (1..16)
+ *   bytes  128..255 : z[r],  the level-2 zero point of row r (0..15)
+ *   bytes 256..8447 : four 2048-byte chunks c = 0..3 (k = 32c .. 32c+31);
+ *                     chunk c holds row r's 16 bytes at offset 16 r; inside,
+ *                     32-bit word w (k = 32c + 8w .. +7) carries the code of
+ *                     k = 32c + 8w + 2i in bits 4i..4i+3 and that of
+ *                     k = 32c + 8w + 2i + 1 in bits 16+4i..16+4i+3 (i = 0..3).
+ * That is 4 + 16/128 bits per weight plus the fp16 s1 per row.
+ */
+size_t qoq_packed_weight_bytes(int N, int K, int g);
+
+/*
+ * Bytes of device workspace that qoq_w4a8_gemm needs for (M, N, K, g)
+ * (host-only; 0 for an unsupported shape).  It holds a status header, the
+ * split-K partial sums and tile counters, and an fp16 copy of Xq laid out
+ * for the tensor-core B operand.  The workspace needs no initialisation and
+ * is rewritten by every call; two calls in flight at the same time must not
+ * share one.
+ */
+size_t qoq_gemm_workspace_bytes(int M, int N, int K, int g);
+
+/*
+ * Offline weight preparation ([QS] "Progressive Group Quantization for W4A8
+ * GEMM"; [L15] 15.6), one call per layer:
+ *   level 1, per output channel n (symmetric, protective range):
+ *     s1[n] = fp16_rn(fp32(max_k |W[n,k]|) / 119)   (IEEE fp32 divide),
+ *     Q8[n,k] = clamp(rint(W[n,k] / s1[n]), -119, 119) (fp32 divide, ties even);
+ *     an all-zero row, or one whose s1 underflows to 0, gets s1 = 0, Q8 = 0;
+ *   level 2, per group of 128 input channels (asymmetric uint4):
+ *     lo = min(0, min Q8), hi = max(0, max Q8),
+ *     s2 = max(1, ceil((hi - lo) / 15)), z = rne(-lo / s2),
+ *     q4 = clamp(rne(Q8 / s2) + z, 0, 15)   (exact integer, ties to even),
+ *   so that w8 = (q4 - z) * s2 ([QF] dequantization) lies in [-127, 127].
+ * In:  W_f16 [N][K] fp16 bits.
+ * Out: packed, qoq_packed_weight_bytes(N, K, g) bytes in the layout above;
+ *      s1_f16 [N] fp16 bits.
+ */
+qoq_status qoq_pack_weights(int N, int K, int g, const uint16_t* W_f16, uint8_t* packed,
+                            uint16_t* s1_f16, qoq_stream_t stream);
+
+/*
+ * Per-token symmetric int8 activation quantization ([QS] "Precision Data
+ * Flow": every linear layer takes 8-bit activations):
+ *   s_x[m] = fp16_rn(fp32(max_k |X[m,k]|) / 127),
+ *   Xq[m,k] = clamp(rint(X[m,k] / s_x[m]), -127, 127) (fp32 divide, ties even);
+ *   an all-zero row gets s_x = 0, Xq = 0.
+ * In:  X_f16 [M][K] fp16 bits.  Out: Xq [M][K] int8, sx_f16 [M] fp16 bits.
+ * Shape rules as above except that N and g are not involved.
+ */
+qoq_status qoq_quant_act(int M, int K, const uint16_t* X_f16, int8_t* Xq, uint16_t* sx_f16,
+                         qoq_stream_t stream);
+
+/*
+ * The W4A8 GEMM ([QS] "Quantized Matrix Multiplication (GEMM) Kernel on
+ * GPUs": 4-bit weights are dequantized to 8 bits before the tensor cores,
+ * the per-channel scales are applied in the epilogue):
+ *   acc[m,n] = sum_k Xq[m,k] * ((q4[n,k] - z[n,k/128]) * s2[n,k/128])  (exact int32),
+ *   Y[m,n]   = fp16_rn(float(acc[m,n]) * (float(s_x[m]) * float(s1[n]))).
+ * In:  Xq [M][K] int8 and sx_f16 [M] (from qoq_quant_act); packed and s1_f16
+ *      (from qoq_pack_weights).
+ * Out: Y_f16 [M][N] fp16 bits; acc_debug [M][N] int32 when not NULL.
+ * workspace: ws_bytes >= qoq_gemm_workspace_bytes(M, N, K, g), 16-byte
+ *      aligned, owned by the caller, used by one call at a time.
+ * A device-side pipeline stall that exceeds the wait limit ends the kernel
+ * early, leaves Y undefined and records QOQ_ERR_DEVICE_TIMEOUT in the
+ * workspace header, which qoq_last_device_status returns.
+ */
+qoq_status qoq_w4a8_gemm(int M, int N, int K, int g, const int8_t* Xq, const uint16_t* sx_f16,
+                         const uint8_t* packed, const uint16_t* s1_f16, uint16_t* Y_f16,
+                         int32_t* acc_debug, void* workspace, size_t ws_bytes,
+                         qoq_stream_t stream);
+
+/*
+ * Inverse of the packing layout, for testing: recovers the logical codes.
+ * Out: q4 [N][K] (one code per byte), s2 [N][K/g], z [N][K/g].
+ */
+qoq_status qoq_unpack_weights_debug(int N, int K, int g, const uint8_t* packed, uint8_t* q4,
+                                    uint8_t* s2, uint8_t* z, qoq_stream_t stream);
+
+/*
+ * Synchronizes `stream`, then reads and clears the device status that the
+ * most recent qoq_w4a8_gemm call on `workspace` recorded (each call resets it
+ * on the device before its GEMM kernel starts).  Returns QOQ_OK,
+ * QOQ_ERR_DEVICE_TIMEOUT, or QOQ_ERR_CUDA (a CUDA error surfaced by the
+ * synchronization, e.g. a failed kernel).
+ */
+qoq_status qoq_last_device_status(void* workspace, qoq_stream_t stream);
+
+/*
+ * Test hooks (process-wide, not thread-safe; leave at defaults in production).
+ * wait_timeout_ns: limit of every device-side pipeline wait (0 = default, 2 s).
+ * fault: 0 = none; 1 = the GEMM's copy producer skips one pipeline stage, so
+ * that the waits downstream of it run out and the kernel returns with
+ * QOQ_ERR_DEVICE_TIMEOUT recorded (no trap, no invalid access).
+ */
+qoq_status qoq_set_debug(uint64_t wait_timeout_ns, int fault);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QOQ_H */

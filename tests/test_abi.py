@@ -1,0 +1,132 @@
+"""The C-ABI library: loads, exports what include/qoq.h declares, validates
+arguments on the host before any device access (CPU only, no compute)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import w4a8_quantized_serving_gb300 as q
+from w4a8_quantized_serving_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qoq.h")
+FAKE = 0x7F0000001000  # 16-byte aligned, never dereferenced: every call below fails validation first
+MIS = FAKE + 8
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(qoq_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("qoq_pack_weights", "qoq_quant_act", "qoq_w4a8_gemm", "qoq_packed_weight_bytes",
+                 "qoq_gemm_workspace_bytes", "qoq_last_device_status", "qoq_unpack_weights_debug"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol():
+    L = q.lib()
+    for name in declared_functions():
+        assert hasattr(L, name), name
+    assert set(binding.EXPORTED) <= set(declared_functions())
+
+
+def test_library_is_built_for_sm103a():
+    out = os.popen(f"cuobjdump --list-elf {q.library_path()} 2>/dev/null").read()
+    if not out:
+        pytest.skip("cuobjdump unavailable")
+    assert "sm_103a" in out
+
+
+def test_status_strings_and_version():
+    assert q.qoq_version() >= 100
+    for code, name in binding.QOQ_ERRORS.items():
+        assert q.qoq_status_str(code) == name
+    assert q.qoq_status_str(99) == "QOQ_ERR_UNKNOWN"
+
+
+def test_packed_weight_bytes_closed_form():
+    # 4 bits per code plus one uint8 scale and one uint8 zero per 128-channel group:
+    # 4 + 16/128 bits per weight (lecture 15: 4 + 16/128 = 4.125 effective bits)
+    for N, K in [(128, 128), (256, 512), (12288, 4096), (28672, 8192)]:
+        nb = q.qoq_packed_weight_bytes(N, K, 128)
+        assert nb == N * K // 2 + 2 * N * (K // 128)
+        assert nb * 8 / (N * K) == pytest.approx(4.125)
+    assert q.qoq_packed_weight_bytes(100, 128, 128) == 0
+    assert q.qoq_packed_weight_bytes(128, 128, 64) == 0
+
+
+def test_workspace_bytes_host_pure_and_monotone():
+    for (M, N, K) in [(8, 256, 512), (16, 12288, 4096), (128, 22016, 4096), (256, 4096, 14336),
+                      (4096, 28672, 8192)]:
+        ws = q.qoq_gemm_workspace_bytes(M, N, K, 128)
+        assert ws > 0 and ws % 256 == 0
+        # holds at least the fp16 copy of the activations
+        assert ws >= 2 * M * K
+    assert q.qoq_gemm_workspace_bytes(0, 128, 128, 128) == 0
+    assert q.qoq_gemm_workspace_bytes(1, 128, 131072 + 128, 128) == 0
+
+
+L = None
+
+
+def _lib():
+    return q.lib()
+
+
+def test_quant_act_validation():
+    L = _lib()
+    assert L.qoq_quant_act(16, 4096, None, FAKE, FAKE, None) == 1
+    assert L.qoq_quant_act(0, 4096, FAKE, FAKE, FAKE, None) == 2
+    assert L.qoq_quant_act(16, 100, FAKE, FAKE, FAKE, None) == 2
+    assert L.qoq_quant_act(16, 4096, MIS, FAKE, FAKE, None) == 4
+
+
+def test_pack_validation():
+    L = _lib()
+    assert L.qoq_pack_weights(128, 256, 128, FAKE, None, FAKE, None) == 1
+    assert L.qoq_pack_weights(128, 256, 64, FAKE, FAKE, FAKE, None) == 3
+    assert L.qoq_pack_weights(100, 256, 128, FAKE, FAKE, FAKE, None) == 2
+    assert L.qoq_pack_weights(128, 256, 128, FAKE, MIS, FAKE, None) == 4
+
+
+def test_gemm_validation():
+    L = _lib()
+    ws = q.qoq_gemm_workspace_bytes(16, 256, 512)
+    args = dict(M=16, N=256, K=512, g=128)
+
+    def call(M=16, N=256, K=512, g=128, Xq=FAKE, sx=FAKE, pk=FAKE, s1=FAKE, Y=FAKE, acc=None, w=FAKE,
+             wb=ws):
+        return L.qoq_w4a8_gemm(M, N, K, g, Xq, sx, pk, s1, Y, acc, w, wb, None)
+
+    assert call(Xq=None) == 1
+    assert call(Y=None) == 1
+    assert call(g=32) == 3
+    assert call(N=200) == 2
+    assert call(K=131072 + 128) == 2
+    assert call(M=0) == 2
+    assert call(pk=MIS) == 4
+    assert call(acc=MIS) == 4
+    assert call(wb=ws - 1) == 5
+    assert call(w=None) == 5
+    assert call(w=MIS) == 4
+
+
+def test_unpack_and_status_validation():
+    L = _lib()
+    assert L.qoq_unpack_weights_debug(128, 256, 128, None, FAKE, FAKE, FAKE, None) == 1
+    assert L.qoq_unpack_weights_debug(128, 256, 96, FAKE, FAKE, FAKE, FAKE, None) == 3
+    assert L.qoq_last_device_status(None, None) == 1
+    assert L.qoq_set_debug(0, 5) == 3
+    assert L.qoq_set_debug(0, 0) == 0
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(binding, "_LIB", None)
+    monkeypatch.setattr(binding._build, "LIB", str(tmp_path / "missing.so"))
+    with pytest.raises(binding.QoQError):
+        binding.lib()

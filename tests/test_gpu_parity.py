@@ -1,0 +1,210 @@
+"""CUDA path vs the oracle, element by element, on seeded inputs (GPU).
+
+Integer outputs (Xq, s_x, q4, s2, z, s1, the int32 accumulators) must be
+bit-exact; fp16 Y within |dY| <= 2e-3 |Y_ref| or |dY| <= 1e-2.
+"""
+import numpy as np
+import pytest
+
+from tests import gpu_cases as gc
+from tests.conftest import gpu_available
+from tests.oracle_pins import f16, load_golden
+from w4a8_quantized_serving_gb300 import synth
+
+pytestmark = [pytest.mark.gpu, pytest.mark.skipif(not gpu_available(), reason="needs a CUDA GPU")]
+
+
+def q():
+    import w4a8_quantized_serving_gb300 as mod
+
+    return mod
+
+
+def _edge_rows(K: int, seed: int) -> np.ndarray:
+    rng = np.random.default_rng(seed)
+    rows = [
+        np.zeros(K), np.full(K, 0.5), np.full(K, -3.0), np.linspace(-2, 2, K),
+        np.where(np.arange(K) % 2 == 0, 1.0, -1.0), rng.standard_normal(K) * 1e-6,
+        np.where(np.arange(K) == 7, 60000.0, 0.0), rng.standard_normal(K) * 30.0,
+    ]
+    return f16(np.stack(rows))
+
+
+# ------------------------------------------------------------------ act quant --
+
+@pytest.mark.parametrize("M,K", [(1, 128), (7, 256), (8, 512), (16, 4096), (129, 384), (33, 8192)])
+def test_act_quant_bit_exact(M, K):
+    X = synth.activations(M, K, 100 + M)
+    if M >= 8:
+        X[:8] = _edge_rows(K, M)
+    Xd = gc.to_dev_f16(X)
+    Xq, sx = q().qoq_quant_act(Xd)
+    oXq, osx = gc.oracle.act_quant(synth.bits(X))
+    assert np.array_equal(Xq.cpu().numpy(), oXq)
+    assert np.array_equal(gc.f16_bits(sx), osx)
+
+
+# ---------------------------------------------------------------------- pack --
+
+@pytest.mark.parametrize("N,K", [(128, 128), (256, 512), (384, 1152), (128, 8192)])
+def test_pack_bit_exact_and_layout(N, K):
+    W = synth.weights(N, K, 200 + N)
+    W[:8] = _edge_rows(K, N) * 0.01
+    Wd = gc.to_dev_f16(W)
+    packed, s1 = q().qoq_pack_weights(Wd)
+    o = gc.oracle.weight_quant(synth.bits(W), 128)
+    gc.check_weights(q(), dict(packed=packed, s1=s1), o, N, K)
+    # the blob itself follows the documented layout
+    want = gc.pack_reference_layout(o["q4"], o["s2"], o["z"])
+    assert np.array_equal(packed.cpu().numpy()[:want.size], want)
+
+
+# ---------------------------------------------------------------------- GEMM --
+
+def _run_full(M, N, K, seed, W=None, X=None):
+    if W is None:
+        W = synth.weights(N, K, seed)
+    if X is None:
+        X = synth.activations(M, K, seed)
+    g = gc.gpu_layer(W, X)
+    o = gc.oracle_layer(W, X)
+    gc.check_weights(q(), g, o, N, K)
+    gc.check_acts(g, o)
+    acc = g["acc"].cpu().numpy()
+    assert np.array_equal(acc.astype(np.int64), o["acc"]), \
+        f"acc mismatch at {np.argwhere(acc != o['acc'])[:5].tolist()}"
+    ok, rel, ab = gc.y_close(gc.f16_bits(g["Y"]), o["Y"])
+    assert ok, (rel, ab)
+    return g, o
+
+
+def test_gemm_appendix_example_g128():
+    gold = load_golden("appendix_a_g4.txt")
+    K = 256
+    Wl = np.zeros(K)
+    Xl = np.zeros(K)
+    for j in range(2):
+        Wl[128 * j:128 * j + 4] = np.array(gold["Q8"][4 * j:4 * j + 4]) * 2.0 ** -7
+        Xl[128 * j:128 * j + 4] = np.array(gold["Xq"][4 * j:4 * j + 4]) * 2.0 ** -6
+    W = np.repeat(f16(Wl).reshape(1, K), 128, axis=0)
+    X = f16(Xl).reshape(1, K)
+    g, o = _run_full(1, 128, K, 0, W=W, X=X)
+    assert (g["acc"].cpu().numpy() == gold["acc"]).all()
+    assert (gc.f16_bits(g["Y"]) == gold["Y_bits"]).all()
+
+
+def test_gemm_config0_tiny():
+    c = synth.WORKLOADS[0]
+    _run_full(c["M"], c["N"], c["K"], c["seed"])
+
+
+@pytest.mark.parametrize("M", [1, 7, 15, 16, 17, 32, 33, 64, 65, 128, 129, 200])
+def test_gemm_token_counts(M):
+    # 9 groups: crosses the 8-group fp32 -> int32 fold boundary
+    _run_full(M, 384, 1152, 300 + M)
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 128, 4096), (64, 1024, 2048), (128, 2048, 1024), (5, 128, 16384)])
+def test_gemm_split_k_shapes(M, N, K):
+    _run_full(M, N, K, 400 + M)
+
+
+@pytest.mark.parametrize("K", [1024, 8192])
+def test_gemm_worst_case_magnitudes(K):
+    """All codes at their extremes: every chunk's fp32 partial sums reach the
+    largest values the format allows (127 * 120 * 1024 < 2^24)."""
+    M, N = 16, 256
+    W = np.full((N, K), np.float16(1.0))
+    W[1::2] = np.float16(-1.0)  # Q8 = -119: group [-119, 0] -> w8 = -120
+    X = np.full((M, K), np.float16(2.0))
+    X[1::2] = np.float16(-2.0)
+    g, o = _run_full(M, N, K, 0, W=W, X=X)
+    assert int(np.abs(o["acc"]).max()) == 127 * 120 * K
+
+
+def test_gemm_max_k():
+    """K = 131072, the largest K the int32 accumulator admits."""
+    M, N, K = 2, 128, 131072
+    W = np.full((N, K), np.float16(0.5))
+    X = np.full((M, K), np.float16(0.25))  # Xq = 127; Y stays within the fp16 range
+    g, o = _run_full(M, N, K, 0, W=W, X=X)
+    assert int(o["acc"].max()) == 127 * 120 * K
+
+
+def test_gemm_zero_inputs():
+    M, N, K = 4, 128, 256
+    W = synth.weights(N, K, 9)
+    X = np.zeros((M, K), np.float16)
+    g, o = _run_full(M, N, K, 0, W=W, X=X)
+    assert (g["acc"].cpu().numpy() == 0).all()
+
+
+def test_gemm_deterministic_and_workspace_reuse():
+    M, N, K = 24, 512, 3072
+    W = synth.weights(N, K, 51)
+    X = synth.activations(M, K, 51)
+    g1 = gc.gpu_layer(W, X)
+    g2 = gc.gpu_layer(W, X, ws=g1["ws"])
+    assert np.array_equal(g1["acc"].cpu().numpy(), g2["acc"].cpu().numpy())
+    assert np.array_equal(gc.f16_bits(g1["Y"]), gc.f16_bits(g2["Y"]))
+
+
+# ------------------------------------------------------- full-size workloads --
+
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4])
+def test_gemm_workload_sampled(cfg):
+    """Full-size workloads in the benchmark's launch configuration: bit-exact
+    quantization outputs, and the GEMM on sampled entries the oracle computes
+    one by one."""
+    c = synth.WORKLOADS[cfg]
+    M, N, K = c["M"], c["N"], c["K"]
+    W = synth.weights(N, K, c["seed"])
+    X = synth.activations(M, K, c["seed"])
+    g = gc.gpu_layer(W, X)
+    o = gc.oracle_layer(W, X, full_gemm=False)
+    gc.check_weights(q(), g, o, N, K)
+    gc.check_acts(g, o)
+    rng = np.random.default_rng(cfg)
+    ns = 3000
+    mi = np.concatenate([rng.integers(0, M, ns), np.full(N // 128, M - 1), np.zeros(64, np.int64)])
+    ni = np.concatenate([rng.integers(0, N, ns), np.arange(0, N, 128) + 127, np.arange(64)])
+    acc_ref, y_ref = gc.oracle.gemm_entries(mi, ni, o["Xq"], o["sx"], o["q4"], o["s2"], o["z"], o["s1"])
+    acc = g["acc"].cpu().numpy()[mi, ni]
+    Y = gc.f16_bits(g["Y"])[mi, ni]
+    assert np.array_equal(acc.astype(np.int64), acc_ref)
+    ok, rel, ab = gc.y_close(Y, y_ref)
+    assert ok, (rel, ab)
+
+
+# ------------------------------------------------------- failure detection --
+
+def test_device_wait_timeout_is_reported_and_context_survives():
+    """A producer that skips one pipeline stage (test hook) makes the waits
+    downstream run out after a short limit; the kernel returns, the status
+    reads QOQ_ERR_DEVICE_TIMEOUT, and the next call is correct."""
+    mod = q()
+    t = gc.torch()
+    M, N, K = 16, 128 * 152, 8192
+    W = synth.weights(N, K, 61)
+    X = synth.activations(M, K, 61)
+    Wd, Xd = gc.to_dev_f16(W), gc.to_dev_f16(X)
+    packed, s1 = mod.qoq_pack_weights(Wd)
+    Xq, sx = mod.qoq_quant_act(Xd)
+    ws = t.empty(mod.qoq_gemm_workspace_bytes(M, N, K), dtype=t.uint8, device="cuda")
+    try:
+        mod.qoq_set_debug(5_000_000, 1)  # 5 ms wait limit, skip one stage
+        mod.qoq_w4a8_gemm(Xq, sx, packed, s1, N, workspace=ws)
+        assert mod.qoq_last_device_status(ws) == 7
+    finally:
+        mod.qoq_set_debug(0, 0)
+    acc = t.empty((M, N), dtype=t.int32, device="cuda")
+    mod.qoq_w4a8_gemm(Xq, sx, packed, s1, N, acc_debug=acc, workspace=ws)
+    assert mod.qoq_last_device_status(ws) == 0
+    # the oracle quantizes rows independently: only the sampled rows are needed
+    rows = np.arange(0, N, N // 8)
+    o = gc.oracle.weight_quant(synth.bits(W[rows]), 128)
+    oXq, osx = gc.oracle.act_quant(synth.bits(X))
+    mi = np.arange(0, M).repeat(len(rows))
+    ni = np.tile(np.arange(len(rows)), M)
+    acc_ref, _ = gc.oracle.gemm_entries(mi, ni, oXq, osx, o["q4"], o["s2"], o["z"], o["s1"])
+    assert np.array_equal(acc.cpu().numpy()[mi, rows[ni]].astype(np.int64), acc_ref)

@@ -1,0 +1,564 @@
+// gemm.cu -- the W4A8 g128 GEMM on sm_103a tensor cores.
+//
+// Computes, for Xq [M][K] int8 (per-token scale s_x) and the packed weights
+// (level-2 codes q4, integer scale s2, zero z per 128-channel group; level-1
+// fp16 scale s1 per output channel):
+//   acc[m,n] = sum_k Xq[m,k] * ((q4[n,k] - z[n,k/128]) * s2[n,k/128])   (exact)
+//   Y[m,n]   = fp16_rn(float(acc) * (float(s_x[m]) * float(s1[n])))
+// QServe talk write-up, "Quantized Matrix Multiplication (GEMM) Kernel on
+// GPUs" and "Challenges and Design Details": the 4-bit weights are
+// dequantized to 8-bit integers before the tensor cores (never partial-sum
+// dequant), the main loop is tensor-core work only, and the per-channel
+// scales go to the epilogue.  Lecture 15 notes, section 15.5: the dequant
+// instruction count per weight is what decides whether the weight stream can
+// reach the HBM floor.
+//
+// sm_103a has no integer tcgen05 MMA, so the exact int8 x int8 product runs on
+// tcgen05.mma kind::f16: both operands are small integers (|v| <= 127), exact
+// in fp16; each product (<= 16129) and each partial sum below 2^24 is exact in
+// the fp32 accumulator, and the epilogue folds the fp32 TMEM partials into
+// int32 registers every 8 groups (1024 channels, 127*127*1024 < 2^24).
+//
+// Data path per CTA (one persistent CTA per SM, warp-specialised):
+//   warp 0      producer: per 128-channel group, one bulk copy of the packed
+//               weight tile (8448 B) and one of the fp16 activation tile
+//               (pre-swizzled, 128B-swizzle K-major) into an S-stage ring.
+//   warps 2..   dequant: thread r owns weight row r of the tile; it expands its
+//               64 code bytes to 128 fp16 values (q4 - z) * s2 with two packed
+//               fp16 ops per pair (exact) and stores them straight into tensor
+//               memory (tcgen05.st), which is the MMA's A operand: dequantized
+//               weights never touch shared memory.
+//   warp 1      MMA issuer: 8 x tcgen05.mma (M=128, N=BN, K=16) per group,
+//               A from TMEM, B from shared memory, D in one of two TMEM
+//               accumulators (double-buffered per 8-group fold chunk).
+//   last 4      epilogue: fold fp32 partials to int32, then either write Y
+//               (whole-K tiles) or add int32 partials into the workspace
+//               (split-K tiles; the last contributor writes Y).
+// Every mbarrier wait is bounded (globaltimer); on expiry the CTA records
+// QOQ_ERR_DEVICE_TIMEOUT in the workspace header, drains its copies and MMAs,
+// frees its tensor memory and returns.
+#include <cuda_fp16.h>
+
+#include <algorithm>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace qoq {
+namespace {
+
+constexpr int kTmemCols = 512;
+constexpr int kACol0 = 256;  // A buffers live at TMEM columns 256 + 64 a
+constexpr int kABufs = 4;
+constexpr int kStatusTimeout = 7;  // QOQ_ERR_DEVICE_TIMEOUT
+
+template <int BN>
+struct Cfg {
+  static constexpr int NDQ = BN <= 64 ? 8 : 4;  // dequant warps
+  static constexpr int NEPI = 4;                // epilogue warps (one per TMEM lane quadrant)
+  static constexpr int WARPS = 2 + NDQ + NEPI;
+  static constexpr int THREADS = WARPS * 32;
+  static constexpr int EPI_WARP0 = 2 + NDQ;
+  static constexpr int B_BYTES = BN * kGroup * 2;  // fp16 activation tile per group
+  static constexpr int STAGES = BN == 128 ? 5 : (BN == 64 ? 8 : (BN == 32 ? 12 : 16));
+  static constexpr int B_REGION = STAGES * B_BYTES;
+  static constexpr int W_REGION = STAGES * kWTileBytes;
+  static constexpr int BAR_OFF = B_REGION + W_REGION;
+  static constexpr int NBARS = 2 * STAGES + 2 * kABufs + 4 + 1;
+  static constexpr int TMEM_SLOT_OFF = BAR_OFF + NBARS * 8;
+  static constexpr int FLAG_OFF = TMEM_SLOT_OFF + 8;
+  static constexpr int SMEM_BYTES = FLAG_OFF + 8 + 1024;  // + slack for 1024-B alignment
+  // tcgen05 instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B
+  // fp16 (bits 7-9, 10-12 = 0), both K-major (bits 15, 16 = 0),
+  // N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+  static constexpr uint32_t IDESC =
+      (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(kTileN >> 4) << 24);
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
+  static_assert(2 * BN <= kACol0, "accumulators overlap A buffers");
+  static_assert(B_BYTES % 1024 == 0, "128B-swizzle atoms need 1024-B alignment");
+  static_assert(SMEM_BYTES <= 232448, "shared memory");
+};
+
+// Shared-memory matrix descriptor: 128-byte swizzle, K-major, 8-row groups
+// 1024 B apart (SBO), version 1 (bit 46), layout code 2 (bits 61-63).
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+struct Unit {
+  int tile, g0, g1;
+};
+
+// The CTA's sequence of (tile, group range) units: whole tiles first, then
+// its stream-K range.  Every role walks the same sequence.
+struct UnitIter {
+  int dp_next;
+  long long it, it_end;
+  __device__ __forceinline__ void init(const GemmParams& p) {
+    dp_next = blockIdx.x;
+    it = (long long)blockIdx.x * p.I_sk / p.P;
+    it_end = (long long)(blockIdx.x + 1) * p.I_sk / p.P;
+  }
+  __device__ __forceinline__ bool next(const GemmParams& p, Unit& u) {
+    if (dp_next < p.T_dp) {
+      u.tile = dp_next;
+      u.g0 = 0;
+      u.g1 = p.G;
+      dp_next += p.P;
+      return true;
+    }
+    if (it < it_end) {
+      const long long sk = it / p.G;
+      const int g0 = (int)(it - sk * p.G);
+      const long long rem = it_end - it;
+      const long long g1 = rem < (long long)(p.G - g0) ? g0 + rem : (long long)p.G;
+      u.tile = p.T_dp + (int)sk;
+      u.g0 = g0;
+      u.g1 = (int)g1;
+      it += g1 - g0;
+      return true;
+    }
+    return false;
+  }
+};
+
+// Bounded wait on an mbarrier phase.  Returns false if the wait ran out (the
+// timeout is recorded) or, when honor_abort, if another thread already
+// recorded one for this call.
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const GemmParams& p,
+                                       bool honor_abort) {
+  volatile int* abort_flag = p.status + 1;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 15) == 0) {
+      if (honor_abort && *abort_flag) return false;
+      if (global_timer_ns() - t0 > p.timeout_ns) {
+        atomicExch(p.status, kStatusTimeout);
+        atomicExch(p.status + 1, 1);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const GemmParams& p,
+                                         bool honor_abort = true) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_slow(bar, parity, p, honor_abort);
+}
+
+__device__ __forceinline__ void epi_bar_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+template <int BN>
+__device__ __forceinline__ void write_tile_out(const GemmParams& p, const int32_t (&run)[BN], int mt,
+                                               int n) {
+  const float s1f = __half2float(__ushort_as_half(p.s1[n]));
+#pragma unroll
+  for (int i = 0; i < BN; ++i) {
+    const int m = mt * BN + i;
+    if (m < p.M) {
+      const float sxf = __half2float(__ushort_as_half(p.sx[m]));
+      const float y = (float)run[i] * (sxf * s1f);
+      p.Y[(size_t)m * p.N + n] = __half_as_ushort(__float2half_rn(y));
+      if (p.acc_debug) p.acc_debug[(size_t)m * p.N + n] = run[i];
+    }
+  }
+}
+
+template <int BN>
+__global__ void __launch_bounds__(Cfg<BN>::THREADS, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
+  using C = Cfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t sbase = smem_addr(smem);
+  const uint32_t bars = sbase + C::BAR_OFF;
+  const uint32_t bar_full = bars, bar_empty = bars + 8 * C::STAGES;
+  const uint32_t bar_afull = bars + 8 * (2 * C::STAGES), bar_aempty = bar_afull + 8 * kABufs;
+  const uint32_t bar_accfull = bar_aempty + 8 * kABufs, bar_accempty = bar_accfull + 16;
+  const uint32_t bar_drain = bar_accempty + 16;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1 + C::NDQ);
+    }
+    for (int a = 0; a < kABufs; ++a) {
+      mbar_init(bar_afull + 8 * a, C::NDQ);
+      mbar_init(bar_aempty + 8 * a, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_accfull + 8 * b, 1);
+      mbar_init(bar_accempty + 8 * b, C::NEPI);
+    }
+    mbar_init(bar_drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(sbase + C::TMEM_SLOT_OFF, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + C::TMEM_SLOT_OFF);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer --
+    if (lane == 0) {
+      const uint64_t pol_w = p.MT == 1 ? policy_evict_first() : policy_evict_last();
+      const uint64_t pol_x = policy_evict_last();
+      UnitIter iter;
+      iter.init(p);
+      Unit u;
+      bool have = iter.next(p, u);
+      int g = have ? u.g0 : 0;
+      uint32_t issued_mask = 0, issued_par = 0;  // per stage: last issue and its parity
+      auto w_src = [&](const Unit& uu, int gg) {
+        return p.packed + ((size_t)(uu.tile / p.MT) * p.G + gg) * kWTileBytes;
+      };
+      auto x_src = [&](const Unit& uu, int gg) {
+        return p.xh + ((size_t)(uu.tile % p.MT) * p.G + gg) * (C::B_BYTES / 2);
+      };
+      // Weights do not depend on the preceding kernel: start streaming them
+      // for the first ring's worth of groups before waiting on it.
+      int npre = 0;
+      int pre_tile[C::STAGES], pre_g[C::STAGES];
+      while (have && npre < C::STAGES) {
+        const int s = npre;
+        mbar_arrive_expect_tx(bar_full + 8 * s, kWTileBytes + C::B_BYTES);
+        bulk_g2s(sbase + C::B_REGION + s * kWTileBytes, w_src(u, g), kWTileBytes, bar_full + 8 * s, pol_w);
+        pre_tile[npre] = u.tile;
+        pre_g[npre] = g;
+        issued_mask |= 1u << s;
+        ++npre;
+        if (++g >= u.g1) {
+          have = iter.next(p, u);
+          if (have) g = u.g0;
+        }
+      }
+      grid_dep_wait();
+      for (int i = 0; i < npre; ++i) {
+        Unit uu{pre_tile[i], 0, 0};
+        bulk_g2s(sbase + i * C::B_BYTES, x_src(uu, pre_g[i]), C::B_BYTES, bar_full + 8 * i, pol_x);
+      }
+      uint32_t gi = npre;
+      while (have) {
+        const int s = gi % C::STAGES;
+        const uint32_t ph = (gi / C::STAGES) & 1;
+        if (!wait_bar(bar_empty + 8 * s, ph ^ 1, p)) break;
+        if (!(p.fault == 1 && gi == (uint32_t)C::STAGES + 1)) {  // test hook: skip one stage
+          mbar_arrive_expect_tx(bar_full + 8 * s, kWTileBytes + C::B_BYTES);
+          bulk_g2s(sbase + C::B_REGION + s * kWTileBytes, w_src(u, g), kWTileBytes, bar_full + 8 * s, pol_w);
+          bulk_g2s(sbase + s * C::B_BYTES, x_src(u, g), C::B_BYTES, bar_full + 8 * s, pol_x);
+          issued_mask |= 1u << s;
+          issued_par = (issued_par & ~(1u << s)) | (ph << s);
+        } else {
+          issued_mask &= ~(1u << s);
+        }
+        ++gi;
+        if (++g >= u.g1) {
+          have = iter.next(p, u);
+          if (have) g = u.g0;
+        }
+      }
+      // Let every copy still in flight land before the CTA may exit.
+      for (int s = 0; s < C::STAGES; ++s)
+        if (issued_mask & (1u << s)) wait_bar(bar_full + 8 * s, (issued_par >> s) & 1, p, false);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer --
+    if (lane == 0) {
+      grid_dep_wait();
+      UnitIter iter;
+      iter.init(p);
+      Unit u;
+      uint32_t gi = 0, chunk = 0;
+      bool ok = true;
+      while (ok && iter.next(p, u)) {
+        for (int c0 = u.g0; c0 < u.g1; c0 += kFoldGroups) {
+          const int c1 = min(u.g1, c0 + kFoldGroups);
+          const int b = chunk & 1;
+          if (!wait_bar(bar_accempty + 8 * b, ((chunk >> 1) & 1) ^ 1, p)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem + b * BN;
+          for (int g = c0; g < c1; ++g, ++gi) {
+            const int s = gi % C::STAGES;
+            const int a = gi % kABufs;
+            if (!wait_bar(bar_afull + 8 * a, (gi / kABufs) & 1, p) ||
+                !wait_bar(bar_full + 8 * s, (gi / C::STAGES) & 1, p)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t b_base = sbase + s * C::B_BYTES;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const uint32_t b_addr = b_base + (j >> 2) * (BN * 128) + (j & 3) * 32;
+              tc_mma_ts(d_tmem, tmem + kACol0 + a * 64 + 8 * j, desc_sw128(b_addr), C::IDESC,
+                        (g > c0 || j > 0) ? 1u : 0u);
+            }
+            tc_commit(bar_empty + 8 * s);
+            tc_commit(bar_aempty + 8 * a);
+          }
+          if (!ok) break;
+          tc_commit(bar_accfull + 8 * b);
+          ++chunk;
+        }
+      }
+      // all MMAs issued by this thread complete before TMEM is released
+      tc_commit(bar_drain);
+      wait_bar(bar_drain, 0, p, false);
+    }
+    __syncwarp();
+  } else if (warp < C::EPI_WARP0) {
+    // ------------------------------------------------------------- dequant --
+    grid_dep_wait();
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    constexpr int kChunks = C::NDQ == 8 ? 2 : 4;
+    const int c_first = C::NDQ == 8 ? ((warp - 2) >> 2) * 2 : 0;
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    UnitIter iter;
+    iter.init(p);
+    Unit u;
+    uint32_t gi = 0;
+    bool ok = true;
+    while (ok && iter.next(p, u)) {
+      for (int g = u.g0; g < u.g1; ++g, ++gi) {
+        const int s = gi % C::STAGES;
+        const int a = gi % kABufs;
+        if (!wait_bar(bar_full + 8 * s, (gi / C::STAGES) & 1, p) ||
+            !wait_bar(bar_aempty + 8 * a, ((gi / kABufs) & 1) ^ 1, p)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();  // the MMAs that read this A buffer are complete
+        const uint8_t* wt = smem + C::B_REGION + s * kWTileBytes;
+        const uint32_t s2 = wt[row], z = wt[128 + row];
+        // 1024 + z and 1024 + 16 z as fp16 (exact: the code sits in the mantissa)
+        const uint32_t c_lo = (0x6400u | z) * 0x00010001u;
+        const uint32_t c_hi = (0x6400u | (z << 4)) * 0x00010001u;
+        const uint32_t sc_lo = (uint32_t)__half_as_ushort(__uint2half_rn(s2)) * 0x00010001u;
+        const uint32_t sc_hi = (uint32_t)__half_as_ushort(__float2half_rn((float)s2 * 0.0625f)) * 0x00010001u;
+#pragma unroll
+        for (int cc = 0; cc < kChunks; ++cc) {
+          const int c = c_first + cc;
+          const uint4 v = *reinterpret_cast<const uint4*>(wt + kWNibOffset + c * kWChunkBytes + row * 16);
+          const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+          uint32_t out[16];
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            const uint32_t x = wv[w], y = wv[w] >> 8;
+            // channels 8w + {0,1}: nibbles at bits 0-3 | 16-19 -> 1024 + q
+            out[4 * w + 0] = hsub_hmul2(lop3_and_or(x, 0x000F000Fu, 0x64006400u), c_lo, sc_lo);
+            // channels 8w + {2,3}: bits 4-7 | 20-23 -> 1024 + 16 q
+            out[4 * w + 1] = hsub_hmul2(lop3_and_or(x, 0x00F000F0u, 0x64006400u), c_hi, sc_hi);
+            // channels 8w + {4,5} and {6,7} from the upper byte of each half-word
+            out[4 * w + 2] = hsub_hmul2(lop3_and_or(y, 0x000F000Fu, 0x64006400u), c_lo, sc_lo);
+            out[4 * w + 3] = hsub_hmul2(lop3_and_or(y, 0x00F000F0u, 0x64006400u), c_hi, sc_hi);
+          }
+          tmem_st16(tmem + lane_base + kACol0 + a * 64 + c * 16, out);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(bar_afull + 8 * a);
+          mbar_arrive(bar_empty + 8 * s);
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue --
+    grid_dep_wait();
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const int etid = threadIdx.x - C::EPI_WARP0 * 32;  // 0..127
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    volatile int* last_flag = reinterpret_cast<volatile int*>(smem + C::FLAG_OFF);
+    UnitIter iter;
+    iter.init(p);
+    Unit u;
+    uint32_t chunk = 0;
+    bool ok = true;  // once false, keep the control flow (named barriers) but do no work
+    while (iter.next(p, u)) {
+      const int nt = u.tile / p.MT, mt = u.tile % p.MT;
+      const int n = nt * kTileN + row;
+      int32_t run[BN];
+#pragma unroll
+      for (int i = 0; i < BN; ++i) run[i] = 0;
+      for (int c0 = u.g0; c0 < u.g1; c0 += kFoldGroups, ++chunk) {
+        const int b = chunk & 1;
+        if (ok) ok = wait_bar(bar_accfull + 8 * b, (chunk >> 1) & 1, p);
+        if (ok) {
+          tc_fence_after();
+#pragma unroll
+          for (int piece = 0; piece < BN / 16; ++piece) {
+            uint32_t v[16];
+            tmem_ld16_wait(tmem + lane_base + b * BN + piece * 16, v);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) run[piece * 16 + i] += __float2int_rn(__uint_as_float(v[i]));
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_accempty + 8 * b);
+        }
+      }
+      if (u.g0 == 0 && u.g1 == p.G) {
+        if (ok) write_tile_out<BN>(p, run, mt, n);
+      } else {
+        const int sk = u.tile - p.T_dp;
+        int32_t* part = p.sk_acc + (size_t)sk * BN * kTileN;
+        if (ok) {
+#pragma unroll
+          for (int i = 0; i < BN; ++i) atomicAdd(part + i * kTileN + row, run[i]);
+        }
+        __threadfence();
+        epi_bar_sync();
+        if (etid == 0) {
+          int last = 0;
+          if (ok) {
+            const int add = u.g1 - u.g0;
+            last = (atomicAdd(p.sk_cnt + sk, add) + add == p.G) ? 1 : 0;
+            __threadfence();
+          }
+          *last_flag = last;
+        }
+        epi_bar_sync();
+        if (ok && *last_flag) {
+#pragma unroll
+          for (int i = 0; i < BN; ++i) run[i] = __ldcg(part + i * kTileN + row);
+          write_tile_out<BN>(p, run, mt, n);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// fp16 copy of Xq in the B-operand layout, and the per-call clearing of the
+// workspace header and split-K state.  Layout of xh: [MT][G][2][BN][64] fp16,
+// each [BN][64] block 128B-swizzled (16-byte chunk c of row r stored at chunk
+// c ^ (r & 7)), rows m >= M zero.
+__global__ void __launch_bounds__(256) convert_kernel(const ConvertParams c) {
+  grid_dep_launch_dependents();
+  const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = tid; i < c.zero_count; i += stride) c.zero_words[i] = 0;
+  const int kc_per_row = c.K / 16;
+  const int G = c.K / kGroup;
+  const long long total = (long long)c.MT * c.BN * kc_per_row;
+  for (long long idx = tid; idx < total; idx += stride) {
+    const int m = (int)(idx / kc_per_row);
+    const int k0 = (int)(idx % kc_per_row) * 16;
+    uint4 raw = make_uint4(0, 0, 0, 0);
+    if (m < c.M) raw = __ldg(reinterpret_cast<const uint4*>(c.Xq + (size_t)m * c.K + k0));
+    const int8_t* b = reinterpret_cast<const int8_t*>(&raw);
+    uint32_t h[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      h[i] = (uint32_t)__half_as_ushort(__int2half_rn(b[2 * i])) |
+             ((uint32_t)__half_as_ushort(__int2half_rn(b[2 * i + 1])) << 16);
+    const int g = k0 / kGroup, kk = k0 % kGroup, half = kk / 64, chunk0 = (kk % 64) / 8;
+    const int mt = m / c.BN, r = m % c.BN;
+    uint16_t* blk = c.xh + ((size_t)(mt * G + g) * 2 + half) * c.BN * 64 + (size_t)r * 64;
+    *reinterpret_cast<uint4*>(blk + ((chunk0 ^ (r & 7)) * 8)) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4*>(blk + (((chunk0 + 1) ^ (r & 7)) * 8)) = make_uint4(h[4], h[5], h[6], h[7]);
+  }
+}
+
+template <int BN>
+cudaError_t launch_gemm_bn(const GemmParams& p, cudaStream_t s) {
+  using C = Cfg<BN>;
+  cudaError_t e = cudaFuncSetAttribute(gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.P);
+  cfg.blockDim = dim3(C::THREADS);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_kernel<BN>, p);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(int M, int N, int K, const int8_t* Xq, const uint16_t* sx,
+                        const uint8_t* packed, const uint16_t* s1, uint16_t* Y, int32_t* acc_debug,
+                        void* ws, int num_sms, unsigned long long timeout_ns, int fault,
+                        cudaStream_t s) {
+  const int BN = gemm_bn_for_m(M);
+  const WsLayout L = gemm_ws_layout(M, N, K);
+  GemmParams p = {};
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.G = K / kGroup;
+  p.MT = (M + BN - 1) / BN;
+  p.NT = N / kTileN;
+  p.T = p.MT * p.NT;
+  const int P0 = std::max(1, std::min(num_sms, kMaxGrid));
+  if (p.T >= P0) {
+    const int rem = p.T % P0;
+    p.T_sk = rem == 0 ? 0 : std::min(p.T, rem + P0);
+    p.T_dp = p.T - p.T_sk;
+    p.P = P0;
+  } else {
+    p.T_dp = 0;
+    p.T_sk = p.T;
+    const long long want = ((long long)p.T * p.G + 3) / 4;  // at least ~4 groups per CTA
+    p.P = (int)std::max<long long>(1, std::min<long long>(P0, want));
+  }
+  p.I_sk = (long long)p.T_sk * p.G;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  p.status = reinterpret_cast<int*>(w);
+  p.sk_cnt = reinterpret_cast<int32_t*>(w + L.cnt_off);
+  p.sk_acc = reinterpret_cast<int32_t*>(w + L.acc_off);
+  p.xh = reinterpret_cast<const uint16_t*>(w + L.xh_off);
+  p.packed = packed;
+  p.sx = sx;
+  p.s1 = s1;
+  p.Y = Y;
+  p.acc_debug = acc_debug;
+  p.timeout_ns = timeout_ns;
+  p.fault = fault;
+
+  ConvertParams c = {};
+  c.Xq = Xq;
+  c.xh = reinterpret_cast<uint16_t*>(w + L.xh_off);
+  c.zero_words = reinterpret_cast<int32_t*>(w);
+  c.zero_count = (long long)(L.acc_off + (size_t)p.T_sk * BN * kTileN * 4) / 4;
+  c.M = M;
+  c.K = K;
+  c.BN = BN;
+  c.MT = p.MT;
+  const long long work = std::max<long long>((long long)p.MT * BN * (K / 16), c.zero_count);
+  const int cblocks = (int)std::max<long long>(1, std::min<long long>((work + 255) / 256, (long long)P0 * 4));
+  convert_kernel<<<cblocks, 256, 0, s>>>(c);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  switch (BN) {
+    case 16: return launch_gemm_bn<16>(p, s);
+    case 32: return launch_gemm_bn<32>(p, s);
+    case 64: return launch_gemm_bn<64>(p, s);
+    default: return launch_gemm_bn<128>(p, s);
+  }
+}
+
+}  // namespace qoq
