@@ -23,15 +23,17 @@
 //   warp 0      producer: per 128-channel group, one bulk copy of the packed
 //               weight tile (8448 B) and one of the fp16 activation tile
 //               (pre-swizzled, 128B-swizzle K-major) into an S-stage ring.
-//   warps 2..   dequant: thread r owns weight row r of the tile; it expands its
-//               64 code bytes to 128 fp16 values (q4 - z) * s2 with two packed
-//               fp16 ops per pair (exact) and stores them straight into tensor
-//               memory (tcgen05.st), which is the MMA's A operand: dequantized
+//   warps 2..   dequant: NSLOT slots of 4 warps (one per TMEM lane quadrant);
+//               slot j takes every NSLOT-th group, so NSLOT groups are in
+//               flight.  Thread r owns weight row r of the tile and expands its
+//               64 code bytes to 128 fp16 values with one mask and one packed
+//               FMA per pair (see dequant_pair), storing them straight into
+//               tensor memory (tcgen05.st): the MMA's A operand.  Dequantized
 //               weights never touch shared memory.
 //   warp 1      MMA issuer: 8 x tcgen05.mma (M=128, N=BN, K=16) per group,
 //               A from TMEM, B from shared memory, D in one of two TMEM
 //               accumulators (double-buffered per 8-group fold chunk).
-//   last 4      epilogue: fold fp32 partials to int32, then either write Y
+//   last NEPI   epilogue: fold fp32 partials to int32, then either write Y
 //               (whole-K tiles) or add int32 partials into the workspace
 //               (split-K tiles; the last contributor writes Y).
 // Every mbarrier wait is bounded (globaltimer); on expiry the CTA records
@@ -40,6 +42,7 @@
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -48,23 +51,29 @@ namespace qoq {
 namespace {
 
 constexpr int kTmemCols = 512;
-constexpr int kACol0 = 256;  // A buffers live at TMEM columns 256 + 64 a
-constexpr int kABufs = 4;
 constexpr int kStatusTimeout = 7;  // QOQ_ERR_DEVICE_TIMEOUT
+// The A operand carries w8 * 2^-13 (see dequant_pair); the epilogue undoes it.
+constexpr float kAccScale = 8192.0f;
 
 template <int BN>
 struct Cfg {
-  static constexpr int NDQ = BN <= 64 ? 8 : 4;  // dequant warps
-  static constexpr int NEPI = 4;                // epilogue warps (one per TMEM lane quadrant)
+  static constexpr int NSLOT = BN == 128 ? 2 : (BN == 64 ? 3 : 4);  // groups dequantized concurrently
+  static constexpr int NDQ = 4 * NSLOT;           // dequant warps
+  static constexpr int NEPI = BN >= 64 ? 8 : 4;  // epilogue warps
+  static constexpr int EPI_COLS = BN / (NEPI / 4);  // accumulator columns per epilogue warp
   static constexpr int WARPS = 2 + NDQ + NEPI;
   static constexpr int THREADS = WARPS * 32;
   static constexpr int EPI_WARP0 = 2 + NDQ;
+  // TMEM columns: two fp32 accumulators [0, 2 BN), then A buffers of 64
+  // columns (128 fp16 channels x 128 rows) from ACOL0 to 512.
+  static constexpr int ACOL0 = (2 * BN + 63) / 64 * 64 < 64 ? 64 : (2 * BN + 63) / 64 * 64;
+  static constexpr int NABUF = (kTmemCols - ACOL0) / 64;
   static constexpr int B_BYTES = BN * kGroup * 2;  // fp16 activation tile per group
   static constexpr int STAGES = BN == 128 ? 5 : (BN == 64 ? 8 : (BN == 32 ? 12 : 16));
   static constexpr int B_REGION = STAGES * B_BYTES;
   static constexpr int W_REGION = STAGES * kWTileBytes;
   static constexpr int BAR_OFF = B_REGION + W_REGION;
-  static constexpr int NBARS = 2 * STAGES + 2 * kABufs + 4 + 1;
+  static constexpr int NBARS = 2 * STAGES + 2 * NABUF + 4 + 1;
   static constexpr int TMEM_SLOT_OFF = BAR_OFF + NBARS * 8;
   static constexpr int FLAG_OFF = TMEM_SLOT_OFF + 8;
   static constexpr int SMEM_BYTES = FLAG_OFF + 8 + 1024;  // + slack for 1024-B alignment
@@ -74,10 +83,25 @@ struct Cfg {
   static constexpr uint32_t IDESC =
       (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(kTileN >> 4) << 24);
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
-  static_assert(2 * BN <= kACol0, "accumulators overlap A buffers");
+  static_assert(NABUF >= NSLOT + 1, "A buffers");
   static_assert(B_BYTES % 1024 == 0, "128B-swizzle atoms need 1024-B alignment");
+  static_assert(EPI_COLS % 16 == 0, "epilogue loads 16 columns at a time");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
+
+// Exact dequant of a pair of 4-bit codes (QServe "subtraction after
+// multiplication": the zero point enters after the scale, as one packed FMA).
+// `h` holds the two codes q in the same 4-bit field of each fp16 half, at bit
+// p (p = 0 or 4) and nothing else, i.e. the fp16 subnormals q * 2^(p-24).
+// With sc = s2 * 2^(11-p) and c = -(z * s2) * 2^-13 (both exact in fp16),
+//   fma(h, sc, c) = (q - z) * s2 * 2^-13
+// computed exactly then rounded once; the result is representable (|.| <= 240
+// units of 2^-13, and every non-zero value is a normal fp16), so it is exact.
+__device__ __forceinline__ uint32_t dequant_pair(uint32_t h, uint32_t sc, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(h), "r"(sc), "r"(c));
+  return d;
+}
 
 // Shared-memory matrix descriptor: 128-byte swizzle, K-major, 8-row groups
 // 1024 B apart (SBO), version 1 (bit 46), layout code 2 (bits 61-63).
@@ -125,16 +149,21 @@ struct UnitIter {
 
 // Bounded wait on an mbarrier phase.  Returns false if the wait ran out (the
 // timeout is recorded) or, when honor_abort, if another thread already
-// recorded one for this call.
+// recorded one for this call.  The loop polls only the barrier for the first
+// ~100k cycles; the global timer and the abort flag in global memory are read
+// after that, so a normal hand-off never waits behind a global load.
 __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const GemmParams& p,
                                        bool honor_abort) {
   volatile int* abort_flag = p.status + 1;
-  const uint64_t t0 = global_timer_ns();
+  const long long c0 = clock64();
+  uint64_t t0 = 0;
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 15) == 0) {
+    if ((i & 255) == 0 && clock64() - c0 > 100000) {
+      const uint64_t now = global_timer_ns();
+      if (t0 == 0) t0 = now;
       if (honor_abort && *abort_flag) return false;
-      if (global_timer_ns() - t0 > p.timeout_ns) {
+      if (now - t0 > p.timeout_ns) {
         atomicExch(p.status, kStatusTimeout);
         atomicExch(p.status + 1, 1);
         return false;
@@ -149,15 +178,19 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ge
   return wait_slow(bar, parity, p, honor_abort);
 }
 
-__device__ __forceinline__ void epi_bar_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+template <int NTHREADS>
+__device__ __forceinline__ void epi_bar_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(NTHREADS) : "memory");
+}
 
-template <int BN>
-__device__ __forceinline__ void write_tile_out(const GemmParams& p, const int32_t (&run)[BN], int mt,
+// Y[m, n] for the COLS tokens m = m0 .. m0+COLS-1 held by this thread.
+template <int COLS>
+__device__ __forceinline__ void write_tile_out(const GemmParams& p, const int32_t (&run)[COLS], int m0,
                                                int n) {
   const float s1f = __half2float(__ushort_as_half(p.s1[n]));
 #pragma unroll
-  for (int i = 0; i < BN; ++i) {
-    const int m = mt * BN + i;
+  for (int i = 0; i < COLS; ++i) {
+    const int m = m0 + i;
     if (m < p.M) {
       const float sxf = __half2float(__ushort_as_half(p.sx[m]));
       const float y = (float)run[i] * (sxf * s1f);
@@ -176,17 +209,17 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1) gemm_kernel(const __grid_
   const uint32_t sbase = smem_addr(smem);
   const uint32_t bars = sbase + C::BAR_OFF;
   const uint32_t bar_full = bars, bar_empty = bars + 8 * C::STAGES;
-  const uint32_t bar_afull = bars + 8 * (2 * C::STAGES), bar_aempty = bar_afull + 8 * kABufs;
-  const uint32_t bar_accfull = bar_aempty + 8 * kABufs, bar_accempty = bar_accfull + 16;
+  const uint32_t bar_afull = bars + 8 * (2 * C::STAGES), bar_aempty = bar_afull + 8 * C::NABUF;
+  const uint32_t bar_accfull = bar_aempty + 8 * C::NABUF, bar_accempty = bar_accfull + 16;
   const uint32_t bar_drain = bar_accempty + 16;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, 1 + C::NDQ);
+      mbar_init(bar_empty + 8 * s, 1 + 4);  // MMA commit + the 4 warps of one dequant slot
     }
-    for (int a = 0; a < kABufs; ++a) {
-      mbar_init(bar_afull + 8 * a, C::NDQ);
+    for (int a = 0; a < C::NABUF; ++a) {
+      mbar_init(bar_afull + 8 * a, 4);
       mbar_init(bar_aempty + 8 * a, 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -287,8 +320,8 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1) gemm_kernel(const __grid_
           const uint32_t d_tmem = tmem + b * BN;
           for (int g = c0; g < c1; ++g, ++gi) {
             const int s = gi % C::STAGES;
-            const int a = gi % kABufs;
-            if (!wait_bar(bar_afull + 8 * a, (gi / kABufs) & 1, p) ||
+            const int a = gi % C::NABUF;
+            if (!wait_bar(bar_afull + 8 * a, (gi / C::NABUF) & 1, p) ||
                 !wait_bar(bar_full + 8 * s, (gi / C::STAGES) & 1, p)) {
               ok = false;
               break;
@@ -298,7 +331,7 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1) gemm_kernel(const __grid_
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
               const uint32_t b_addr = b_base + (j >> 2) * (BN * 128) + (j & 3) * 32;
-              tc_mma_ts(d_tmem, tmem + kACol0 + a * 64 + 8 * j, desc_sw128(b_addr), C::IDESC,
+              tc_mma_ts(d_tmem, tmem + C::ACOL0 + a * 64 + 8 * j, desc_sw128(b_addr), C::IDESC,
                         (g > c0 || j > 0) ? 1u : 0u);
             }
             tc_commit(bar_empty + 8 * s);
@@ -318,9 +351,8 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1) gemm_kernel(const __grid_
     // ------------------------------------------------------------- dequant --
     grid_dep_wait();
     const int quad = warp & 3;
+    const int slot = (warp - 2) >> 2;
     const int row = quad * 32 + lane;
-    constexpr int kChunks = C::NDQ == 8 ? 2 : 4;
-    const int c_first = C::NDQ == 8 ? ((warp - 2) >> 2) * 2 : 0;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     UnitIter iter;
     iter.init(p);
@@ -329,39 +361,37 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1) gemm_kernel(const __grid_
     bool ok = true;
     while (ok && iter.next(p, u)) {
       for (int g = u.g0; g < u.g1; ++g, ++gi) {
+        if ((int)(gi % C::NSLOT) != slot) continue;
         const int s = gi % C::STAGES;
-        const int a = gi % kABufs;
+        const int a = gi % C::NABUF;
         if (!wait_bar(bar_full + 8 * s, (gi / C::STAGES) & 1, p) ||
-            !wait_bar(bar_aempty + 8 * a, ((gi / kABufs) & 1) ^ 1, p)) {
+            !wait_bar(bar_aempty + 8 * a, ((gi / C::NABUF) & 1) ^ 1, p)) {
           ok = false;
           break;
         }
         tc_fence_after();  // the MMAs that read this A buffer are complete
         const uint8_t* wt = smem + C::B_REGION + s * kWTileBytes;
         const uint32_t s2 = wt[row], z = wt[128 + row];
-        // 1024 + z and 1024 + 16 z as fp16 (exact: the code sits in the mantissa)
-        const uint32_t c_lo = (0x6400u | z) * 0x00010001u;
-        const uint32_t c_hi = (0x6400u | (z << 4)) * 0x00010001u;
-        const uint32_t sc_lo = (uint32_t)__half_as_ushort(__uint2half_rn(s2)) * 0x00010001u;
-        const uint32_t sc_hi = (uint32_t)__half_as_ushort(__float2half_rn((float)s2 * 0.0625f)) * 0x00010001u;
+        // sc0 = s2 * 2^11 (codes at bit 0), sc4 = s2 * 2^7 (codes at bit 4),
+        // c = -(z * s2) * 2^-13; all exact in fp16 (s2 <= 16, z * s2 <= 240)
+        const uint32_t sc0 = (uint32_t)__half_as_ushort(__float2half_rn((float)(s2 << 11))) * 0x00010001u;
+        const uint32_t sc4 = (uint32_t)__half_as_ushort(__float2half_rn((float)(s2 << 7))) * 0x00010001u;
+        const uint32_t cz =
+            (uint32_t)__half_as_ushort(__float2half_rn(-(float)(z * s2) * (1.0f / 8192.0f))) * 0x00010001u;
 #pragma unroll
-        for (int cc = 0; cc < kChunks; ++cc) {
-          const int c = c_first + cc;
+        for (int c = 0; c < 4; ++c) {
           const uint4 v = *reinterpret_cast<const uint4*>(wt + kWNibOffset + c * kWChunkBytes + row * 16);
           const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
           uint32_t out[16];
 #pragma unroll
           for (int w = 0; w < 4; ++w) {
             const uint32_t x = wv[w], y = wv[w] >> 8;
-            // channels 8w + {0,1}: nibbles at bits 0-3 | 16-19 -> 1024 + q
-            out[4 * w + 0] = hsub_hmul2(lop3_and_or(x, 0x000F000Fu, 0x64006400u), c_lo, sc_lo);
-            // channels 8w + {2,3}: bits 4-7 | 20-23 -> 1024 + 16 q
-            out[4 * w + 1] = hsub_hmul2(lop3_and_or(x, 0x00F000F0u, 0x64006400u), c_hi, sc_hi);
-            // channels 8w + {4,5} and {6,7} from the upper byte of each half-word
-            out[4 * w + 2] = hsub_hmul2(lop3_and_or(y, 0x000F000Fu, 0x64006400u), c_lo, sc_lo);
-            out[4 * w + 3] = hsub_hmul2(lop3_and_or(y, 0x00F000F0u, 0x64006400u), c_hi, sc_hi);
+            out[4 * w + 0] = dequant_pair(x & 0x000F000Fu, sc0, cz);  // channels 8w + 0, 1
+            out[4 * w + 1] = dequant_pair(x & 0x00F000F0u, sc4, cz);  // channels 8w + 2, 3
+            out[4 * w + 2] = dequant_pair(y & 0x000F000Fu, sc0, cz);  // channels 8w + 4, 5
+            out[4 * w + 3] = dequant_pair(y & 0x00F000F0u, sc4, cz);  // channels 8w + 6, 7
           }
-          tmem_st16(tmem + lane_base + kACol0 + a * 64 + c * 16, out);
+          tmem_st16(tmem + lane_base + C::ACOL0 + a * 64 + c * 16, out);
         }
         tmem_wait_st();
         tc_fence_before();
@@ -375,9 +405,11 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1) gemm_kernel(const __grid_
   } else {
     // ------------------------------------------------------------ epilogue --
     grid_dep_wait();
+    const int e = warp - C::EPI_WARP0;
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
-    const int etid = threadIdx.x - C::EPI_WARP0 * 32;  // 0..127
+    const int col0 = (e >> 2) * C::EPI_COLS;  // this warp's accumulator columns
+    const int etid = threadIdx.x - C::EPI_WARP0 * 32;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     volatile int* last_flag = reinterpret_cast<volatile int*>(smem + C::FLAG_OFF);
     UnitIter iter;
@@ -388,20 +420,21 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1) gemm_kernel(const __grid_
     while (iter.next(p, u)) {
       const int nt = u.tile / p.MT, mt = u.tile % p.MT;
       const int n = nt * kTileN + row;
-      int32_t run[BN];
+      int32_t run[C::EPI_COLS];
 #pragma unroll
-      for (int i = 0; i < BN; ++i) run[i] = 0;
+      for (int i = 0; i < C::EPI_COLS; ++i) run[i] = 0;
       for (int c0 = u.g0; c0 < u.g1; c0 += kFoldGroups, ++chunk) {
         const int b = chunk & 1;
         if (ok) ok = wait_bar(bar_accfull + 8 * b, (chunk >> 1) & 1, p);
         if (ok) {
           tc_fence_after();
 #pragma unroll
-          for (int piece = 0; piece < BN / 16; ++piece) {
+          for (int piece = 0; piece < C::EPI_COLS / 16; ++piece) {
             uint32_t v[16];
-            tmem_ld16_wait(tmem + lane_base + b * BN + piece * 16, v);
+            tmem_ld16_wait(tmem + lane_base + b * BN + col0 + piece * 16, v);
 #pragma unroll
-            for (int i = 0; i < 16; ++i) run[piece * 16 + i] += __float2int_rn(__uint_as_float(v[i]));
+            for (int i = 0; i < 16; ++i)
+              run[piece * 16 + i] += __float2int_rn(__uint_as_float(v[i]) * kAccScale);
           }
           tc_fence_before();
           __syncwarp();
@@ -409,30 +442,32 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1) gemm_kernel(const __grid_
         }
       }
       if (u.g0 == 0 && u.g1 == p.G) {
-        if (ok) write_tile_out<BN>(p, run, mt, n);
+        if (ok) write_tile_out<C::EPI_COLS>(p, run, mt * BN + col0, n);
       } else {
         const int sk = u.tile - p.T_dp;
-        int32_t* part = p.sk_acc + (size_t)sk * BN * kTileN;
+        int32_t* part = p.sk_acc + (size_t)sk * BN * kTileN + (size_t)col0 * kTileN;
         if (ok) {
 #pragma unroll
-          for (int i = 0; i < BN; ++i) atomicAdd(part + i * kTileN + row, run[i]);
+          for (int i = 0; i < C::EPI_COLS; ++i) red_add_relaxed(part + i * kTileN + row, run[i]);
         }
-        __threadfence();
-        epi_bar_sync();
+        // The barrier orders every epilogue thread's partial sums before one
+        // thread's acq_rel count update (release is cumulative over the
+        // barrier); the last contributor's acquire makes the other CTAs' sums
+        // visible, and the second barrier passes that on to its warps.
+        epi_bar_sync<C::NEPI * 32>();
         if (etid == 0) {
           int last = 0;
           if (ok) {
             const int add = u.g1 - u.g0;
-            last = (atomicAdd(p.sk_cnt + sk, add) + add == p.G) ? 1 : 0;
-            __threadfence();
+            last = (atom_add_acq_rel(p.sk_cnt + sk, add) + add == p.G) ? 1 : 0;
           }
           *last_flag = last;
         }
-        epi_bar_sync();
+        epi_bar_sync<C::NEPI * 32>();
         if (ok && *last_flag) {
 #pragma unroll
-          for (int i = 0; i < BN; ++i) run[i] = __ldcg(part + i * kTileN + row);
-          write_tile_out<BN>(p, run, mt, n);
+          for (int i = 0; i < C::EPI_COLS; ++i) run[i] = ld_relaxed(part + i * kTileN + row);
+          write_tile_out<C::EPI_COLS>(p, run, mt * BN + col0, n);
         }
       }
     }
@@ -477,11 +512,27 @@ __global__ void __launch_bounds__(256) convert_kernel(const ConvertParams c) {
   }
 }
 
+// Opt the kernel into its dynamic shared memory once per device (not a
+// stream operation; done before any graph capture can reach it).
+template <int BN>
+cudaError_t set_smem_attr_once() {
+  static std::mutex mu;
+  static uint64_t done_mask = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev < 64 && (done_mask >> dev) & 1) return cudaSuccess;
+  e = cudaFuncSetAttribute(gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Cfg<BN>::SMEM_BYTES);
+  if (e == cudaSuccess && dev < 64) done_mask |= 1ull << dev;
+  return e;
+}
+
 template <int BN>
 cudaError_t launch_gemm_bn(const GemmParams& p, cudaStream_t s) {
   using C = Cfg<BN>;
-  cudaError_t e = cudaFuncSetAttribute(gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       C::SMEM_BYTES);
+  cudaError_t e = set_smem_attr_once<BN>();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.P);

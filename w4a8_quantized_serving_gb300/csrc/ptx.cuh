@@ -155,6 +155,24 @@ __device__ __forceinline__ void tmem_ld16_wait(uint32_t taddr, uint32_t (&v)[16]
       : "memory");
 }
 
+// ------------------------------------------------------ global atomics --
+
+__device__ __forceinline__ void red_add_relaxed(int32_t* addr, int32_t v) {
+  asm volatile("red.relaxed.gpu.global.add.s32 [%0], %1;" ::"l"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int32_t atom_add_acq_rel(int32_t* addr, int32_t v) {
+  int32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
+  return old;
+}
+
+__device__ __forceinline__ int32_t ld_relaxed(const int32_t* addr) {
+  int32_t v;
+  asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(addr) : "memory");
+  return v;
+}
+
 // ------------------------------------------------------- small ALU helpers --
 
 // (a & b) | c in one instruction.
