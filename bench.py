@@ -245,7 +245,7 @@ def run_ours(args, c: dict) -> None:
             Xq=torch.empty((M, K), dtype=torch.int8, device=dev),
             sx=torch.empty(M, dtype=torch.float16, device=dev),
             Y=torch.empty((M, N), dtype=torch.float16, device=dev),
-            ws=torch.empty(ws_bytes, dtype=torch.uint8, device=dev)))
+            ws=torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)))
     del packed, s1
 
     def step(i: int):

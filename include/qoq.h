@@ -89,10 +89,13 @@ size_t qoq_packed_weight_bytes(int N, int K, int g);
 /*
  * Bytes of device workspace that qoq_w4a8_gemm needs for (M, N, K, g)
  * (host-only; 0 for an unsupported shape).  It holds a status header, the
- * split-K partial sums and tile counters, and an fp16 copy of Xq laid out
- * for the tensor-core B operand.  The workspace needs no initialisation and
- * is rewritten by every call; two calls in flight at the same time must not
- * share one.
+ * split-K partial sums and tile counters, and (for M > 64) an fp16 copy of Xq
+ * laid out for the tensor-core B operand.
+ * The caller zero-fills the workspace once after allocating it (e.g.
+ * cudaMemsetAsync); every call that completes leaves it zeroed again, so no
+ * per-call clearing is needed.  After a call that reported
+ * QOQ_ERR_DEVICE_TIMEOUT, zero-fill it again before reuse.  Two calls in
+ * flight at the same time must not share one workspace.
  */
 size_t qoq_gemm_workspace_bytes(int M, int N, int K, int g);
 
@@ -137,7 +140,11 @@ qoq_status qoq_quant_act(int M, int K, const uint16_t* X_f16, int8_t* Xq, uint16
  *      (from qoq_pack_weights).
  * Out: Y_f16 [M][N] fp16 bits; acc_debug [M][N] int32 when not NULL.
  * workspace: ws_bytes >= qoq_gemm_workspace_bytes(M, N, K, g), 16-byte
- *      aligned, owned by the caller, used by one call at a time.
+ *      aligned, zero-filled once by the caller (see above), used by one call
+ *      at a time.
+ * The kernels are launched with programmatic dependent launch: the GEMM
+ * starts streaming weights while the preceding kernel on the stream (e.g.
+ * qoq_quant_act) finishes, and waits for it before reading Xq and s_x.
  * A device-side pipeline stall that exceeds the wait limit ends the kernel
  * early, leaves Y undefined and records QOQ_ERR_DEVICE_TIMEOUT in the
  * workspace header, which qoq_last_device_status returns.
@@ -155,9 +162,9 @@ qoq_status qoq_unpack_weights_debug(int N, int K, int g, const uint8_t* packed, 
                                     uint8_t* s2, uint8_t* z, qoq_stream_t stream);
 
 /*
- * Synchronizes `stream`, then reads and clears the device status that the
- * most recent qoq_w4a8_gemm call on `workspace` recorded (each call resets it
- * on the device before its GEMM kernel starts).  Returns QOQ_OK,
+ * Synchronizes `stream`, then reads and clears the device status recorded in
+ * `workspace` by the qoq_w4a8_gemm calls since the previous read (the status
+ * is sticky: any timeout among them is reported).  Returns QOQ_OK,
  * QOQ_ERR_DEVICE_TIMEOUT, or QOQ_ERR_CUDA (a CUDA error surfaced by the
  * synchronization, e.g. a failed kernel).
  */

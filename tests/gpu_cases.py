@@ -39,7 +39,7 @@ def gpu_layer(W: np.ndarray, X: np.ndarray, want_acc: bool = True, ws=None):
     Xq, sx = q.qoq_quant_act(Xd)
     acc = t.empty((M, N), dtype=t.int32, device="cuda") if want_acc else None
     if ws is None:
-        ws = t.empty(q.qoq_gemm_workspace_bytes(M, N, K), dtype=t.uint8, device="cuda")
+        ws = t.zeros(q.qoq_gemm_workspace_bytes(M, N, K), dtype=t.uint8, device="cuda")
     Y = q.qoq_w4a8_gemm(Xq, sx, packed, s1, N, acc_debug=acc, workspace=ws)
     status = q.qoq_last_device_status(ws)
     assert status == 0, f"device status {status}"

@@ -190,13 +190,14 @@ def test_device_wait_timeout_is_reported_and_context_survives():
     Wd, Xd = gc.to_dev_f16(W), gc.to_dev_f16(X)
     packed, s1 = mod.qoq_pack_weights(Wd)
     Xq, sx = mod.qoq_quant_act(Xd)
-    ws = t.empty(mod.qoq_gemm_workspace_bytes(M, N, K), dtype=t.uint8, device="cuda")
+    ws = t.zeros(mod.qoq_gemm_workspace_bytes(M, N, K), dtype=t.uint8, device="cuda")
     try:
         mod.qoq_set_debug(5_000_000, 1)  # 5 ms wait limit, skip one stage
         mod.qoq_w4a8_gemm(Xq, sx, packed, s1, N, workspace=ws)
         assert mod.qoq_last_device_status(ws) == 7
     finally:
         mod.qoq_set_debug(0, 0)
+    ws.zero_()  # an aborted call leaves split-K state behind: clear before reuse
     acc = t.empty((M, N), dtype=t.int32, device="cuda")
     mod.qoq_w4a8_gemm(Xq, sx, packed, s1, N, acc_debug=acc, workspace=ws)
     assert mod.qoq_last_device_status(ws) == 0

@@ -171,8 +171,8 @@ def qoq_w4a8_gemm(Xq, sx, packed, s1, N: int | None = None, g: int = 128, Y=None
     if Y is None:
         Y = torch.empty((M, N), dtype=torch.float16, device=Xq.device)
     ws_need = qoq_gemm_workspace_bytes(M, N, K, g)
-    if workspace is None:
-        workspace = torch.empty(max(ws_need, 16), dtype=torch.uint8, device=Xq.device)
+    if workspace is None:  # zero-filled once; every completed call leaves it zeroed
+        workspace = torch.zeros(max(ws_need, 16), dtype=torch.uint8, device=Xq.device)
     acc_ptr = None if acc_debug is None else _dev(acc_debug, torch.int32, "acc_debug", (M, N))
     code = lib().qoq_w4a8_gemm(M, N, K, g, _dev(Xq, torch.int8, "Xq"), _dev(sx, torch.float16, "sx", (M,)),
                                _dev(packed, torch.uint8, "packed"), _dev(s1, torch.float16, "s1", (N,)),
@@ -193,6 +193,12 @@ def qoq_unpack_weights_debug(packed, N: int, K: int, g: int = 128, stream=None):
                                           s2.data_ptr(), z.data_ptr(), _stream(stream)),
            "qoq_unpack_weights_debug")
     return q4, s2, z
+
+
+def workspace_for(M: int, N: int, K: int, g: int = 128, device="cuda"):
+    """A zero-filled workspace for qoq_w4a8_gemm at (M, N, K)."""
+    torch = _torch()
+    return torch.zeros(max(qoq_gemm_workspace_bytes(M, N, K, g), 16), dtype=torch.uint8, device=device)
 
 
 def qoq_last_device_status(workspace, stream=None) -> int:
@@ -217,7 +223,7 @@ class QoQLinear:
         torch = _torch()
         if M not in self._ws:
             need = qoq_gemm_workspace_bytes(M, self.N, self.K, self.g)
-            self._ws[M] = torch.empty(need, dtype=torch.uint8, device=self.packed.device)
+            self._ws[M] = torch.zeros(need, dtype=torch.uint8, device=self.packed.device)
         return self._ws[M]
 
     def __call__(self, X, stream=None):

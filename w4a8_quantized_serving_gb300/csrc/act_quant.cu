@@ -7,19 +7,23 @@
 //   Xq[m,k] = clamp(rint(X[m,k] / s_x[m]), -127, 127)      (fp32 divide, ties even)
 // An all-zero row gets s_x = 0 and Xq = 0.
 //
-// One CTA per token row: each thread loads up to 16 vectors of 8 fp16 values
-// (16 bytes) into registers, the CTA reduces the max-abs (warp shuffles, then
-// shared memory), and the same registers are quantized and stored, so X is
-// read from HBM once.  The work is HBM bound: 2 bytes read and 1 byte written
-// per element.
+// Each token row is owned by T threads (T a power of two, 32..1024), each
+// holding up to 16 vectors of 8 fp16 values in registers, so X is read from
+// HBM once; the row max-abs is reduced with warp shuffles (and shared memory
+// when T > 32).  CTAs have 128 threads when T <= 128 (several rows each) so
+// that they fit beside the GEMM's persistent CTAs: the kernel lets the
+// dependent GEMM launch at once (programmatic dependent launch), and the GEMM
+// streams its weights while this kernel runs.  HBM bound: 2 bytes read and
+// 1 byte written per element.
 #include <cuda_fp16.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace qoq {
 namespace {
 
-constexpr int kMaxVecPerThread = 16;  // K <= 131072 with 1024 threads
+constexpr int kMaxVecPerThread = 16;  // K <= 131072 with T = 1024
 
 __device__ __forceinline__ float absmax8(uint4 v, float m) {
   const __half2* h = reinterpret_cast<const __half2*>(&v);
@@ -43,45 +47,47 @@ __device__ __forceinline__ uint32_t quant4(const __half* h, float sf) {
 
 __global__ void __launch_bounds__(1024) act_quant_kernel(const uint16_t* __restrict__ X,
                                                          int8_t* __restrict__ Xq,
-                                                         uint16_t* __restrict__ sx, int K) {
+                                                         uint16_t* __restrict__ sx, int M, int K,
+                                                         int T) {
+  grid_dep_launch_dependents();
   __shared__ float warp_max[32];
-  const int row = blockIdx.x;
+  const int rows_per_cta = blockDim.x / T;
+  const int row = blockIdx.x * rows_per_cta + threadIdx.x / T;
+  const int t = threadIdx.x % T;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nvec = K / 8;
-  const uint4* xr = reinterpret_cast<const uint4*>(X + (size_t)row * K);
+  const bool live = row < M;
+  const uint4* xr = reinterpret_cast<const uint4*>(X + (size_t)(live ? row : 0) * K);
   uint4 v[kMaxVecPerThread];
   float amax = 0.0f;
 #pragma unroll
   for (int i = 0; i < kMaxVecPerThread; ++i) {
-    const int idx = threadIdx.x + i * blockDim.x;
-    if (idx < nvec) {
+    const int idx = t + i * T;
+    if (live && idx < nvec) {
       v[i] = __ldg(xr + idx);
       amax = absmax8(v[i], amax);
     }
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) warp_max[warp] = amax;
-  __syncthreads();
-  if (warp == 0) {
-    const int nw = blockDim.x >> 5;
-    float m = lane < nw ? warp_max[lane] : 0.0f;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-    if (lane == 0) warp_max[0] = m;
+  if (T > 32) {  // combine the T/32 warps of this row
+    if (lane == 0) warp_max[warp] = amax;
+    __syncthreads();
+    const int w0 = (threadIdx.x / T) * (T / 32);
+    amax = 0.0f;
+    for (int w = 0; w < T / 32; ++w) amax = fmaxf(amax, warp_max[w0 + w]);
   }
-  __syncthreads();
-  amax = warp_max[0];
+  if (!live) return;
 
   __half s = __float2half_rn(0.0f);
   if (amax > 0.0f) s = __float2half_rn(__fdiv_rn(amax, 127.0f));
   const float sf = __half2float(s);
-  if (threadIdx.x == 0) sx[row] = __half_as_ushort(s);
+  if (t == 0) sx[row] = __half_as_ushort(s);
 
   uint2* qr = reinterpret_cast<uint2*>(Xq + (size_t)row * K);
 #pragma unroll
   for (int i = 0; i < kMaxVecPerThread; ++i) {
-    const int idx = threadIdx.x + i * blockDim.x;
+    const int idx = t + i * T;
     if (idx < nvec) {
       uint2 out = make_uint2(0, 0);
       if (sf != 0.0f) {
@@ -98,10 +104,12 @@ __global__ void __launch_bounds__(1024) act_quant_kernel(const uint16_t* __restr
 cudaError_t launch_act_quant(int M, int K, const uint16_t* X, int8_t* Xq, uint16_t* sx,
                              cudaStream_t s) {
   const int nvec = K / 8;
-  // one vector per thread up to 1024 threads (latency), up to 16 beyond (K <= 131072)
-  int threads = (nvec + 31) / 32 * 32;
-  if (threads > 1024) threads = 1024;
-  act_quant_kernel<<<M, threads, 0, s>>>(X, Xq, sx, K);
+  int T = 32;  // threads per row: a power of two with <= 16 vectors each
+  while (T * kMaxVecPerThread < nvec) T *= 2;
+  const int threads = T < 128 ? 128 : T;
+  const int rows_per_cta = threads / T;
+  const int grid = (M + rows_per_cta - 1) / rows_per_cta;
+  act_quant_kernel<<<grid, threads, 0, s>>>(X, Xq, sx, M, K, T);
   return cudaGetLastError();
 }
 

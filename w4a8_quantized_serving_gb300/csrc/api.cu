@@ -20,6 +20,8 @@ constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s
 
 std::atomic<unsigned long long> g_timeout_ns{0};
 std::atomic<int> g_fault{0};
+std::atomic<unsigned long long*> g_trace{nullptr};
+std::atomic<unsigned> g_call_id{0};
 
 struct DevInfo {
   std::once_flag once;
@@ -135,8 +137,11 @@ qoq_status qoq_w4a8_gemm(int M, int N, int K, int g, const int8_t* Xq, const uin
   if (st != QOQ_OK) return st;
   unsigned long long tmo = g_timeout_ns.load();
   if (tmo == 0) tmo = kDefaultTimeoutNs;
+  unsigned call_id = g_call_id.fetch_add(1) + 1;
+  if (call_id == 0) call_id = g_call_id.fetch_add(1) + 1;  // skip 0 on wrap-around
   return from_cuda(qoq::launch_gemm(M, N, K, Xq, sx_f16, packed, s1_f16, Y_f16, acc_debug, workspace,
-                                    sms, tmo, g_fault.load(), reinterpret_cast<cudaStream_t>(stream)));
+                                    sms, tmo, g_fault.load(), call_id, g_trace.load(),
+                                    reinterpret_cast<cudaStream_t>(stream)));
 }
 
 qoq_status qoq_unpack_weights_debug(int N, int K, int g, const uint8_t* packed, uint8_t* q4,
@@ -158,7 +163,7 @@ qoq_status qoq_last_device_status(void* workspace, qoq_stream_t stream) {
   cudaError_t e = cudaMemcpyAsync(host, workspace, sizeof(host), cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return from_cuda(e);
-  e = cudaMemsetAsync(workspace, 0, sizeof(host), s);
+  e = cudaMemsetAsync(workspace, 0, sizeof(int), s);  // the sticky status word
   if (e != cudaSuccess) return from_cuda(e);
   return host[0] == 0 ? QOQ_OK : (host[0] == QOQ_ERR_DEVICE_TIMEOUT ? QOQ_ERR_DEVICE_TIMEOUT : QOQ_ERR_CUDA);
 }
@@ -169,5 +174,13 @@ qoq_status qoq_set_debug(uint64_t wait_timeout_ns, int fault) {
   g_fault.store(fault);
   return QOQ_OK;
 }
+
+#ifdef QOQ_TRACE
+// Trace builds only: device buffer of (grid size x kTraceSlots) uint64 that
+// the next GEMM launches fill with pipeline event clocks (NULL disables).
+void qoq_debug_set_trace(void* device_buffer) {
+  g_trace.store(static_cast<unsigned long long*>(device_buffer));
+}
+#endif
 
 }  // extern "C"

@@ -14,15 +14,17 @@
 // reach the HBM floor.
 //
 // sm_103a has no integer tcgen05 MMA, so the exact int8 x int8 product runs on
-// tcgen05.mma kind::f16: both operands are small integers (|v| <= 127), exact
-// in fp16; each product (<= 16129) and each partial sum below 2^24 is exact in
-// the fp32 accumulator, and the epilogue folds the fp32 TMEM partials into
-// int32 registers every 8 groups (1024 channels, 127*127*1024 < 2^24).
+// tcgen05.mma kind::f16: both operands are small integers times a power of
+// two, exact in fp16; each product and each partial sum below 2^24 units is
+// exact in the fp32 accumulator, and the epilogue folds the fp32 TMEM partials
+// into int32 every 8 groups (1024 channels, 127*127*1024 < 2^24).
 //
 // Data path per CTA (one persistent CTA per SM, warp-specialised):
 //   warp 0      producer: per 128-channel group, one bulk copy of the packed
-//               weight tile (8448 B) and one of the fp16 activation tile
-//               (pre-swizzled, 128B-swizzle K-major) into an S-stage ring.
+//               weight tile (8448 B) and the activation tile into an S-stage
+//               ring: for token tiles of <= 64 rows the int8 Xq tile by 2D TMA
+//               (converted to fp16 in shared memory by the dequant warps), for
+//               128-row tiles a pre-swizzled fp16 tile made by convert_kernel.
 //   warps 2..   dequant: NSLOT slots of 4 warps (one per TMEM lane quadrant);
 //               slot j takes every NSLOT-th group, so NSLOT groups are in
 //               flight.  Thread r owns weight row r of the tile and expands its
@@ -30,18 +32,25 @@
 //               FMA per pair (see dequant_pair), storing them straight into
 //               tensor memory (tcgen05.st): the MMA's A operand.  Dequantized
 //               weights never touch shared memory.
-//   warp 1      MMA issuer: 8 x tcgen05.mma (M=128, N=BN, K=16) per group,
-//               A from TMEM, B from shared memory, D in one of two TMEM
-//               accumulators (double-buffered per 8-group fold chunk).
-//   last NEPI   epilogue: fold fp32 partials to int32, then either write Y
+//   warp 1      MMA issuer: 8 x tcgen05.mma (M=128, N=BN, K=16) per group, A
+//               from TMEM, B from shared memory, D in one of two TMEM
+//               accumulators (double-buffered per fold chunk).  The warp stays
+//               converged and one elected lane issues: a diverged single
+//               thread issues tcgen05 ops about 2.5x slower, and each mbarrier
+//               wait costs ~100 cycles even when the phase is complete, so the
+//               loop waits once per group.
+//   last NEPI   epilogue: sum the R chains, fold fp32 to int32, then write Y
 //               (whole-K tiles) or add int32 partials into the workspace
-//               (split-K tiles; the last contributor writes Y).
-// Every mbarrier wait is bounded (globaltimer); on expiry the CTA records
+//               (split-K tiles; the last contributor writes Y and clears them).
+// Every mbarrier wait is bounded; on expiry the CTA records
 // QOQ_ERR_DEVICE_TIMEOUT in the workspace header, drains its copies and MMAs,
 // frees its tensor memory and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <cstring>
 #include <mutex>
 
 #include "internal.h"
@@ -51,29 +60,36 @@ namespace qoq {
 namespace {
 
 constexpr int kTmemCols = 512;
+constexpr int kACol0 = 256;  // A buffers: TMEM columns 256 + 64 a
+constexpr int kNABuf = 4;
 constexpr int kStatusTimeout = 7;  // QOQ_ERR_DEVICE_TIMEOUT
 // The A operand carries w8 * 2^-13 (see dequant_pair); the epilogue undoes it.
 constexpr float kAccScale = 8192.0f;
+constexpr int kSmemBudget = 228 * 1024;
 
 template <int BN>
 struct Cfg {
-  static constexpr int NSLOT = BN == 128 ? 2 : (BN == 64 ? 3 : 4);  // groups dequantized concurrently
-  static constexpr int NDQ = 4 * NSLOT;           // dequant warps
-  static constexpr int NEPI = BN >= 64 ? 8 : 4;  // epilogue warps
-  static constexpr int EPI_COLS = BN / (NEPI / 4);  // accumulator columns per epilogue warp
+  static constexpr bool IN_KERNEL_B = BN <= 64;  // int8 tile by TMA, fp16 made in shared memory
+  static constexpr int R = 1;                                   // accumulator chains per set
+  static constexpr int ACC_COLS = R * BN;                       // TMEM columns per accumulator set
+  static constexpr int NACC = 2;                                // accumulator sets (double buffer)
+  static constexpr int NSLOT = BN <= 32 ? 3 : 2;               // groups dequantized concurrently
+  static constexpr int NDQ = 4 * NSLOT;                        // dequant warps
+  static constexpr int NEPI = BN == 128 ? 16 : (BN == 64 ? 8 : 4);  // epilogue warps
+  static constexpr int EPI_TOK = BN / (NEPI / 4);              // tokens per epilogue thread
   static constexpr int WARPS = 2 + NDQ + NEPI;
   static constexpr int THREADS = WARPS * 32;
   static constexpr int EPI_WARP0 = 2 + NDQ;
-  // TMEM columns: two fp32 accumulators [0, 2 BN), then A buffers of 64
-  // columns (128 fp16 channels x 128 rows) from ACOL0 to 512.
-  static constexpr int ACOL0 = (2 * BN + 63) / 64 * 64 < 64 ? 64 : (2 * BN + 63) / 64 * 64;
-  static constexpr int NABUF = (kTmemCols - ACOL0) / 64;
-  static constexpr int B_BYTES = BN * kGroup * 2;  // fp16 activation tile per group
-  static constexpr int STAGES = BN == 128 ? 5 : (BN == 64 ? 8 : (BN == 32 ? 12 : 16));
-  static constexpr int B_REGION = STAGES * B_BYTES;
-  static constexpr int W_REGION = STAGES * kWTileBytes;
-  static constexpr int BAR_OFF = B_REGION + W_REGION;
-  static constexpr int NBARS = 2 * STAGES + 2 * NABUF + 4 + 1;
+  static constexpr int B_BYTES = BN * kGroup * 2;               // fp16 B tile per group
+  static constexpr int X8_BYTES = IN_KERNEL_B ? BN * kGroup : 0; // int8 staging per group
+  static constexpr int STAGE_BYTES = B_BYTES + X8_BYTES + kWTileBytes;
+  static constexpr int STAGES_FIT = (kSmemBudget - 2048) / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_FIT > 16 ? 16 : STAGES_FIT;
+  static constexpr int B_OFF = 0;
+  static constexpr int X8_OFF = STAGES * B_BYTES;
+  static constexpr int W_OFF = X8_OFF + STAGES * X8_BYTES;
+  static constexpr int BAR_OFF = W_OFF + STAGES * kWTileBytes;
+  static constexpr int NBARS = 2 * STAGES + 2 * kNABuf + 2 * NACC + 1;
   static constexpr int TMEM_SLOT_OFF = BAR_OFF + NBARS * 8;
   static constexpr int FLAG_OFF = TMEM_SLOT_OFF + 8;
   static constexpr int SMEM_BYTES = FLAG_OFF + 8 + 1024;  // + slack for 1024-B alignment
@@ -83,9 +99,12 @@ struct Cfg {
   static constexpr uint32_t IDESC =
       (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(kTileN >> 4) << 24);
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
-  static_assert(NABUF >= NSLOT + 1, "A buffers");
-  static_assert(B_BYTES % 1024 == 0, "128B-swizzle atoms need 1024-B alignment");
-  static_assert(EPI_COLS % 16 == 0, "epilogue loads 16 columns at a time");
+  static_assert(8 % R == 0, "chains divide the 8 K-steps of a group");
+  static_assert(NACC * ACC_COLS <= kACol0, "accumulators overlap A buffers");
+  static_assert(kNABuf >= NSLOT + 1, "A buffers");
+  static_assert(B_BYTES % 1024 == 0 && X8_BYTES % 1024 == 0, "1024-B aligned tiles");
+  static_assert(EPI_TOK % 16 == 0, "epilogue loads 16 columns at a time");
+  static_assert(STAGES >= 3, "pipeline depth");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
@@ -101,6 +120,18 @@ __device__ __forceinline__ uint32_t dequant_pair(uint32_t h, uint32_t sc, uint32
   uint32_t d;
   asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(h), "r"(sc), "r"(c));
   return d;
+}
+
+// Four int8 lanes of `x` -> two fp16x2 (exact): the biased byte u = b ^ 0x80
+// becomes the fp16 1024 + u through its mantissa, and 1024 + 128 is removed.
+__device__ __forceinline__ void int8x4_to_half2x2(uint32_t x, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = x ^ 0x80808080u;
+  const uint32_t bias = 0x64806480u;  // fp16 (1152, 1152)
+  uint32_t a, b;
+  asm("prmt.b32 %0, %1, %2, 0x7170;" : "=r"(a) : "r"(u), "r"(0x64646464u));
+  asm("prmt.b32 %0, %1, %2, 0x7372;" : "=r"(b) : "r"(u), "r"(0x64646464u));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(bias));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(bias));
 }
 
 // Shared-memory matrix descriptor: 128-byte swizzle, K-major, 8-row groups
@@ -148,13 +179,13 @@ struct UnitIter {
 };
 
 // Bounded wait on an mbarrier phase.  Returns false if the wait ran out (the
-// timeout is recorded) or, when honor_abort, if another thread already
-// recorded one for this call.  The loop polls only the barrier for the first
-// ~100k cycles; the global timer and the abort flag in global memory are read
-// after that, so a normal hand-off never waits behind a global load.
+// timeout is recorded) or, when honor_abort, if another thread of this call
+// already recorded one.  The loop polls only the barrier for the first ~100k
+// cycles; the global timer and the abort word in global memory are read after
+// that, so a normal hand-off never waits behind a global load.
 __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const GemmParams& p,
                                        bool honor_abort) {
-  volatile int* abort_flag = p.status + 1;
+  volatile unsigned* abort_word = reinterpret_cast<volatile unsigned*>(p.status + 1);
   const long long c0 = clock64();
   uint64_t t0 = 0;
   for (uint32_t i = 1;; ++i) {
@@ -162,10 +193,10 @@ __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const Gemm
     if ((i & 255) == 0 && clock64() - c0 > 100000) {
       const uint64_t now = global_timer_ns();
       if (t0 == 0) t0 = now;
-      if (honor_abort && *abort_flag) return false;
+      if (honor_abort && *abort_word == p.call_id) return false;
       if (now - t0 > p.timeout_ns) {
         atomicExch(p.status, kStatusTimeout);
-        atomicExch(p.status + 1, 1);
+        atomicExch(reinterpret_cast<unsigned*>(p.status + 1), p.call_id);
         return false;
       }
     }
@@ -201,7 +232,8 @@ __device__ __forceinline__ void write_tile_out(const GemmParams& p, const int32_
 }
 
 template <int BN>
-__global__ void __launch_bounds__(Cfg<BN>::THREADS, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
+__global__ void __launch_bounds__(Cfg<BN>::THREADS, 1)
+    gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap xmap) {
   using C = Cfg<BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -209,20 +241,20 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1) gemm_kernel(const __grid_
   const uint32_t sbase = smem_addr(smem);
   const uint32_t bars = sbase + C::BAR_OFF;
   const uint32_t bar_full = bars, bar_empty = bars + 8 * C::STAGES;
-  const uint32_t bar_afull = bars + 8 * (2 * C::STAGES), bar_aempty = bar_afull + 8 * C::NABUF;
-  const uint32_t bar_accfull = bar_aempty + 8 * C::NABUF, bar_accempty = bar_accfull + 16;
-  const uint32_t bar_drain = bar_accempty + 16;
+  const uint32_t bar_afull = bars + 8 * (2 * C::STAGES), bar_aempty = bar_afull + 8 * kNABuf;
+  const uint32_t bar_accfull = bar_aempty + 8 * kNABuf, bar_accempty = bar_accfull + 8 * C::NACC;
+  const uint32_t bar_drain = bar_accempty + 8 * C::NACC;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1 + 4);  // MMA commit + the 4 warps of one dequant slot
     }
-    for (int a = 0; a < C::NABUF; ++a) {
+    for (int a = 0; a < kNABuf; ++a) {
       mbar_init(bar_afull + 8 * a, 4);
       mbar_init(bar_aempty + 8 * a, 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < C::NACC; ++b) {
       mbar_init(bar_accfull + 8 * b, 1);
       mbar_init(bar_accempty + 8 * b, C::NEPI);
     }
@@ -234,32 +266,47 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1) gemm_kernel(const __grid_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + C::TMEM_SLOT_OFF);
+  if (threadIdx.x == 0) {
+    QOQ_TRACE_AT(p, 0, 0);
+    QOQ_TRACE_AT(p, 1, 0);
+  }
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer --
     if (lane == 0) {
       const uint64_t pol_w = p.MT == 1 ? policy_evict_first() : policy_evict_last();
       const uint64_t pol_x = policy_evict_last();
+      if (C::IN_KERNEL_B) prefetch_tensormap(&xmap);
       UnitIter iter;
       iter.init(p);
       Unit u;
       bool have = iter.next(p, u);
       int g = have ? u.g0 : 0;
       uint32_t issued_mask = 0, issued_par = 0;  // per stage: last issue and its parity
-      auto w_src = [&](const Unit& uu, int gg) {
-        return p.packed + ((size_t)(uu.tile / p.MT) * p.G + gg) * kWTileBytes;
+      constexpr uint32_t kStageTx = kWTileBytes + (C::IN_KERNEL_B ? C::X8_BYTES : C::B_BYTES);
+      auto issue_w = [&](int s, int tile, int gg) {
+        const uint8_t* src = p.packed + ((size_t)(tile / p.MT) * p.G + gg) * kWTileBytes;
+        bulk_g2s(sbase + C::W_OFF + s * kWTileBytes, src, kWTileBytes, bar_full + 8 * s, pol_w);
       };
-      auto x_src = [&](const Unit& uu, int gg) {
-        return p.xh + ((size_t)(uu.tile % p.MT) * p.G + gg) * (C::B_BYTES / 2);
+      auto issue_x = [&](int s, int tile, int gg) {
+        const int mt = tile % p.MT;
+        if (C::IN_KERNEL_B) {
+          tma_load_2d(sbase + C::X8_OFF + s * C::X8_BYTES, &xmap, gg * kGroup, mt * BN, bar_full + 8 * s,
+                      pol_x);
+        } else {
+          const uint16_t* src = p.xh + ((size_t)mt * p.G + gg) * (C::B_BYTES / 2);
+          bulk_g2s(sbase + C::B_OFF + s * C::B_BYTES, src, C::B_BYTES, bar_full + 8 * s, pol_x);
+        }
       };
-      // Weights do not depend on the preceding kernel: start streaming them
-      // for the first ring's worth of groups before waiting on it.
+      // Weights do not depend on the preceding kernels (activation quant,
+      // B-operand convert): stream the first ring's worth before waiting on them.
       int npre = 0;
       int pre_tile[C::STAGES], pre_g[C::STAGES];
       while (have && npre < C::STAGES) {
         const int s = npre;
-        mbar_arrive_expect_tx(bar_full + 8 * s, kWTileBytes + C::B_BYTES);
-        bulk_g2s(sbase + C::B_REGION + s * kWTileBytes, w_src(u, g), kWTileBytes, bar_full + 8 * s, pol_w);
+        mbar_arrive_expect_tx(bar_full + 8 * s, kStageTx);
+        issue_w(s, u.tile, g);
+        QOQ_TRACE_AT(p, 16 + npre, 0);
         pre_tile[npre] = u.tile;
         pre_g[npre] = g;
         issued_mask |= 1u << s;
@@ -270,19 +317,17 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1) gemm_kernel(const __grid_
         }
       }
       grid_dep_wait();
-      for (int i = 0; i < npre; ++i) {
-        Unit uu{pre_tile[i], 0, 0};
-        bulk_g2s(sbase + i * C::B_BYTES, x_src(uu, pre_g[i]), C::B_BYTES, bar_full + 8 * i, pol_x);
-      }
+      for (int i = 0; i < npre; ++i) issue_x(i, pre_tile[i], pre_g[i]);
       uint32_t gi = npre;
       while (have) {
         const int s = gi % C::STAGES;
         const uint32_t ph = (gi / C::STAGES) & 1;
         if (!wait_bar(bar_empty + 8 * s, ph ^ 1, p)) break;
         if (!(p.fault == 1 && gi == (uint32_t)C::STAGES + 1)) {  // test hook: skip one stage
-          mbar_arrive_expect_tx(bar_full + 8 * s, kWTileBytes + C::B_BYTES);
-          bulk_g2s(sbase + C::B_REGION + s * kWTileBytes, w_src(u, g), kWTileBytes, bar_full + 8 * s, pol_w);
-          bulk_g2s(sbase + s * C::B_BYTES, x_src(u, g), C::B_BYTES, bar_full + 8 * s, pol_x);
+          mbar_arrive_expect_tx(bar_full + 8 * s, kStageTx);
+          issue_w(s, u.tile, g);
+          issue_x(s, u.tile, g);
+          QOQ_TRACE_AT(p, 16 + (int)gi, 0);
           issued_mask |= 1u << s;
           issued_par = (issued_par & ~(1u << s)) | (ph << s);
         } else {
@@ -301,51 +346,64 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1) gemm_kernel(const __grid_
     __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer --
-    if (lane == 0) {
-      grid_dep_wait();
-      UnitIter iter;
-      iter.init(p);
-      Unit u;
-      uint32_t gi = 0, chunk = 0;
-      bool ok = true;
-      while (ok && iter.next(p, u)) {
-        for (int c0 = u.g0; c0 < u.g1; c0 += kFoldGroups) {
-          const int c1 = min(u.g1, c0 + kFoldGroups);
-          const int b = chunk & 1;
-          if (!wait_bar(bar_accempty + 8 * b, ((chunk >> 1) & 1) ^ 1, p)) {
+    // The whole warp walks the loop; lane 0 waits and broadcasts the outcome,
+    // one elected lane issues the MMAs and commits.
+    grid_dep_wait();
+    UnitIter iter;
+    iter.init(p);
+    Unit u;
+    uint32_t gi = 0, chunk = 0;
+    bool ok = true;
+    while (ok && iter.next(p, u)) {
+      for (int c0 = u.g0; c0 < u.g1; c0 += kFoldGroups) {
+        const int c1 = min(u.g1, c0 + kFoldGroups);
+        const int b = chunk % C::NACC;
+        int w_ok = 1;
+        if (lane == 0) w_ok = wait_bar(bar_accempty + 8 * b, ((chunk / C::NACC) & 1) ^ 1, p);
+        if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_base = tmem + b * C::ACC_COLS;
+        for (int g = c0; g < c1; ++g, ++gi) {
+          const int s = gi % C::STAGES;
+          const int a = gi % kNABuf;
+          // the dequant slot of this group waited for the stage's copies before
+          // arriving, so A-full also means the B tile is in shared memory
+          if (lane == 0) w_ok = wait_bar(bar_afull + 8 * a, (gi / kNABuf) & 1, p);
+          if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t d_tmem = tmem + b * BN;
-          for (int g = c0; g < c1; ++g, ++gi) {
-            const int s = gi % C::STAGES;
-            const int a = gi % C::NABUF;
-            if (!wait_bar(bar_afull + 8 * a, (gi / C::NABUF) & 1, p) ||
-                !wait_bar(bar_full + 8 * s, (gi / C::STAGES) & 1, p)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t b_base = sbase + s * C::B_BYTES;
+          if (lane == 0) QOQ_TRACE_AT(p, 128 + (int)gi, 0);
+          const uint32_t b_base = sbase + C::B_OFF + s * C::B_BYTES;
+          if (lane == 0) QOQ_TRACE_AT(p, 800 + (int)gi, 0);
+          if (elect_one()) {
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
               const uint32_t b_addr = b_base + (j >> 2) * (BN * 128) + (j & 3) * 32;
-              tc_mma_ts(d_tmem, tmem + C::ACOL0 + a * 64 + 8 * j, desc_sw128(b_addr), C::IDESC,
-                        (g > c0 || j > 0) ? 1u : 0u);
+              const int r = j % C::R;
+              tc_mma_ts(d_base + r * BN, tmem + kACol0 + a * 64 + 8 * j, desc_sw128(b_addr), C::IDESC,
+                        (g > c0 || j >= C::R) ? 1u : 0u);
             }
             tc_commit(bar_empty + 8 * s);
             tc_commit(bar_aempty + 8 * a);
           }
-          if (!ok) break;
-          tc_commit(bar_accfull + 8 * b);
-          ++chunk;
+          __syncwarp();
+          if (lane == 0) QOQ_TRACE_AT(p, 900 + (int)gi, 0);
         }
+        if (!ok) break;
+        if (elect_one()) tc_commit(bar_accfull + 8 * b);
+        __syncwarp();
+        ++chunk;
       }
-      // all MMAs issued by this thread complete before TMEM is released
-      tc_commit(bar_drain);
-      wait_bar(bar_drain, 0, p, false);
     }
+    // all MMAs issued by this warp complete before TMEM is released
+    if (elect_one()) tc_commit(bar_drain);
+    __syncwarp();
+    if (lane == 0) wait_bar(bar_drain, 0, p, false);
     __syncwarp();
   } else if (warp < C::EPI_WARP0) {
     // ------------------------------------------------------------- dequant --
@@ -353,6 +411,7 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1) gemm_kernel(const __grid_
     const int quad = warp & 3;
     const int slot = (warp - 2) >> 2;
     const int row = quad * 32 + lane;
+    const int stid = ((warp - 2) & 3) * 32 + lane;  // 0..127 within the slot
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     UnitIter iter;
     iter.init(p);
@@ -363,14 +422,36 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1) gemm_kernel(const __grid_
       for (int g = u.g0; g < u.g1; ++g, ++gi) {
         if ((int)(gi % C::NSLOT) != slot) continue;
         const int s = gi % C::STAGES;
-        const int a = gi % C::NABUF;
+        const int a = gi % kNABuf;
         if (!wait_bar(bar_full + 8 * s, (gi / C::STAGES) & 1, p) ||
-            !wait_bar(bar_aempty + 8 * a, ((gi / C::NABUF) & 1) ^ 1, p)) {
+            !wait_bar(bar_aempty + 8 * a, ((gi / kNABuf) & 1) ^ 1, p)) {
           ok = false;
           break;
         }
         tc_fence_after();  // the MMAs that read this A buffer are complete
-        const uint8_t* wt = smem + C::B_REGION + s * kWTileBytes;
+        if (quad == 0 && lane == 0) QOQ_TRACE_AT(p, 256 + (int)gi, 0);
+        if (C::IN_KERNEL_B) {
+          // int8 [BN][128] tile -> fp16 B operand: two [BN][64] 128B-swizzled halves
+          const uint8_t* x8 = smem + C::X8_OFF + s * C::X8_BYTES;
+          uint8_t* bt = smem + C::B_OFF + s * C::B_BYTES;
+#pragma unroll
+          for (int i = 0; i < BN / 16; ++i) {
+            const int q = stid + i * 128;  // 16-byte int8 chunk: row q / 8, channels 16 (q % 8) ..
+            const int r = q >> 3, kc = q & 7;
+            const uint4 v = *reinterpret_cast<const uint4*>(x8 + q * 16);
+            uint32_t h[8];
+            int8x4_to_half2x2(v.x, h[0], h[1]);
+            int8x4_to_half2x2(v.y, h[2], h[3]);
+            int8x4_to_half2x2(v.z, h[4], h[5]);
+            int8x4_to_half2x2(v.w, h[6], h[7]);
+            const int c = 2 * (kc & 3);  // first 16-byte fp16 chunk inside the 64-channel half
+            uint8_t* line = bt + (kc >> 2) * (BN * 128) + r * 128;
+            *reinterpret_cast<uint4*>(line + ((c ^ (r & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+            *reinterpret_cast<uint4*>(line + (((c + 1) ^ (r & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
+          }
+          fence_proxy_async_smem();  // generic-proxy writes -> the MMA's async-proxy reads
+        }
+        const uint8_t* wt = smem + C::W_OFF + s * kWTileBytes;
         const uint32_t s2 = wt[row], z = wt[128 + row];
         // sc0 = s2 * 2^11 (codes at bit 0), sc4 = s2 * 2^7 (codes at bit 4),
         // c = -(z * s2) * 2^-13; all exact in fp16 (s2 <= 16, z * s2 <= 240)
@@ -391,7 +472,7 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1) gemm_kernel(const __grid_
             out[4 * w + 2] = dequant_pair(y & 0x000F000Fu, sc0, cz);  // channels 8w + 4, 5
             out[4 * w + 3] = dequant_pair(y & 0x00F000F0u, sc4, cz);  // channels 8w + 6, 7
           }
-          tmem_st16(tmem + lane_base + C::ACOL0 + a * 64 + c * 16, out);
+          tmem_st16(tmem + lane_base + kACol0 + a * 64 + c * 16, out);
         }
         tmem_wait_st();
         tc_fence_before();
@@ -399,6 +480,7 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1) gemm_kernel(const __grid_
         if (lane == 0) {
           mbar_arrive(bar_afull + 8 * a);
           mbar_arrive(bar_empty + 8 * s);
+          if (quad == 0) QOQ_TRACE_AT(p, 384 + (int)gi, 0);
         }
       }
     }
@@ -408,7 +490,7 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1) gemm_kernel(const __grid_
     const int e = warp - C::EPI_WARP0;
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
-    const int col0 = (e >> 2) * C::EPI_COLS;  // this warp's accumulator columns
+    const int tok0 = (e >> 2) * C::EPI_TOK;  // this thread's tokens within the tile
     const int etid = threadIdx.x - C::EPI_WARP0 * 32;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     volatile int* last_flag = reinterpret_cast<volatile int*>(smem + C::FLAG_OFF);
@@ -416,39 +498,45 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1) gemm_kernel(const __grid_
     iter.init(p);
     Unit u;
     uint32_t chunk = 0;
+    int unit_no = 0;
     bool ok = true;  // once false, keep the control flow (named barriers) but do no work
     while (iter.next(p, u)) {
       const int nt = u.tile / p.MT, mt = u.tile % p.MT;
       const int n = nt * kTileN + row;
-      int32_t run[C::EPI_COLS];
+      int32_t run[C::EPI_TOK];
 #pragma unroll
-      for (int i = 0; i < C::EPI_COLS; ++i) run[i] = 0;
+      for (int i = 0; i < C::EPI_TOK; ++i) run[i] = 0;
       for (int c0 = u.g0; c0 < u.g1; c0 += kFoldGroups, ++chunk) {
-        const int b = chunk & 1;
-        if (ok) ok = wait_bar(bar_accfull + 8 * b, (chunk >> 1) & 1, p);
+        const int b = chunk % C::NACC;
+        if (ok) ok = wait_bar(bar_accfull + 8 * b, (chunk / C::NACC) & 1, p);
+        if (e == 0 && lane == 0) QOQ_TRACE_AT(p, 512 + (int)chunk, 0);
         if (ok) {
           tc_fence_after();
 #pragma unroll
-          for (int piece = 0; piece < C::EPI_COLS / 16; ++piece) {
-            uint32_t v[16];
-            tmem_ld16_wait(tmem + lane_base + b * BN + col0 + piece * 16, v);
+          for (int r = 0; r < C::R; ++r) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              run[piece * 16 + i] += __float2int_rn(__uint_as_float(v[i]) * kAccScale);
+            for (int piece = 0; piece < C::EPI_TOK / 16; ++piece) {
+              uint32_t v[16];
+              tmem_ld16_wait(tmem + lane_base + b * C::ACC_COLS + r * BN + tok0 + piece * 16, v);
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                run[piece * 16 + i] += __float2int_rn(__uint_as_float(v[i]) * kAccScale);
+            }
           }
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar_accempty + 8 * b);
+          if (e == 0 && lane == 0) QOQ_TRACE_AT(p, 576 + (int)chunk, 0);
         }
       }
       if (u.g0 == 0 && u.g1 == p.G) {
-        if (ok) write_tile_out<C::EPI_COLS>(p, run, mt * BN + col0, n);
+        if (ok) write_tile_out<C::EPI_TOK>(p, run, mt * BN + tok0, n);
       } else {
         const int sk = u.tile - p.T_dp;
-        int32_t* part = p.sk_acc + (size_t)sk * BN * kTileN + (size_t)col0 * kTileN;
+        int32_t* part = p.sk_acc + (size_t)sk * BN * kTileN + (size_t)tok0 * kTileN;
         if (ok) {
 #pragma unroll
-          for (int i = 0; i < C::EPI_COLS; ++i) red_add_relaxed(part + i * kTileN + row, run[i]);
+          for (int i = 0; i < C::EPI_TOK; ++i) red_add_relaxed(part + i * kTileN + row, run[i]);
         }
         // The barrier orders every epilogue thread's partial sums before one
         // thread's acq_rel count update (release is cumulative over the
@@ -460,36 +548,44 @@ __global__ void __launch_bounds__(Cfg<BN>::THREADS, 1) gemm_kernel(const __grid_
           if (ok) {
             const int add = u.g1 - u.g0;
             last = (atom_add_acq_rel(p.sk_cnt + sk, add) + add == p.G) ? 1 : 0;
+            if (last) p.sk_cnt[sk] = 0;  // every contributor has counted: reset for the next call
           }
           *last_flag = last;
         }
         epi_bar_sync<C::NEPI * 32>();
         if (ok && *last_flag) {
 #pragma unroll
-          for (int i = 0; i < C::EPI_COLS; ++i) run[i] = ld_relaxed(part + i * kTileN + row);
-          write_tile_out<C::EPI_COLS>(p, run, mt * BN + col0, n);
+          for (int i = 0; i < C::EPI_TOK; ++i) {
+            run[i] = ld_relaxed(part + i * kTileN + row);
+            part[i * kTileN + row] = 0;  // leave the workspace zeroed
+          }
+          write_tile_out<C::EPI_TOK>(p, run, mt * BN + tok0, n);
         }
       }
+      if (e == 0 && lane == 0) QOQ_TRACE_AT(p, 640 + unit_no, 0);
+      ++unit_no;
     }
   }
 
   tc_fence_before();
+  if (lane == 0) QOQ_TRACE_AT(p, 700 + 2 * warp, 0);
   __syncthreads();
+  if (lane == 0) QOQ_TRACE_AT(p, 701 + 2 * warp, 0);
+  if (threadIdx.x == 0) QOQ_TRACE_AT(p, 2, 0);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
 }
 
-// fp16 copy of Xq in the B-operand layout, and the per-call clearing of the
-// workspace header and split-K state.  Layout of xh: [MT][G][2][BN][64] fp16,
-// each [BN][64] block 128B-swizzled (16-byte chunk c of row r stored at chunk
-// c ^ (r & 7)), rows m >= M zero.
+// fp16 copy of Xq in the B-operand layout for 128-token tiles: [MT][G][2][128][64]
+// fp16, each [128][64] block 128B-swizzled (16-byte chunk c of row r stored at
+// chunk c ^ (r & 7)), rows m >= M zero.
 __global__ void __launch_bounds__(256) convert_kernel(const ConvertParams c) {
-  grid_dep_launch_dependents();
+  grid_dep_launch_dependents();  // the GEMM may launch and start streaming weights
+  grid_dep_wait();               // Xq comes from the preceding kernel
   const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long stride = (long long)gridDim.x * blockDim.x;
-  for (long long i = tid; i < c.zero_count; i += stride) c.zero_words[i] = 0;
   const int kc_per_row = c.K / 16;
   const int G = c.K / kGroup;
   const long long total = (long long)c.MT * c.BN * kc_per_row;
@@ -529,8 +625,15 @@ cudaError_t set_smem_attr_once() {
   return e;
 }
 
+cudaLaunchAttribute pdl_attr() {
+  cudaLaunchAttribute a;
+  a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a.val.programmaticStreamSerializationAllowed = 1;
+  return a;
+}
+
 template <int BN>
-cudaError_t launch_gemm_bn(const GemmParams& p, cudaStream_t s) {
+cudaError_t launch_gemm_bn(const GemmParams& p, const CUtensorMap& xmap, cudaStream_t s) {
   using C = Cfg<BN>;
   cudaError_t e = set_smem_attr_once<BN>();
   if (e != cudaSuccess) return e;
@@ -539,12 +642,43 @@ cudaError_t launch_gemm_bn(const GemmParams& p, cudaStream_t s) {
   cfg.blockDim = dim3(C::THREADS);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[1] = {pdl_attr()};
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_kernel<BN>, p);
+  return cudaLaunchKernelEx(&cfg, gemm_kernel<BN>, p, xmap);
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// dependency on libcuda).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+// 2D map over int8 Xq [M][K]: boxes of 128 channels x BN tokens, rows past M
+// read as zero.
+cudaError_t make_xq_map(CUtensorMap* map, const int8_t* Xq, int M, int K, int BN) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+  const cuuint64_t strides[1] = {(cuuint64_t)K};
+  const cuuint32_t box[2] = {(cuuint32_t)kGroup, (cuuint32_t)BN};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(Xq), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 }  // namespace
@@ -552,7 +686,7 @@ cudaError_t launch_gemm_bn(const GemmParams& p, cudaStream_t s) {
 cudaError_t launch_gemm(int M, int N, int K, const int8_t* Xq, const uint16_t* sx,
                         const uint8_t* packed, const uint16_t* s1, uint16_t* Y, int32_t* acc_debug,
                         void* ws, int num_sms, unsigned long long timeout_ns, int fault,
-                        cudaStream_t s) {
+                        unsigned call_id, unsigned long long* trace, cudaStream_t s) {
   const int BN = gemm_bn_for_m(M);
   const WsLayout L = gemm_ws_layout(M, N, K);
   GemmParams p = {};
@@ -588,27 +722,40 @@ cudaError_t launch_gemm(int M, int N, int K, const int8_t* Xq, const uint16_t* s
   p.acc_debug = acc_debug;
   p.timeout_ns = timeout_ns;
   p.fault = fault;
+  p.call_id = call_id;
+  p.trace = trace;
 
-  ConvertParams c = {};
-  c.Xq = Xq;
-  c.xh = reinterpret_cast<uint16_t*>(w + L.xh_off);
-  c.zero_words = reinterpret_cast<int32_t*>(w);
-  c.zero_count = (long long)(L.acc_off + (size_t)p.T_sk * BN * kTileN * 4) / 4;
-  c.M = M;
-  c.K = K;
-  c.BN = BN;
-  c.MT = p.MT;
-  const long long work = std::max<long long>((long long)p.MT * BN * (K / 16), c.zero_count);
-  const int cblocks = (int)std::max<long long>(1, std::min<long long>((work + 255) / 256, (long long)P0 * 4));
-  convert_kernel<<<cblocks, 256, 0, s>>>(c);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  CUtensorMap xmap;
+  std::memset(&xmap, 0, sizeof(xmap));
+  if (BN <= 64) {
+    cudaError_t e = make_xq_map(&xmap, Xq, M, K, BN);
+    if (e != cudaSuccess) return e;
+  } else {
+    ConvertParams c = {};
+    c.Xq = Xq;
+    c.xh = reinterpret_cast<uint16_t*>(w + L.xh_off);
+    c.M = M;
+    c.K = K;
+    c.BN = BN;
+    c.MT = p.MT;
+    const long long work = (long long)p.MT * BN * (K / 16);
+    const int cblocks = (int)std::max<long long>(1, std::min<long long>((work + 255) / 256, (long long)P0 * 4));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cblocks);
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1] = {pdl_attr()};
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, convert_kernel, c);
+    if (e != cudaSuccess) return e;
+  }
 
   switch (BN) {
-    case 16: return launch_gemm_bn<16>(p, s);
-    case 32: return launch_gemm_bn<32>(p, s);
-    case 64: return launch_gemm_bn<64>(p, s);
-    default: return launch_gemm_bn<128>(p, s);
+    case 16: return launch_gemm_bn<16>(p, xmap, s);
+    case 32: return launch_gemm_bn<32>(p, xmap, s);
+    case 64: return launch_gemm_bn<64>(p, xmap, s);
+    default: return launch_gemm_bn<128>(p, xmap, s);
   }
 }
 

@@ -20,7 +20,7 @@ constexpr int kFoldGroups = 8;     // fp32 TMEM partials are folded to int32 eve
 constexpr int kMaxSkTiles = 512;   // upper bound of split-K tiles per call (workspace sizing)
 constexpr int kMaxGrid = 256;      // upper bound of persistent CTAs per call
 
-constexpr int kWsHeaderBytes = 256;  // [0] status, [1] abort flag
+constexpr int kWsHeaderBytes = 256;  // [0] sticky status, [1] id of a call that aborted
 
 // Token-tile width (MMA N) used for a given M.
 inline int gemm_bn_for_m(int M) {
@@ -37,6 +37,8 @@ struct WsLayout {
   size_t cnt_off, acc_off, xh_off, total;
 };
 
+// Header, split-K tile counters, split-K int32 partial tiles, and (128-token
+// tiles only) the fp16 B-operand copy of Xq.
 inline WsLayout gemm_ws_layout(int M, int N, int K) {
   const int BN = gemm_bn_for_m(M);
   const long long MT = (M + BN - 1) / BN;
@@ -46,12 +48,15 @@ inline WsLayout gemm_ws_layout(int M, int N, int K) {
   L.cnt_off = kWsHeaderBytes;
   L.acc_off = align_up(L.cnt_off + (size_t)skmax * 4, 256);
   L.xh_off = align_up(L.acc_off + (size_t)skmax * BN * kTileN * 4, 1024);
-  L.total = align_up(L.xh_off + (size_t)MT * K * BN * 2, 256);
+  const size_t xh_bytes = BN > 64 ? (size_t)MT * K * BN * 2 : 0;
+  L.total = align_up(L.xh_off + xh_bytes, 256);
   return L;
 }
 
 // --------------------------------------------------------------- schedule --
 // Tiles: tile t -> weight tile nt = t / MT, token tile mt = t % MT.
+// Split-K state lives in the workspace and is left zeroed by every call that
+// completes (the last contributor of a tile clears its partial sums and count).
 // Tiles [0, T_dp) are processed whole, round-robin over the P CTAs; the
 // remaining T_sk tiles are split along K: their T_sk * G group-iterations are
 // cut into P equal contiguous ranges (stream-K), and partial int32 sums meet
@@ -70,13 +75,35 @@ struct GemmParams {
   long long I_sk;
   unsigned long long timeout_ns;
   int fault;
+  unsigned call_id;           // non-zero, distinct per call: the abort word names the aborting call
+  unsigned long long* trace;  // per-CTA event clock, only with -DQOQ_TRACE (else unused)
 };
+
+// Event tracing for pipeline studies: compiled in only with -DQOQ_TRACE.
+// Per CTA kTraceSlots 64-bit slots of %globaltimer (ns, common to all warps):
+// [0], [1] start, [2] end; producer issue of group i at 16+i; MMA issue at
+// 128+i; dequant start/end (slot 0..3, quadrant 0) at 256+i / 384+i; epilogue
+// chunk ready/folded at 512+c / 576+c; unit done at 640+u.
+constexpr int kTraceSlots = 1024;
+#ifdef QOQ_TRACE
+#define QOQ_TRACE_AT(p, slot, value)                                                     \
+  do {                                                                                    \
+    if ((p).trace && (slot) < kTraceSlots) {                                              \
+      (void)(value);                                                                      \
+      unsigned long long qoq_t_;                                                          \
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(qoq_t_));                         \
+      (p).trace[(size_t)blockIdx.x * kTraceSlots + (slot)] = qoq_t_;                      \
+    }                                                                                     \
+  } while (0)
+#else
+#define QOQ_TRACE_AT(p, slot, value) \
+  do {                               \
+  } while (0)
+#endif
 
 struct ConvertParams {
   const int8_t* Xq;
   uint16_t* xh;
-  int32_t* zero_words;  // workspace region cleared each call (header + split-K state)
-  long long zero_count; // number of int32 words to clear
   int M, K, BN, MT;
 };
 
@@ -90,6 +117,6 @@ cudaError_t launch_unpack(int N, int K, const uint8_t* packed, uint8_t* q4, uint
 cudaError_t launch_gemm(int M, int N, int K, const int8_t* Xq, const uint16_t* sx,
                         const uint8_t* packed, const uint16_t* s1, uint16_t* Y, int32_t* acc_debug,
                         void* ws, int num_sms, unsigned long long timeout_ns, int fault,
-                        cudaStream_t s);
+                        unsigned call_id, unsigned long long* trace, cudaStream_t s);
 
 }  // namespace qoq
