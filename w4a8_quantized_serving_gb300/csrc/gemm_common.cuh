@@ -1,0 +1,388 @@
+// gemm_common.cuh -- pieces shared by the two W4A8 GEMM kernels (the
+// register-fed decode kernel for token tiles of <= 64 rows and the
+// bulk-copy-fed kernel for 128-token tiles): exact dequant arithmetic, the
+// work schedule, bounded waits, and the MMA-issue and epilogue roles.
+//
+// Exactness (QServe talk write-up, "Quantized Matrix Multiplication (GEMM)
+// Kernel on GPUs": the product runs on tensor cores in 8-bit integers):
+// sm_103a has no integer tcgen05 MMA, so the int8 x int8 product runs on
+// tcgen05.mma kind::f16 with operands that are small integers times a power of
+// two (exact in fp16).  Each product and each partial sum below 2^24 units is
+// exact in the fp32 accumulator; the epilogue folds the TMEM partials into
+// int32 every 8 groups (1024 channels, 127 * 127 * 1024 < 2^24).
+#pragma once
+
+#include <cuda_fp16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace qoq {
+
+constexpr int kTmemCols = 512;
+constexpr int kStatusTimeout = 7;  // QOQ_ERR_DEVICE_TIMEOUT
+// The A operand carries w8 * 2^-13 (see dequant_pair); the epilogue undoes it.
+constexpr float kAccScale = 8192.0f;
+constexpr int kSmemBudget = 227 * 1024;  // per-CTA dynamic shared memory limit
+
+// tcgen05 instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B
+// fp16 (bits 7-9, 10-12 = 0), both K-major (bits 15, 16 = 0), N >> 3 in bits
+// 17-22, M >> 4 in bits 24-28; M = 128 (one weight tile).
+__host__ __device__ constexpr uint32_t mma_idesc(int n) {
+  return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kTileN >> 4) << 24);
+}
+
+// Exact dequant of a pair of 4-bit codes (QServe "subtraction after
+// multiplication": the zero point enters after the scale, as one packed FMA).
+// `h` holds the two codes q in the same 4-bit field of each fp16 half, at bit
+// p (p = 0 or 4) and nothing else, i.e. the fp16 subnormals q * 2^(p-24).
+// With sc = s2 * 2^(11-p) and c = -(z * s2) * 2^-13 (both exact in fp16),
+//   fma(h, sc, c) = (q - z) * s2 * 2^-13
+// computed exactly then rounded once; the result is representable (|.| <= 240
+// units of 2^-13, and every non-zero value is a normal fp16), so it is exact.
+__device__ __forceinline__ uint32_t dequant_pair(uint32_t h, uint32_t sc, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(h), "r"(sc), "r"(c));
+  return d;
+}
+
+// Per-row constants of dequant_pair for a group with scale s2 and zero z:
+// sc0 = s2 * 2^11 (codes at bit 0), sc4 = s2 * 2^7 (codes at bit 4),
+// c = -(z * s2) * 2^-13, each duplicated into both fp16 halves.
+struct DequantConsts {
+  uint32_t sc0, sc4, cz;
+};
+
+__device__ __forceinline__ DequantConsts dequant_consts(uint32_t s2, uint32_t z) {
+  DequantConsts k;
+  k.sc0 = (uint32_t)__half_as_ushort(__float2half_rn((float)(s2 << 11))) * 0x00010001u;
+  k.sc4 = (uint32_t)__half_as_ushort(__float2half_rn((float)(s2 << 7))) * 0x00010001u;
+  k.cz = (uint32_t)__half_as_ushort(__float2half_rn(-(float)(z * s2) * (1.0f / 8192.0f))) * 0x00010001u;
+  return k;
+}
+
+// 16 packed code bytes (32 channels, layout of include/qoq.h) -> 16 fp16x2
+// words in channel order, ready for tcgen05.st (column c holds channels 2c, 2c+1).
+__device__ __forceinline__ void dequant_chunk(const uint4& v, const DequantConsts& k, uint32_t (&out)[16]) {
+  const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const uint32_t x = wv[w], y = wv[w] >> 8;
+    out[4 * w + 0] = dequant_pair(x & 0x000F000Fu, k.sc0, k.cz);  // channels 8w + 0, 1
+    out[4 * w + 1] = dequant_pair(x & 0x00F000F0u, k.sc4, k.cz);  // channels 8w + 2, 3
+    out[4 * w + 2] = dequant_pair(y & 0x000F000Fu, k.sc0, k.cz);  // channels 8w + 4, 5
+    out[4 * w + 3] = dequant_pair(y & 0x00F000F0u, k.sc4, k.cz);  // channels 8w + 6, 7
+  }
+}
+
+// Four int8 lanes of `x` -> two fp16x2 (exact): the biased byte u = b ^ 0x80
+// becomes the fp16 1024 + u through its mantissa, and 1024 + 128 is removed.
+__device__ __forceinline__ void int8x4_to_half2x2(uint32_t x, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = x ^ 0x80808080u;
+  const uint32_t bias = 0x64806480u;  // fp16 (1152, 1152)
+  uint32_t a, b;
+  asm("prmt.b32 %0, %1, %2, 0x7170;" : "=r"(a) : "r"(u), "r"(0x64646464u));
+  asm("prmt.b32 %0, %1, %2, 0x7372;" : "=r"(b) : "r"(u), "r"(0x64646464u));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(bias));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(bias));
+}
+
+// 16 int8 activations (one 16-byte chunk: row r, channels 16 kc .. 16 kc + 15
+// of a 128-channel group) -> fp16 into the B operand tile: two [BN][64]
+// halves, K-major, 128-byte swizzled (16-byte chunk c of row r at c ^ (r & 7)).
+__device__ __forceinline__ void store_b_chunk(uint8_t* btile, int bn, int r, int kc, const uint4& v) {
+  uint32_t h[8];
+  int8x4_to_half2x2(v.x, h[0], h[1]);
+  int8x4_to_half2x2(v.y, h[2], h[3]);
+  int8x4_to_half2x2(v.z, h[4], h[5]);
+  int8x4_to_half2x2(v.w, h[6], h[7]);
+  const int c = 2 * (kc & 3);  // first 16-byte fp16 chunk inside the 64-channel half
+  uint8_t* line = btile + (kc >> 2) * (bn * 128) + r * 128;
+  *reinterpret_cast<uint4*>(line + ((c ^ (r & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+  *reinterpret_cast<uint4*>(line + (((c + 1) ^ (r & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
+}
+
+// Shared-memory matrix descriptor: 128-byte swizzle, K-major, 8-row groups
+// 1024 B apart (SBO), version 1 (bit 46), layout code 2 (bits 61-63).
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// ------------------------------------------------------------------ schedule --
+
+struct Unit {
+  int tile, g0, g1;
+};
+
+// The CTA's sequence of (tile, group range) units: whole tiles first, then
+// its stream-K range.  Every role walks the same sequence.
+struct UnitIter {
+  int dp_next;
+  long long it, it_end;
+  __device__ __forceinline__ void init(const GemmParams& p) {
+    dp_next = blockIdx.x;
+    it = (long long)blockIdx.x * p.I_sk / p.P;
+    it_end = (long long)(blockIdx.x + 1) * p.I_sk / p.P;
+  }
+  __device__ __forceinline__ bool next(const GemmParams& p, Unit& u) {
+    if (dp_next < p.T_dp) {
+      u.tile = dp_next;
+      u.g0 = 0;
+      u.g1 = p.G;
+      dp_next += p.P;
+      return true;
+    }
+    if (it < it_end) {
+      const long long sk = it / p.G;
+      const int g0 = (int)(it - sk * p.G);
+      const long long rem = it_end - it;
+      const long long g1 = rem < (long long)(p.G - g0) ? g0 + rem : (long long)p.G;
+      u.tile = p.T_dp + (int)sk;
+      u.g0 = g0;
+      u.g1 = (int)g1;
+      it += g1 - g0;
+      return true;
+    }
+    return false;
+  }
+};
+
+// ------------------------------------------------------------------- waits --
+
+// Bounded wait on an mbarrier phase.  Returns false if the wait ran out (the
+// timeout is recorded) or, when honor_abort, if another thread of this call
+// already recorded one.  The loop polls only the barrier for the first ~100k
+// cycles; the global timer and the abort word in global memory are read after
+// that, so a normal hand-off never waits behind a global load.
+__device__ __noinline__ inline bool wait_slow(uint32_t bar, uint32_t parity, const GemmParams& p,
+                                              bool honor_abort) {
+  volatile unsigned* abort_word = reinterpret_cast<volatile unsigned*>(p.status + 1);
+  const long long c0 = clock64();
+  uint64_t t0 = 0;
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255) == 0 && clock64() - c0 > 100000) {
+      const uint64_t now = global_timer_ns();
+      if (t0 == 0) t0 = now;
+      if (honor_abort && *abort_word == p.call_id) return false;
+      if (now - t0 > p.timeout_ns) {
+        atomicExch(p.status, kStatusTimeout);
+        atomicExch(reinterpret_cast<unsigned*>(p.status + 1), p.call_id);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const GemmParams& p,
+                                         bool honor_abort = true) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_slow(bar, parity, p, honor_abort);
+}
+
+// Lane 0 waits, the warp learns the outcome (keeps the warp converged).
+__device__ __forceinline__ bool warp_wait_bar(uint32_t bar, uint32_t parity, const GemmParams& p) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, p);
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+template <int NTHREADS>
+__device__ __forceinline__ void named_bar_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(NTHREADS) : "memory");
+}
+
+// ------------------------------------------------------------------ output --
+
+// Y[m, n] for the COLS tokens m = m0 .. m0+COLS-1 held by this thread.
+template <int COLS>
+__device__ __forceinline__ void write_tile_out(const GemmParams& p, const int32_t (&run)[COLS], int m0,
+                                               int n) {
+  const float s1f = __half2float(__ushort_as_half(p.s1[n]));
+#pragma unroll
+  for (int i = 0; i < COLS; ++i) {
+    const int m = m0 + i;
+    if (m < p.M) {
+      const float sxf = __half2float(__ushort_as_half(p.sx[m]));
+      const float y = (float)run[i] * (sxf * s1f);
+      p.Y[(size_t)m * p.N + n] = __half_as_ushort(__float2half_rn(y));
+      if (p.acc_debug) p.acc_debug[(size_t)m * p.N + n] = run[i];
+    }
+  }
+}
+
+// ------------------------------------------------------------- MMA issuer --
+// One converged warp; lane 0 waits, one elected lane issues 8 MMAs per group
+// (M=128, N=BN, K=16; A = dequantized weights in TMEM, B = fp16 activations
+// in shared memory) and commits.  A diverged single thread issues tcgen05 ops
+// about 2.5x slower, and an mbarrier wait costs ~100 cycles even on a completed
+// phase, so the loop waits once per group.  `b_tile(gi, a)` gives the shared
+// address of group gi's B tile; the group's A-full barrier covers it too.
+// After each MMA group: commits to `bar_aempty[a]` and to `extra_commit(gi)`
+// (0 = none).
+template <int BN, int NACC, int NABUF, int ACOL0, typename BTile, typename ExtraCommit>
+__device__ __forceinline__ void mma_role(const GemmParams& p, uint32_t tmem, uint32_t bar_afull,
+                                         uint32_t bar_aempty, uint32_t bar_accfull, uint32_t bar_accempty,
+                                         uint32_t bar_drain, BTile b_tile, ExtraCommit extra_commit) {
+  constexpr uint32_t kIdesc = mma_idesc(BN);
+  UnitIter iter;
+  iter.init(p);
+  Unit u;
+  uint32_t gi = 0, chunk = 0;
+  bool ok = true;
+  while (ok && iter.next(p, u)) {
+    for (int c0 = u.g0; c0 < u.g1; c0 += kFoldGroups) {
+      const int c1 = min(u.g1, c0 + kFoldGroups);
+      const int b = chunk % NACC;
+      if (!warp_wait_bar(bar_accempty + 8 * b, ((chunk / NACC) & 1) ^ 1, p)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem + b * BN;
+      for (int g = c0; g < c1; ++g, ++gi) {
+        const int a = gi % NABUF;
+        if (!warp_wait_bar(bar_afull + 8 * a, (gi / NABUF) & 1, p)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if ((threadIdx.x & 31) == 0) QOQ_TRACE_AT(p, 128 + (int)gi, 0);
+        const uint32_t b_base = b_tile(gi, a);
+        if (elect_one()) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t b_addr = b_base + (j >> 2) * (BN * 128) + (j & 3) * 32;
+            tc_mma_ts(d_tmem, tmem + ACOL0 + a * 64 + 8 * j, desc_sw128(b_addr), kIdesc,
+                      (g > c0 || j > 0) ? 1u : 0u);
+          }
+          tc_commit(bar_aempty + 8 * a);
+          const uint32_t xc = extra_commit(gi);
+          if (xc) tc_commit(xc);
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+      if (elect_one()) tc_commit(bar_accfull + 8 * b);
+      __syncwarp();
+      ++chunk;
+    }
+  }
+  // all MMAs issued by this warp complete before TMEM is released
+  if (elect_one()) tc_commit(bar_drain);
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) wait_bar(bar_drain, 0, p, false);
+  __syncwarp();
+}
+
+// ---------------------------------------------------------------- epilogue --
+// NEPI warps (a multiple of 4: warp w reads TMEM lanes 32 (w % 4) ..); warp e
+// owns tokens (e / 4) * TOK .. + TOK of the tile for weight row 32 (w % 4) +
+// lane.  Per fold chunk: read the fp32 accumulator, convert to int32 (exact),
+// add.  At a unit's end: write Y (whole-K tile), or add the int32 partials
+// into the workspace and let the last contributor write Y and clear them.
+template <int BN, int NEPI, int NACC>
+__device__ __forceinline__ void epilogue_role(const GemmParams& p, uint32_t tmem, int epi_warp0,
+                                              uint32_t bar_accfull, uint32_t bar_accempty,
+                                              volatile int* last_flag) {
+  constexpr int TOK = BN / (NEPI / 4);
+  static_assert(TOK % 16 == 0, "epilogue loads 16 columns at a time");
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = warp - epi_warp0;
+  const int quad = warp & 3;
+  const int row = quad * 32 + lane;
+  const int tok0 = (e >> 2) * TOK;
+  const int etid = threadIdx.x - epi_warp0 * 32;
+  const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+  UnitIter iter;
+  iter.init(p);
+  Unit u;
+  uint32_t chunk = 0;
+  int unit_no = 0;
+  bool ok = true;  // once false, keep the control flow (named barriers) but do no work
+  while (iter.next(p, u)) {
+    const int nt = u.tile / p.MT, mt = u.tile % p.MT;
+    const int n = nt * kTileN + row;
+    int32_t run[TOK];
+#pragma unroll
+    for (int i = 0; i < TOK; ++i) run[i] = 0;
+    for (int c0 = u.g0; c0 < u.g1; c0 += kFoldGroups, ++chunk) {
+      const int b = chunk % NACC;
+      if (ok) ok = wait_bar(bar_accfull + 8 * b, (chunk / NACC) & 1, p);
+      if (e == 0 && lane == 0) QOQ_TRACE_AT(p, 512 + (int)chunk, 0);
+      if (ok) {
+        tc_fence_after();
+#pragma unroll
+        for (int piece = 0; piece < TOK / 16; ++piece) {
+          uint32_t v[16];
+          tmem_ld16_wait(tmem + lane_base + b * BN + tok0 + piece * 16, v);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) run[piece * 16 + i] += __float2int_rn(__uint_as_float(v[i]) * kAccScale);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_accempty + 8 * b);
+        if (e == 0 && lane == 0) QOQ_TRACE_AT(p, 576 + (int)chunk, 0);
+      }
+    }
+    if (u.g0 == 0 && u.g1 == p.G) {
+      if (ok) write_tile_out<TOK>(p, run, mt * BN + tok0, n);
+    } else {
+      const int sk = u.tile - p.T_dp;
+      int32_t* part = p.sk_acc + (size_t)sk * BN * kTileN + (size_t)tok0 * kTileN;
+      if (ok) {
+#pragma unroll
+        for (int i = 0; i < TOK; ++i) red_add_relaxed(part + i * kTileN + row, run[i]);
+      }
+      // The barrier orders every epilogue thread's partial sums before one
+      // thread's acq_rel count update (release is cumulative over the
+      // barrier); the last contributor's acquire makes the other CTAs' sums
+      // visible, and the second barrier passes that on to its warps.
+      if (e == 0 && lane == 0) QOQ_TRACE_AT(p, 960 + 4 * (unit_no & 7) + 0, 0);
+      named_bar_sync<NEPI * 32>();
+      if (etid == 0) {
+        int last = 0;
+        if (ok) {
+          const int add = u.g1 - u.g0;
+          last = (atom_add_acq_rel(p.sk_cnt + sk, add) + add == p.G) ? 1 : 0;
+          if (last) p.sk_cnt[sk] = 0;  // every contributor has counted: reset for the next call
+        }
+        *last_flag = last;
+      }
+      named_bar_sync<NEPI * 32>();
+      if (e == 0 && lane == 0) QOQ_TRACE_AT(p, 960 + 4 * (unit_no & 7) + 2, 0);
+      if (ok && *last_flag) {
+#pragma unroll
+        for (int i = 0; i < TOK; ++i) run[i] = __ldcg(part + i * kTileN + row);
+#pragma unroll
+        for (int i = 0; i < TOK; ++i) __stcg(part + i * kTileN + row, 0);  // leave it zeroed
+        write_tile_out<TOK>(p, run, mt * BN + tok0, n);
+      }
+    }
+    if (e == 0 && lane == 0) QOQ_TRACE_AT(p, 640 + unit_no, 0);
+    ++unit_no;
+  }
+}
+
+// Opt a kernel into its dynamic shared memory once per device (not a stream
+// operation; done before any graph capture can reach it).
+template <typename Kernel>
+cudaError_t set_smem_attr_once(Kernel kernel, int bytes, uint64_t& done_mask) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 64 && (done_mask >> dev) & 1) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && dev < 64) done_mask |= 1ull << dev;
+  return e;
+}
+
+inline cudaLaunchAttribute pdl_attr() {
+  cudaLaunchAttribute a;
+  a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a.val.programmaticStreamSerializationAllowed = 1;
+  return a;
+}
+
+}  // namespace qoq

@@ -63,7 +63,8 @@ inline WsLayout gemm_ws_layout(int M, int N, int K) {
 // in the workspace, where the last contributor of a tile writes the output.
 struct GemmParams {
   const uint8_t* packed;
-  const uint16_t* xh;  // tiled fp16 copy of Xq (B operand layout)
+  const uint16_t* xh;  // tiled fp16 copy of Xq (B operand layout), 128-token tiles
+  const int8_t* xq;    // Xq itself, read directly for token tiles of <= 64 rows
   const uint16_t* sx;
   const uint16_t* s1;
   uint16_t* Y;
@@ -83,7 +84,9 @@ struct GemmParams {
 // Per CTA kTraceSlots 64-bit slots of %globaltimer (ns, common to all warps):
 // [0], [1] start, [2] end; producer issue of group i at 16+i; MMA issue at
 // 128+i; dequant start/end (slot 0..3, quadrant 0) at 256+i / 384+i; epilogue
-// chunk ready/folded at 512+c / 576+c; unit done at 640+u.
+// chunk ready/folded at 512+c / 576+c; unit done at 640+u; per-warp final
+// barrier arrive/depart at 700+2w / 701+2w; MMA warp group start/end at
+// 800+i / 900+i; split-K hand-off steps at 960+4u+{0,1,2}.
 constexpr int kTraceSlots = 1024;
 #ifdef QOQ_TRACE
 #define QOQ_TRACE_AT(p, slot, value)                                                     \
@@ -114,6 +117,7 @@ cudaError_t launch_pack(int N, int K, const uint16_t* W, uint8_t* packed, uint16
                         cudaStream_t s);
 cudaError_t launch_unpack(int N, int K, const uint8_t* packed, uint8_t* q4, uint8_t* s2, uint8_t* z,
                           cudaStream_t s);
+cudaError_t launch_gemm_decode(const GemmParams& p, int BN, cudaStream_t s);
 cudaError_t launch_gemm(int M, int N, int K, const int8_t* Xq, const uint16_t* sx,
                         const uint8_t* packed, const uint16_t* s1, uint16_t* Y, int32_t* acc_debug,
                         void* ws, int num_sms, unsigned long long timeout_ns, int fault,

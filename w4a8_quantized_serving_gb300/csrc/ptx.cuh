@@ -76,21 +76,6 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
-// 2D tiled tensor copy (TMA) global -> shared, completing on an mbarrier.
-// c0 is the innermost coordinate (its byte offset must be a multiple of 16).
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int c0, int c1, uint32_t bar,
-                                            uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
-      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(tmap), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
-      : "memory");
-}
-
-__device__ __forceinline__ void prefetch_tensormap(const void* tmap) {
-  asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
-}
-
 // Order this thread's generic-proxy shared-memory writes before later
 // async-proxy reads (tensor-core operand fetch).
 __device__ __forceinline__ void fence_proxy_async_smem() {
