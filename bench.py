@@ -22,6 +22,7 @@ check against) on the host cores instead: it is the reference arm.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -58,6 +59,32 @@ def load_peaks() -> tuple[dict, str]:
             return json.load(f), "measured"
     except (OSError, ValueError):
         return dict(FALLBACK_PEAKS), "fallback"
+
+
+GEMM_SOURCES = ["gemm.cu", "gemm_decode.cu", "gemm_common.cuh", "ptx.cuh", "internal.h"]
+
+
+def gemm_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in GEMM_SOURCES:
+        with open(os.path.join(ROOT, "w4a8_quantized_serving_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(workload: str) -> tuple[float | None, str]:
+    """DRAM bytes per GEMM launch from the committed ncu record, if the GEMM
+    sources are unchanged since it was taken (else None)."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f).get(workload)
+    except (OSError, ValueError):
+        return None, "no ncu record"
+    if not rec:
+        return None, "no ncu record for this workload"
+    if rec.get("source_sha256") != gemm_source_hash():
+        return None, "GEMM sources changed since the ncu capture"
+    return float(rec["dram_bytes_per_launch"]), rec.get("capture", "")
 
 
 def dist_env() -> tuple[int, int, int]:
@@ -371,7 +398,9 @@ def run_ours(args, c: dict) -> None:
         roof = {"bound": "tensor", "achieved": achieved, "peak": pk, "unit": "TFLOP/s",
                 "frac": achieved / pk, "traffic": args.traffic,
                 "peak_source": f"{peak_src} bf16 dense (fp16 operands run at the bf16 rate)"}
-    roof["kernel"] = "qoq_w4a8_gemm call (B-operand convert + GEMM kernel), timed alone over K launches"
+    if roof["traffic"] is None:
+        roof["traffic"], roof["traffic_source"] = recorded_traffic(c["name"])
+    roof["kernel"] = "qoq_w4a8_gemm call (the GEMM kernel; + B-operand convert for M > 64), timed alone over K launches"
     roof["algorithmic_bytes_per_launch"] = nbytes["gemm"]
     roof["ms_per_launch"] = gemm_ms
     roof["gb_per_s_algorithmic"] = nbytes["gemm"] / (gemm_ms * 1e-3) / 1e9
@@ -395,7 +424,8 @@ def run_ours(args, c: dict) -> None:
                 "h2d_bytes_per_step": 2 * M * K, "d2h_bytes_per_step": 2 * M * N,
                 "ms_per_step": e2e_ms},
         "clocks": clocks,
-        "gpu_launches": 3 * args.steps,
+        # per step: act-quant + GEMM; for M > 64 also the B-operand convert
+        "gpu_launches": (2 if M <= 64 else 3) * args.steps,
         "pack_ms": pack_ms,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -21,11 +21,16 @@ def q():
 
 
 def _edge_rows(K: int, seed: int) -> np.ndarray:
+    """Rows that stress the quantizers: zeros, constants, saturation, a row
+    whose values sit exactly on rounding ties (amax = 127 * 2^-6 makes the
+    activation scale 2^-6 and X / s_x = n + 1/2), subnormals, large values."""
     rng = np.random.default_rng(seed)
-    rows = [
+    ties = ((np.arange(K) % 254) - 127 + 0.5) * 2.0 ** -6
+    ties[0] = 127 * 2.0 ** -6
+    rows = [ties,
         np.zeros(K), np.full(K, 0.5), np.full(K, -3.0), np.linspace(-2, 2, K),
         np.where(np.arange(K) % 2 == 0, 1.0, -1.0), rng.standard_normal(K) * 1e-6,
-        np.where(np.arange(K) == 7, 60000.0, 0.0), rng.standard_normal(K) * 30.0,
+        np.where(np.arange(K) == 7, 60000.0, 0.0),
     ]
     return f16(np.stack(rows))
 
@@ -50,6 +55,10 @@ def test_act_quant_bit_exact(M, K):
 def test_pack_bit_exact_and_layout(N, K):
     W = synth.weights(N, K, 200 + N)
     W[:8] = _edge_rows(K, N) * 0.01
+    # exact level-1 ties: amax = 119 * 2^-7 makes s1 = 2^-7 and W / s1 = n + 1/2
+    wt = ((np.arange(K) % 238) - 119 + 0.5) * 2.0 ** -7
+    wt[0] = 119 * 2.0 ** -7
+    W[8] = f16(wt)
     Wd = gc.to_dev_f16(W)
     packed, s1 = q().qoq_pack_weights(Wd)
     o = gc.oracle.weight_quant(synth.bits(W), 128)

@@ -4,7 +4,8 @@
 // Fusion": every linear layer takes 8-bit activations (the write-up fuses the
 // quantizer into the preceding LayerNorm; here it is a standalone kernel).
 //   s_x[m]  = fp16_rn(fp32(max_k |X[m,k]|) / 127)        (IEEE fp32 divide)
-//   Xq[m,k] = clamp(rint(X[m,k] / s_x[m]), -127, 127)      (fp32 divide, ties even)
+//   Xq[m,k] = clamp(rint(X[m,k] / s_x[m]), -127, 127)      (fp32 divide, ties even;
+//             computed without a divide by rint_div_fp16, which gives the same codes)
 // An all-zero row gets s_x = 0 and Xq = 0.
 //
 // Each token row is owned by T threads (T a power of two, 32..1024), each
@@ -35,12 +36,12 @@ __device__ __forceinline__ float absmax8(uint4 v, float m) {
   return m;
 }
 
-__device__ __forceinline__ uint32_t quant4(const __half* h, float sf) {
+__device__ __forceinline__ uint32_t quant4(const __half* h, float sf, float rf) {
   uint32_t r = 0;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const int q = min(127, max(-127, __float2int_rn(__fdiv_rn(__half2float(h[i]), sf))));
-    r |= (uint32_t)(q & 0xff) << (8 * i);
+    const float q = fminf(127.0f, fmaxf(-127.0f, rint_div_fp16(__half2float(h[i]), sf, rf)));
+    r |= (uint32_t)((int)q & 0xff) << (8 * i);
   }
   return r;
 }
@@ -82,6 +83,7 @@ __global__ void __launch_bounds__(1024) act_quant_kernel(const uint16_t* __restr
   __half s = __float2half_rn(0.0f);
   if (amax > 0.0f) s = __float2half_rn(__fdiv_rn(amax, 127.0f));
   const float sf = __half2float(s);
+  const float rf = sf != 0.0f ? __frcp_rn(sf) : 0.0f;
   if (t == 0) sx[row] = __half_as_ushort(s);
 
   uint2* qr = reinterpret_cast<uint2*>(Xq + (size_t)row * K);
@@ -92,7 +94,7 @@ __global__ void __launch_bounds__(1024) act_quant_kernel(const uint16_t* __restr
       uint2 out = make_uint2(0, 0);
       if (sf != 0.0f) {
         const __half* h = reinterpret_cast<const __half*>(&v[i]);
-        out = make_uint2(quant4(h, sf), quant4(h + 4, sf));
+        out = make_uint2(quant4(h, sf, rf), quant4(h + 4, sf, rf));
       }
       qr[idx] = out;
     }
@@ -104,8 +106,9 @@ __global__ void __launch_bounds__(1024) act_quant_kernel(const uint16_t* __restr
 cudaError_t launch_act_quant(int M, int K, const uint16_t* X, int8_t* Xq, uint16_t* sx,
                              cudaStream_t s) {
   const int nvec = K / 8;
-  int T = 32;  // threads per row: a power of two with <= 16 vectors each
-  while (T * kMaxVecPerThread < nvec) T *= 2;
+  // threads per row: a power of two, ~4 vectors each (latency), at most 16
+  int T = 32;
+  while (T * 4 < nvec && T < 1024) T *= 2;
   const int threads = T < 128 ? 128 : T;
   const int rows_per_cta = threads / T;
   const int grid = (M + rows_per_cta - 1) / rows_per_cta;

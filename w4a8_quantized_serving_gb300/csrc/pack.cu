@@ -17,6 +17,7 @@
 #include <cuda_fp16.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace qoq {
 namespace {
@@ -75,6 +76,7 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) pack_kernel(const uint16_t
   __half s1 = __float2half_rn(0.0f);
   if (amax > 0.0f) s1 = __float2half_rn(__fdiv_rn(amax, 119.0f));
   const float s1f = __half2float(s1);
+  const float r1f = s1f != 0.0f ? __frcp_rn(s1f) : 0.0f;
   if (lane == 0) s1out[n] = __half_as_ushort(s1);
 
   const int nt = n / kTileN, r = n % kTileN;
@@ -87,7 +89,7 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) pack_kernel(const uint16_t
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       int q = 0;
-      if (s1f != 0.0f) q = min(119, max(-119, __float2int_rn(__fdiv_rn(__half2float(h[i]), s1f))));
+      if (s1f != 0.0f) q = (int)fminf(119.0f, fmaxf(-119.0f, rint_div_fp16(__half2float(h[i]), s1f, r1f)));
       q8[i] = q;
       lo = min(lo, q);
       hi = max(hi, q);

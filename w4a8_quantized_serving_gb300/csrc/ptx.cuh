@@ -184,6 +184,22 @@ __device__ __forceinline__ void tmem_ld16_wait(uint32_t taddr, uint32_t (&v)[16]
       : "memory");
 }
 
+// --------------------------------------------------------- exact rounding --
+
+// rint(x / s) with ties to even, for fp16-valued x and s > 0, without a divide.
+// The exact quotient of two fp16 values is either a half-integer or at least
+// 2^-13 away from every half-integer while |x / s| < 256; y = x * rcp_rn(s) is
+// within 2^-23 |x / s| of it, so rint(y) is right except at exact ties, which
+// one FMA detects exactly ((f + 1/2) * s has at most 20 significant bits).
+// This equals rint(fl32(x / s)) with an IEEE divide, the rule the quantizers
+// follow, because fl32(x / s) cannot cross or land on a half-integer either.
+__device__ __forceinline__ float rint_div_fp16(float x, float s, float rcp_s) {
+  const float y = x * rcp_s;
+  const float f = floorf(y);
+  if (fmaf(f + 0.5f, s, -x) == 0.0f) return (((int)f) & 1) ? f + 1.0f : f;
+  return rintf(y);
+}
+
 // ------------------------------------------------------ global atomics --
 
 __device__ __forceinline__ void red_add_relaxed(int32_t* addr, int32_t v) {
