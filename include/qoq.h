@@ -18,7 +18,8 @@
  *  - All tensor pointers are DEVICE pointers on the current CUDA device; the
  *    caller allocates and owns every buffer (including the workspace).  The
  *    library allocates no device memory and keeps no state beyond a cached
- *    per-device attribute lookup and the debug settings below.
+ *    per-device attribute lookup, the debug settings below, and the fixed
+ *    device array behind qoq_w4a8_gemm_no_alloc.
  *  - fp16 values cross the ABI as their IEEE binary16 bit patterns (uint16_t).
  *  - Matrices are dense row-major.  W is [N][K] (row n = output channel),
  *    X / Xq are [M][K] (row m = token), Y is [M][N]: Y = X * W^T.
@@ -153,6 +154,45 @@ qoq_status qoq_w4a8_gemm(int M, int N, int K, int g, const int8_t* Xq, const uin
                          const uint8_t* packed, const uint16_t* s1_f16, uint16_t* Y_f16,
                          int32_t* acc_debug, void* workspace, size_t ws_bytes,
                          qoq_stream_t stream);
+
+/*
+ * qoq_w4a8_gemm without a caller-supplied workspace.  The paper has no
+ * counterpart: this is a service for callers that cannot allocate device
+ * memory.  Examples are a plugin given only its input and output buffers by a
+ * host program that does not share its allocator, a serving process that
+ * reserved nearly all device memory for its caches at start-up, and a step
+ * that must not synchronise the device as cudaMalloc/cudaFree may.
+ *
+ * Arguments, results and argument errors are those of qoq_w4a8_gemm, with no
+ * workspace.  The workspace lives in a static device array of
+ * QOQ_NO_ALLOC_SCRATCH_BYTES (8 MiB), which every GPU that loads the library's
+ * device code holds until the process exits.  This entry point allocates
+ * nothing and calls no allocating routine.
+ *
+ * Limit: a shape whose qoq_gemm_workspace_bytes(M, N, K, g) exceeds
+ * QOQ_NO_ALLOC_SCRATCH_BYTES returns QOQ_ERR_WORKSPACE before any device
+ * access.  With K up to 131072, every N fits for M <= 16.  N <= 65408 fits
+ * for M <= 32, and N <= 32640 for M <= 64.  Larger M fits only for small
+ * problems.
+ *
+ * The first call on a device (with that device current) looks up the array's
+ * device address once and checks the architecture.  Make that first call
+ * before any stream capture on that device.  A failed look-up returns
+ * QOQ_ERR_CUDA and is not retried.
+ *
+ * Every call shares the one array per device.  Each call first clears, on
+ * `stream`, the part that must start at zero (a small extra kernel), then
+ * runs the GEMM in it.  Calls that can overlap on the GPU (other streams,
+ * other host threads) race on the array and give wrong results: serialise
+ * them.  A device-side wait timeout is not reported, since
+ * qoq_last_device_status needs a workspace pointer.  Y is then undefined, and
+ * the next call starts from a cleared array.
+ */
+#define QOQ_NO_ALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+qoq_status qoq_w4a8_gemm_no_alloc(int M, int N, int K, int g, const int8_t* Xq,
+                                  const uint16_t* sx_f16, const uint8_t* packed,
+                                  const uint16_t* s1_f16, uint16_t* Y_f16, int32_t* acc_debug,
+                                  qoq_stream_t stream);
 
 /*
  * Inverse of the packing layout, for testing: recovers the logical codes.

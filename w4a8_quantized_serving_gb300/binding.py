@@ -22,7 +22,7 @@ QOQ_ERRORS = {
 EXPORTED = (
     "qoq_status_str", "qoq_version", "qoq_packed_weight_bytes", "qoq_gemm_workspace_bytes",
     "qoq_pack_weights", "qoq_quant_act", "qoq_w4a8_gemm", "qoq_unpack_weights_debug",
-    "qoq_last_device_status", "qoq_set_debug",
+    "qoq_last_device_status", "qoq_set_debug", "qoq_w4a8_gemm_no_alloc",
 )
 
 _LOCK = threading.Lock()
@@ -67,6 +67,8 @@ def lib() -> ctypes.CDLL:
             L.qoq_quant_act.restype = i32
             L.qoq_w4a8_gemm.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P, sz, P]
             L.qoq_w4a8_gemm.restype = i32
+            L.qoq_w4a8_gemm_no_alloc.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P]
+            L.qoq_w4a8_gemm_no_alloc.restype = i32
             L.qoq_unpack_weights_debug.argtypes = [i32, i32, i32, P, P, P, P, P]
             L.qoq_unpack_weights_debug.restype = i32
             L.qoq_last_device_status.argtypes = [P, P]
@@ -179,6 +181,28 @@ def qoq_w4a8_gemm(Xq, sx, packed, s1, N: int | None = None, g: int = 128, Y=None
                                _dev(Y, torch.float16, "Y", (M, N)), acc_ptr,
                                _dev(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream))
     _check(code, "qoq_w4a8_gemm")
+    return Y
+
+
+def qoq_w4a8_gemm_no_alloc(Xq, sx, packed, s1, N: int | None = None, g: int = 128, Y=None,
+                           acc_debug=None, stream=None):
+    """qoq_w4a8_gemm with the library's own fixed device scratch instead of a
+    caller workspace (for callers that cannot allocate device memory; calls
+    that overlap on the GPU race on that scratch).  Pass Y (and acc_debug) to
+    keep the call itself free of allocation."""
+    torch = _torch()
+    M, K = Xq.shape
+    if N is None:
+        N = s1.shape[0]
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.float16, device=Xq.device)
+    acc_ptr = None if acc_debug is None else _dev(acc_debug, torch.int32, "acc_debug", (M, N))
+    code = lib().qoq_w4a8_gemm_no_alloc(M, N, K, g, _dev(Xq, torch.int8, "Xq"),
+                                        _dev(sx, torch.float16, "sx", (M,)),
+                                        _dev(packed, torch.uint8, "packed"),
+                                        _dev(s1, torch.float16, "s1", (N,)),
+                                        _dev(Y, torch.float16, "Y", (M, N)), acc_ptr, _stream(stream))
+    _check(code, "qoq_w4a8_gemm_no_alloc")
     return Y
 
 

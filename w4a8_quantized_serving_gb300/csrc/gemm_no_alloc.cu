@@ -1,0 +1,121 @@
+// gemm_no_alloc.cu -- qoq_w4a8_gemm for callers that cannot allocate device
+// memory (declared in include/qoq.h as qoq_w4a8_gemm_no_alloc).
+//
+// qoq_w4a8_gemm needs a caller-supplied workspace (status header, split-K
+// counters and partial sums, and for M > 64 the fp16 B-operand copy of Xq).
+// Some callers have no way to provide one:
+//  - a plugin handed only its input and output buffers by a host program that
+//    does not expose its allocator;
+//  - a serving process that reserved nearly all device memory for its caches
+//    at start-up, so that a later cudaMalloc fails;
+//  - a step that must not synchronise the device, which cudaMalloc and
+//    cudaFree may do.
+// For them this entry point runs the same GEMM with its workspace in a
+// file-scope device array of fixed size, QOQ_NO_ALLOC_SCRATCH_BYTES.
+//
+// In host code `g_no_alloc_scratch` names a host-side stand-in, not device
+// memory; its device address is taken once per device with
+// cudaGetSymbolAddress (with that device current) and passed to the kernels.
+// Device code here names the array directly.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/qoq.h"
+#include "internal.h"
+
+namespace {
+
+static __device__ __align__(256) unsigned char g_no_alloc_scratch[QOQ_NO_ALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+
+struct ScratchSetup {
+  std::once_flag once;
+  void* ptr = nullptr;
+  qoq_status status = QOQ_ERR_CUDA;
+};
+ScratchSetup g_setup[kMaxDevices];
+
+// Once per device, with that device current: check the architecture (the
+// array lives in an sm_103a-only module), then take the array's device address.
+qoq_status scratch_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return QOQ_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= kMaxDevices) return QOQ_ERR_CUDA;
+  ScratchSetup& s = g_setup[dev];
+  std::call_once(s.once, [&] {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+      cudaGetLastError();
+      s.status = QOQ_ERR_CUDA;
+      return;
+    }
+    if (major != 10 || minor != 3) {
+      s.status = QOQ_ERR_ARCH;
+      return;
+    }
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_no_alloc_scratch) != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      s.status = QOQ_ERR_CUDA;
+      return;
+    }
+    s.ptr = p;
+    s.status = QOQ_OK;
+  });
+  *out = s.ptr;
+  return s.status;
+}
+
+// Zeroes the first n16 16-byte words of the array: the part of the workspace
+// that the GEMM requires to start at zero (header, counters, partial sums).
+__global__ void __launch_bounds__(256) no_alloc_clear_kernel(size_t n16) {
+  uint4* p = reinterpret_cast<uint4*>(g_no_alloc_scratch);
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride)
+    p[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" qoq_status qoq_w4a8_gemm_no_alloc(int M, int N, int K, int g, const int8_t* Xq,
+                                             const uint16_t* sx_f16, const uint8_t* packed,
+                                             const uint16_t* s1_f16, uint16_t* Y_f16,
+                                             int32_t* acc_debug, qoq_stream_t stream) {
+  // Argument checks in the order qoq_w4a8_gemm takes them, all before any
+  // device access.
+  if (!Xq || !sx_f16 || !packed || !s1_f16 || !Y_f16) return QOQ_ERR_NULL;
+  if (g != qoq::kGroup) return QOQ_ERR_UNSUPPORTED;
+  const size_t need = qoq_gemm_workspace_bytes(M, N, K, g);
+  if (need == 0) return QOQ_ERR_SHAPE;
+  if (!aligned16(Xq) || !aligned16(sx_f16) || !aligned16(packed) || !aligned16(s1_f16) ||
+      !aligned16(Y_f16) || (acc_debug && !aligned16(acc_debug)))
+    return QOQ_ERR_MISALIGNED;
+  if (need > QOQ_NO_ALLOC_SCRATCH_BYTES) return QOQ_ERR_WORKSPACE;
+
+  void* scratch = nullptr;
+  const qoq_status st = scratch_address(&scratch);
+  if (st != QOQ_OK) return st;
+
+  // The array keeps whatever the previous call left (normally zeros, but not
+  // after a call that ran out of its wait limit), so clear the zero-start part
+  // on the stream before every GEMM.
+  const size_t zero_bytes = qoq::gemm_ws_layout(M, N, K).xh_off;
+  const size_t n16 = zero_bytes / 16;
+  size_t blocks = (n16 + 255) / 256;
+  if (blocks > 1024) blocks = 1024;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  no_alloc_clear_kernel<<<(unsigned)blocks, 256, 0, s>>>(n16);
+  if (cudaGetLastError() != cudaSuccess) return QOQ_ERR_CUDA;
+
+  return qoq_w4a8_gemm(M, N, K, g, Xq, sx_f16, packed, s1_f16, Y_f16, acc_debug, scratch,
+                       QOQ_NO_ALLOC_SCRATCH_BYTES, stream);
+}
