@@ -292,7 +292,7 @@ cudaError_t launch_gemm(int M, int N, int K, const int8_t* Xq, const uint16_t* s
     const long long want = ((long long)p.T * p.G + 3) / 4;  // at least ~4 groups per CTA
     p.P = (int)std::max<long long>(1, std::min<long long>(P0, want));
   }
-  p.I_sk = (long long)p.T_sk * p.G;
+  p.I_sk = (uint32_t)p.T_sk * (uint32_t)p.G;  // T_sk <= 2 P0 - 1 <= 511, G <= 1024
   uint8_t* w = static_cast<uint8_t*>(ws);
   p.status = reinterpret_cast<int*>(w);
   p.sk_cnt = reinterpret_cast<int32_t*>(w + L.cnt_off);
@@ -309,7 +309,10 @@ cudaError_t launch_gemm(int M, int N, int K, const int8_t* Xq, const uint16_t* s
   p.call_id = call_id;
   p.trace = trace;
 
-  if (BN <= 64) return launch_gemm_decode(p, BN, s);
+  if (BN <= 64) {
+    if (p.MT != 1) return cudaErrorInvalidValue;  // the decode kernel holds all M tokens in one tile
+    return launch_gemm_decode(p, BN, s);
+  }
 
   ConvertParams c = {};
   c.Xq = Xq;

@@ -116,14 +116,15 @@ struct Unit {
 };
 
 // The CTA's sequence of (tile, group range) units: whole tiles first, then
-// its stream-K range.  Every role walks the same sequence.
+// its stream-K range.  Every role walks the same sequence.  All quantities fit
+// 32 bits (blockIdx.x * I_sk < 256 * 2^19), which keeps the divisions short.
 struct UnitIter {
   int dp_next;
-  long long it, it_end;
+  uint32_t it, it_end;
   __device__ __forceinline__ void init(const GemmParams& p) {
     dp_next = blockIdx.x;
-    it = (long long)blockIdx.x * p.I_sk / p.P;
-    it_end = (long long)(blockIdx.x + 1) * p.I_sk / p.P;
+    it = blockIdx.x * p.I_sk / (uint32_t)p.P;
+    it_end = (blockIdx.x + 1) * p.I_sk / (uint32_t)p.P;
   }
   __device__ __forceinline__ bool next(const GemmParams& p, Unit& u) {
     if (dp_next < p.T_dp) {
@@ -134,12 +135,13 @@ struct UnitIter {
       return true;
     }
     if (it < it_end) {
-      const long long sk = it / p.G;
-      const int g0 = (int)(it - sk * p.G);
-      const long long rem = it_end - it;
-      const long long g1 = rem < (long long)(p.G - g0) ? g0 + rem : (long long)p.G;
+      const uint32_t G = (uint32_t)p.G;
+      const uint32_t sk = it / G;
+      const uint32_t g0 = it - sk * G;
+      const uint32_t rem = it_end - it;
+      const uint32_t g1 = rem < G - g0 ? g0 + rem : G;
       u.tile = p.T_dp + (int)sk;
-      u.g0 = g0;
+      u.g0 = (int)g0;
       u.g1 = (int)g1;
       it += g1 - g0;
       return true;

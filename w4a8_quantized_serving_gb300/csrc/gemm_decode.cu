@@ -115,6 +115,7 @@ __global__ void __launch_bounds__(DecCfg<BN>::THREADS, 1) gemm_decode_kernel(con
   const uint32_t bar_drain = bar_accempty + 8 * C::NACC;
 
   if (threadIdx.x == 0) {
+    QOQ_TRACE_AT(p, 0, 0);
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 4);  // the 4 warps of the dequant slot that read the stage
@@ -135,10 +136,7 @@ __global__ void __launch_bounds__(DecCfg<BN>::THREADS, 1) gemm_decode_kernel(con
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + C::TMEM_SLOT_OFF);
-  if (threadIdx.x == 0) {
-    QOQ_TRACE_AT(p, 0, 0);
-    QOQ_TRACE_AT(p, 1, 0);
-  }
+  if (threadIdx.x == 0) QOQ_TRACE_AT(p, 1, 0);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer --
@@ -146,31 +144,35 @@ __global__ void __launch_bounds__(DecCfg<BN>::THREADS, 1) gemm_decode_kernel(con
     // fills while it runs.
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();  // each weight tile is read once
+      const uint8_t* const packed = p.packed;     // one token tile: weight tile index = tile
+      const size_t tile_stride = (size_t)p.G * kWTileBytes;
+      const uint32_t w_base = sbase + C::W_OFF;
       UnitIter iter;
       iter.init(p);
       Unit u;
-      uint32_t gi = 0;
-      uint32_t issued_mask = 0, issued_par = 0;  // per stage: last issue and its parity
+      uint32_t gi = 0, ph = 0;
+      int s = 0;  // stage of copy gi, and its phase ph
       bool ok = true;
       while (ok && iter.next(p, u)) {
-        for (int g = u.g0; g < u.g1; ++g, ++gi) {
-          const int s = gi % C::STAGES;
-          const uint32_t ph = (gi / C::STAGES) & 1;
-          if (!wait_bar(bar_empty + 8 * s, ph ^ 1, p)) {
+        const uint8_t* src = packed + (size_t)u.tile * tile_stride + (size_t)u.g0 * kWTileBytes;
+        for (int g = u.g0; g < u.g1; ++g, ++gi, src += kWTileBytes) {
+          if (gi >= (uint32_t)C::STAGES && !wait_bar(bar_empty + 8 * s, ph ^ 1, p)) {
             ok = false;
             break;
           }
           mbar_arrive_expect_tx(bar_full + 8 * s, kWTileBytes);
-          const uint8_t* src = p.packed + ((size_t)(u.tile / p.MT) * p.G + g) * kWTileBytes;
-          bulk_g2s(sbase + C::W_OFF + s * kWTileBytes, src, kWTileBytes, bar_full + 8 * s, pol);
+          bulk_g2s(w_base + s * kWTileBytes, src, kWTileBytes, bar_full + 8 * s, pol);
           QOQ_TRACE_AT(p, 16 + (int)gi, 0);
-          issued_mask |= 1u << s;
-          issued_par = (issued_par & ~(1u << s)) | (ph << s);
+          if (++s == C::STAGES) {
+            s = 0;
+            ph ^= 1;
+          }
         }
       }
-      // Let every copy still in flight land before the CTA may exit.
-      for (int s = 0; s < C::STAGES; ++s)
-        if (issued_mask & (1u << s)) wait_bar(bar_full + 8 * s, (issued_par >> s) & 1, p, false);
+      // Let every copy still in flight land before the CTA may exit: the
+      // last min(gi, STAGES) copies, one per stage.
+      for (uint32_t j = gi > (uint32_t)C::STAGES ? gi - C::STAGES : 0; j < gi; ++j)
+        wait_bar(bar_full + 8 * (j % C::STAGES), (j / C::STAGES) & 1, p, false);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -244,7 +246,6 @@ __global__ void __launch_bounds__(DecCfg<BN>::THREADS, 1) gemm_decode_kernel(con
     while (walk.next(p, tile, g, gi, bp)) {
       // batch bi is filled by slots (2 bi) % NSLOT (first group) and the next one
       if ((int)((2 * bp.bi + bp.pos) % C::NSLOT) != slot) continue;
-      const int mt = tile % p.MT;
       const int s = gi % C::STAGES;
       const int a = bp.bi % C::NBATCH;
       // int8 activation slice: 16-byte chunk q of the [BN][128] tile is row
@@ -253,13 +254,14 @@ __global__ void __launch_bounds__(DecCfg<BN>::THREADS, 1) gemm_decode_kernel(con
 #pragma unroll
       for (int i = 0; i < BN / 16; ++i) {
         const int q = stid + i * 128;
-        const int m = mt * BN + (q >> 3);
+        const int m = q >> 3;  // one token tile: rows 0 .. BN-1
         xv[i] = m < p.M ? __ldcg(reinterpret_cast<const uint4*>(p.xq + (size_t)m * p.K + g * kGroup + (q & 7) * 16))
                         : make_uint4(0, 0, 0, 0);
       }
-      if (!wait_bar(bar_full + 8 * s, (gi / C::STAGES) & 1, p) ||
-          !wait_bar(bar_aempty + 8 * a, ((bp.bi / C::NBATCH) & 1) ^ 1, p))
-        break;
+      if (quad == 0 && lane == 0) QOQ_TRACE_AT(p, 192 + (int)gi, 0);
+      if (!wait_bar(bar_full + 8 * s, (gi / C::STAGES) & 1, p)) break;
+      if (quad == 0 && lane == 0) QOQ_TRACE_AT(p, 320 + (int)gi, 0);
+      if (!wait_bar(bar_aempty + 8 * a, ((bp.bi / C::NBATCH) & 1) ^ 1, p)) break;
       tc_fence_after();  // the MMAs that read this batch buffer are complete
       if (quad == 0 && lane == 0) QOQ_TRACE_AT(p, 256 + (int)gi, 0);
       const uint8_t* wt = smem + C::W_OFF + s * kWTileBytes;

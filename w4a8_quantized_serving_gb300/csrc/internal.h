@@ -73,7 +73,7 @@ struct GemmParams {
   int32_t* sk_cnt;  // [T_sk]
   int* status;      // workspace header
   int M, N, K, G, MT, NT, T, T_dp, T_sk, P;
-  long long I_sk;
+  uint32_t I_sk;  // T_sk * G <= 511 * 1024, so 32-bit schedule arithmetic suffices
   unsigned long long timeout_ns;
   int fault;
   unsigned call_id;           // non-zero, distinct per call: the abort word names the aborting call
