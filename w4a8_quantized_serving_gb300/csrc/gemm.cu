@@ -51,7 +51,8 @@ struct BulkCfg {
   static constexpr int W_OFF = STAGES * B_BYTES;
   static constexpr int BAR_OFF = W_OFF + STAGES * kWTileBytes;
   static constexpr int NBARS = 2 * STAGES + 2 * NABUF + 2 * NACC + 1;
-  static constexpr int TMEM_SLOT_OFF = BAR_OFF + NBARS * 8;
+  static constexpr int SEQ_OFF = BAR_OFF + NBARS * 8;  // one 32-bit sequence word per stage
+  static constexpr int TMEM_SLOT_OFF = SEQ_OFF + ((STAGES * 4 + 7) / 8) * 8;
   static constexpr int FLAG_OFF = TMEM_SLOT_OFF + 8;
   static constexpr int SMEM_BYTES = FLAG_OFF + 8 + 1024;  // + slack for 1024-B alignment
   static_assert(NABUF >= NSLOT + 1, "A buffers");
@@ -71,9 +72,15 @@ __global__ void __launch_bounds__(BulkCfg::THREADS, 1) gemm_bulk_kernel(const __
   const uint32_t bar_afull = bars + 8 * (2 * C::STAGES), bar_aempty = bar_afull + 8 * C::NABUF;
   const uint32_t bar_accfull = bar_aempty + 8 * C::NABUF, bar_accempty = bar_accfull + 8 * C::NACC;
   const uint32_t bar_drain = bar_accempty + 8 * C::NACC;
+  // Stage s last armed for group seq[s] - 1 (0: never).  The two dequant slots
+  // alternate groups over an odd number of stages, so a stage's consumer
+  // changes from lap to lap; the sequence word keeps each consumer's parity
+  // wait on the right lap.
+  const uint32_t seq = sbase + C::SEQ_OFF;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
+      *reinterpret_cast<volatile uint32_t*>(smem + C::SEQ_OFF + 4 * s) = 0;
       mbar_init(bar_full + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1 + 4);  // MMA commit + the 4 warps of one dequant slot
     }
@@ -121,6 +128,7 @@ __global__ void __launch_bounds__(BulkCfg::THREADS, 1) gemm_bulk_kernel(const __
         const int s = npre;
         mbar_arrive_expect_tx(bar_full + 8 * s, kStageTx);
         issue_w(s, u.tile, g);
+        st_release_shared(seq + 4 * s, (uint32_t)npre + 1);
         pre_tile[npre] = u.tile;
         pre_g[npre] = g;
         issued_mask |= 1u << s;
@@ -141,6 +149,7 @@ __global__ void __launch_bounds__(BulkCfg::THREADS, 1) gemm_bulk_kernel(const __
           mbar_arrive_expect_tx(bar_full + 8 * s, kStageTx);
           issue_w(s, u.tile, g);
           issue_x(s, u.tile, g);
+          st_release_shared(seq + 4 * s, gi + 1);
           issued_mask |= 1u << s;
           issued_par = (issued_par & ~(1u << s)) | (ph << s);
         } else {
@@ -181,7 +190,7 @@ __global__ void __launch_bounds__(BulkCfg::THREADS, 1) gemm_bulk_kernel(const __
         if ((int)(gi % C::NSLOT) != slot) continue;
         const int s = gi % C::STAGES;
         const int a = gi % C::NABUF;
-        if (!wait_bar(bar_full + 8 * s, (gi / C::STAGES) & 1, p) ||
+        if (!wait_seq(seq + 4 * s, gi + 1, p) || !wait_bar(bar_full + 8 * s, (gi / C::STAGES) & 1, p) ||
             !wait_bar(bar_aempty + 8 * a, ((gi / C::NABUF) & 1) ^ 1, p)) {
           ok = false;
           break;

@@ -104,10 +104,11 @@ __device__ __forceinline__ void store_b_chunk(uint8_t* btile, int bn, int r, int
 
 // Shared-memory matrix descriptor: 128-byte swizzle, K-major, 8-row groups
 // 1024 B apart (SBO), version 1 (bit 46), layout code 2 (bits 61-63).
-__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
-  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
-         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
+// Given as its two 32-bit halves: shared addresses stay below 2^18, so moving
+// the start address by a multiple of 16 bytes is an add of (bytes >> 4) to
+// the low half.
+__device__ __forceinline__ uint32_t desc_sw128_lo(uint32_t saddr) { return ((saddr & 0x3FFFFu) >> 4) | (1u << 16); }
+constexpr uint32_t kDescSw128Hi = (1024u >> 4) | (1u << 14) | (2u << 29);
 
 // ------------------------------------------------------------------ schedule --
 
@@ -183,6 +184,43 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ge
   return wait_slow(bar, parity, p, honor_abort);
 }
 
+// Per-stage sequence words in shared memory: the producer publishes, with
+// release semantics, the group it armed a stage for; a consumer that is not
+// the stage's previous consumer first waits (acquire) for its own group's
+// number, which proves that the stage's previous phase completed, and only
+// then waits on the stage's phase parity.
+__device__ __forceinline__ void st_release_shared(uint32_t addr, uint32_t v) {
+  asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_shared(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+// Bounded like wait_slow.
+__device__ __noinline__ inline bool wait_seq_slow(uint32_t addr, uint32_t want, const GemmParams& p) {
+  volatile unsigned* abort_word = reinterpret_cast<volatile unsigned*>(p.status + 1);
+  const long long c0 = clock64();
+  uint64_t t0 = 0;
+  for (uint32_t i = 1;; ++i) {
+    if (ld_acquire_shared(addr) == want) return true;
+    if ((i & 255) == 0 && clock64() - c0 > 100000) {
+      const uint64_t now = global_timer_ns();
+      if (t0 == 0) t0 = now;
+      if (*abort_word == p.call_id) return false;
+      if (now - t0 > p.timeout_ns) {
+        atomicExch(p.status, kStatusTimeout);
+        atomicExch(reinterpret_cast<unsigned*>(p.status + 1), p.call_id);
+        return false;
+      }
+    }
+  }
+}
+__device__ __forceinline__ bool wait_seq(uint32_t addr, uint32_t want, const GemmParams& p) {
+  if (ld_acquire_shared(addr) == want) return true;
+  return wait_seq_slow(addr, want, p);
+}
+
 // Lane 0 waits, the warp learns the outcome (keeps the warp converged).
 __device__ __forceinline__ bool warp_wait_bar(uint32_t bar, uint32_t parity, const GemmParams& p) {
   int ok = 1;
@@ -251,14 +289,13 @@ __device__ __forceinline__ void mma_role(const GemmParams& p, uint32_t tmem, uin
         }
         tc_fence_after();
         if ((threadIdx.x & 31) == 0) QOQ_TRACE_AT(p, 128 + (int)gi, 0);
-        const uint32_t b_base = b_tile(gi, a);
+        const uint32_t b_lo = desc_sw128_lo(b_tile(gi, a));
+        const uint32_t a_col = tmem + ACOL0 + a * 64;
         if (elect_one()) {
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint32_t b_addr = b_base + (j >> 2) * (BN * 128) + (j & 3) * 32;
-            tc_mma_ts(d_tmem, tmem + ACOL0 + a * 64 + 8 * j, desc_sw128(b_addr), kIdesc,
-                      (g > c0 || j > 0) ? 1u : 0u);
-          }
+          for (int j = 0; j < 8; ++j)  // K step j: 64-channel half j / 4, 32-byte chunk j % 4
+            tc_mma_ts(d_tmem, a_col + 8 * j, b_lo + (j >> 2) * (BN * 8) + (j & 3) * 2, kDescSw128Hi, kIdesc,
+                       (g > c0 || j > 0) ? 1u : 0u);
           tc_commit(bar_aempty + 8 * a);
           const uint32_t xc = extra_commit(gi);
           if (xc) tc_commit(xc);

@@ -43,6 +43,9 @@ struct DecCfg {
   static constexpr int B_TILES = 2 * NBATCH;
   static constexpr int STAGES_FIT = (kSmemBudget - 2048 - B_TILES * B_BYTES) / kWTileBytes;
   static constexpr int STAGES = STAGES_FIT > 16 ? 16 : STAGES_FIT;
+  // Each slot has a sub-ring of SPS stages: one producer and one consumer per
+  // stage, both in order, so a phase-parity wait can never be a lap ahead.
+  static constexpr int SPS = STAGES / NSLOT;
   static constexpr int W_OFF = B_TILES * B_BYTES;
   static constexpr int BAR_OFF = W_OFF + STAGES * kWTileBytes;
   static constexpr int NBARS = 2 * STAGES + 2 * NBATCH + 2 * NACC + 1;
@@ -52,7 +55,7 @@ struct DecCfg {
   static_assert(BN == 16 || BN == 32 || BN == 64, "decode tiles");
   static_assert(NBATCH >= 2 && ACOL0 + 128 * NBATCH <= kTmemCols, "TMEM columns");
   static_assert(NSLOT % 2 == 0, "slot pairs fill a batch");
-  static_assert(STAGES >= 4, "pipeline depth");
+  static_assert(SPS >= 2, "pipeline depth per slot");
   static_assert(B_BYTES % 1024 == 0, "1024-B aligned B tiles");
   static_assert(SMEM_BYTES <= kSmemBudget, "shared memory");
 };
@@ -67,36 +70,69 @@ struct BatchPos {
   int nb;       // groups in the batch (1 or 2)
 };
 
+// Per-slot counters of the producer (registers, no indexed local array).
+template <int NSLOT>
+struct SlotCounters {
+  uint32_t c[4] = {0, 0, 0, 0};
+  __device__ __forceinline__ uint32_t take(int slot) {
+    uint32_t v = 0;
+#pragma unroll
+    for (int i = 0; i < NSLOT; ++i)
+      if (i == slot) v = c[i]++;
+    return v;
+  }
+  __device__ __forceinline__ uint32_t count(int slot) const {
+    uint32_t v = 0;
+#pragma unroll
+    for (int i = 0; i < NSLOT; ++i)
+      if (i == slot) v = c[i];
+    return v;
+  }
+};
+
 // Walks the groups of one dequant slot.  Within a unit, group g has batch
 // position t = t0 + (g - g0), where t0 = 2 x (batches before the unit); its
 // batch is t / 2, its place in the batch t % 2, and it belongs to slot
-// t % NSLOT.  So a slot steps NSLOT groups at a time and only recomputes at
-// unit boundaries; stepping through the other slots' groups one by one cost
-// ~0.1 us per step on a sub-partition busy with dequant work.
+// t % NSLOT.  So a slot steps NSLOT positions at a time and only recomputes
+// at unit boundaries (stepping through the other slots' groups one by one
+// cost ~0.1 us per step on a sub-partition busy with dequant work).
+// A unit of odd length ends with a one-group batch; its empty second place
+// t0 + len is walked too, as a dummy entry: the slot that owns it waits for
+// the batch's A buffer and arrives on it without writing.  So every slot takes
+// part in every batch of its class (every NSLOT / 2-th batch), and its waits
+// on an A buffer's phase parity always follow its own wait for the lap before
+// (a slot that skipped a batch could otherwise pass a wait a lap early).
 template <int NSLOT>
 struct SlotWalk {
   UnitIter it;
   Unit u;
   bool have;
-  int g, slot;
-  uint32_t gi0, t0;  // index of the unit's first group; its batch position
+  int g, g_end, slot;  // g_end: end of the unit's positions, rounded up to a full batch
+  uint32_t gi0, t0;    // index of the unit's first group; its batch position
+  __device__ __forceinline__ void enter_unit() {
+    g_end = u.g0 + 2 * ((u.g1 - u.g0 + 1) / 2);
+    g = u.g0 + (int)(((uint32_t)slot - t0) & (NSLOT - 1));
+  }
   __device__ __forceinline__ void init(const GemmParams& p, int slot_) {
     slot = slot_;
     it.init(p);
     gi0 = t0 = 0;
     have = it.next(p, u);
-    g = have ? u.g0 + (int)(((uint32_t)slot - t0) & (NSLOT - 1)) : 0;
+    if (have) enter_unit();
   }
-  __device__ __forceinline__ bool next(const GemmParams& p, int& tile, int& gg, uint32_t& gi, BatchPos& bp) {
-    while (have && g >= u.g1) {
+  // dummy: the empty second place of a one-group batch (gi, tile, gg unused).
+  __device__ __forceinline__ bool next(const GemmParams& p, int& tile, int& gg, uint32_t& gi, BatchPos& bp,
+                                       bool& dummy) {
+    while (have && g >= g_end) {
       const uint32_t len = (uint32_t)(u.g1 - u.g0);
       gi0 += len;
       t0 += 2 * ((len + 1) / 2);
       have = it.next(p, u);
-      if (have) g = u.g0 + (int)(((uint32_t)slot - t0) & (NSLOT - 1));
+      if (have) enter_unit();
     }
     if (!have) return false;
     const int off = g - u.g0;
+    dummy = g >= u.g1;
     bp.pos = off & 1;
     bp.bi = (t0 + (uint32_t)off) >> 1;
     bp.nb = min(2, u.g1 - (g - bp.pos));
@@ -128,7 +164,7 @@ __global__ void __launch_bounds__(DecCfg<BN>::THREADS, 1) gemm_decode_kernel(con
       mbar_init(bar_empty + 8 * s, 4);  // the 4 warps of the dequant slot that read the stage
     }
     for (int a = 0; a < C::NBATCH; ++a) {
-      mbar_init(bar_afull + 8 * a, 8);  // 4 warps x 2 groups (a one-group batch arrives twice)
+      mbar_init(bar_afull + 8 * a, 8);  // 4 warps x 2 places (the empty place of a one-group batch too)
       mbar_init(bar_aempty + 8 * a, 1);
     }
     for (int b = 0; b < C::NACC; ++b) {
@@ -154,32 +190,35 @@ __global__ void __launch_bounds__(DecCfg<BN>::THREADS, 1) gemm_decode_kernel(con
       const uint8_t* const packed = p.packed;     // one token tile: weight tile index = tile
       const size_t tile_stride = (size_t)p.G * kWTileBytes;
       const uint32_t w_base = sbase + C::W_OFF;
+      SlotCounters<C::NSLOT> taken;  // groups handed to each slot so far
       UnitIter iter;
       iter.init(p);
       Unit u;
-      uint32_t gi = 0, ph = 0;
-      int s = 0;  // stage of copy gi, and its phase ph
+      uint32_t gi = 0, t0 = 0;  // group index; batch position of the unit's first group
       bool ok = true;
       while (ok && iter.next(p, u)) {
         const uint8_t* src = packed + (size_t)u.tile * tile_stride + (size_t)u.g0 * kWTileBytes;
         for (int g = u.g0; g < u.g1; ++g, ++gi, src += kWTileBytes) {
-          if (gi >= (uint32_t)C::STAGES && !wait_bar(bar_empty + 8 * s, ph ^ 1, p)) {
+          const int slot = (int)((t0 + (uint32_t)(g - u.g0)) % C::NSLOT);
+          const uint32_t k = taken.take(slot);  // the slot's k-th group
+          const int s = slot * C::SPS + (int)(k % C::SPS);
+          if (k >= (uint32_t)C::SPS && !wait_bar(bar_empty + 8 * s, ((k / C::SPS) & 1) ^ 1, p)) {
             ok = false;
             break;
           }
           mbar_arrive_expect_tx(bar_full + 8 * s, kWTileBytes);
           bulk_g2s(w_base + s * kWTileBytes, src, kWTileBytes, bar_full + 8 * s, pol);
           QOQ_TRACE_AT(p, 16 + (int)gi, 0);
-          if (++s == C::STAGES) {
-            s = 0;
-            ph ^= 1;
-          }
         }
+        t0 += 2 * (uint32_t)((u.g1 - u.g0 + 1) / 2);
       }
-      // Let every copy still in flight land before the CTA may exit: the
-      // last min(gi, STAGES) copies, one per stage.
-      for (uint32_t j = gi > (uint32_t)C::STAGES ? gi - C::STAGES : 0; j < gi; ++j)
-        wait_bar(bar_full + 8 * (j % C::STAGES), (j / C::STAGES) & 1, p, false);
+      // Let every copy still in flight land before the CTA may exit: the last
+      // min(k, SPS) copies of each slot, one per stage of its sub-ring.
+      for (int slot = 0; slot < C::NSLOT; ++slot) {
+        const uint32_t n = taken.count(slot);
+        for (uint32_t k = n > (uint32_t)C::SPS ? n - C::SPS : 0; k < n; ++k)
+          wait_bar(bar_full + 8 * (slot * C::SPS + (int)(k % C::SPS)), (k / C::SPS) & 1, p, false);
+      }
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -214,13 +253,12 @@ __global__ void __launch_bounds__(DecCfg<BN>::THREADS, 1) gemm_decode_kernel(con
           if (lane == 0) QOQ_TRACE_AT(p, 128 + (int)bi, 0);
           if (elect_one()) {
             for (int q = 0; q < nb; ++q) {
-              const uint32_t b_base = sbase + (uint32_t)((2 * a + q) * C::B_BYTES);
+              const uint32_t b_lo = desc_sw128_lo(sbase + (uint32_t)((2 * a + q) * C::B_BYTES));
+              const uint32_t a_col = tmem + C::ACOL0 + a * 128 + q * 64;
 #pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                const uint32_t b_addr = b_base + (j >> 2) * (BN * 128) + (j & 3) * 32;
-                tc_mma_ts(d_tmem, tmem + C::ACOL0 + a * 128 + q * 64 + 8 * j, desc_sw128(b_addr), kIdesc,
-                          (g > c0 || q > 0 || j > 0) ? 1u : 0u);
-              }
+              for (int j = 0; j < 8; ++j)  // K step j: 64-channel half j / 4, 32-byte chunk j % 4
+                tc_mma_ts(d_tmem, a_col + 8 * j, b_lo + (j >> 2) * (BN * 8) + (j & 3) * 2, kDescSw128Hi, kIdesc,
+                           (g > c0 || q > 0 || j > 0) ? 1u : 0u);
             }
             tc_commit(bar_aempty + 8 * a);
           }
@@ -248,11 +286,20 @@ __global__ void __launch_bounds__(DecCfg<BN>::THREADS, 1) gemm_decode_kernel(con
     SlotWalk<C::NSLOT> walk;
     walk.init(p, slot);
     int tile, g;
-    uint32_t gi;
+    uint32_t gi, nown = 0;  // groups of this slot so far: its position in its sub-ring
     BatchPos bp;
-    while (walk.next(p, tile, g, gi, bp)) {
-      const int s = gi % C::STAGES;
+    bool dummy;
+    while (walk.next(p, tile, g, gi, bp, dummy)) {
       const int a = bp.bi % C::NBATCH;
+      if (dummy) {  // the empty place of a one-group batch: take part without data
+        if (!wait_bar(bar_aempty + 8 * a, ((bp.bi / C::NBATCH) & 1) ^ 1, p)) break;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_afull + 8 * a);
+        continue;
+      }
+      const int s = slot * C::SPS + (int)(nown % C::SPS);
+      const uint32_t sph = (nown / C::SPS) & 1;
+      ++nown;
       // int8 activation slice: 16-byte chunk q of the [BN][128] tile is row
       // q / 8, channels 16 (q % 8) .. +15; rows past M read as zero
       uint4 xv[BN / 16];
@@ -264,7 +311,7 @@ __global__ void __launch_bounds__(DecCfg<BN>::THREADS, 1) gemm_decode_kernel(con
                         : make_uint4(0, 0, 0, 0);
       }
       if (quad == 0 && lane == 0) QOQ_TRACE_AT(p, 192 + (int)gi, 0);
-      if (!wait_bar(bar_full + 8 * s, (gi / C::STAGES) & 1, p)) break;
+      if (!wait_bar(bar_full + 8 * s, sph, p)) break;
       if (quad == 0 && lane == 0) QOQ_TRACE_AT(p, 320 + (int)gi, 0);
       if (!wait_bar(bar_aempty + 8 * a, ((bp.bi / C::NBATCH) & 1) ^ 1, p)) break;
       tc_fence_after();  // the MMAs that read this batch buffer are complete
@@ -295,10 +342,7 @@ __global__ void __launch_bounds__(DecCfg<BN>::THREADS, 1) gemm_decode_kernel(con
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        if (!(p.fault == 1 && gi == 17)) {  // test hook: one group never arrives
-          mbar_arrive(bar_afull + 8 * a);
-          if (bp.nb == 1) mbar_arrive(bar_afull + 8 * a);  // stands in for the absent second group
-        }
+        if (!(p.fault == 1 && gi == 17)) mbar_arrive(bar_afull + 8 * a);  // test hook: one group never arrives
         if (quad == 0) QOQ_TRACE_AT(p, 384 + (int)gi, 0);
         if (quad == 3) QOQ_TRACE_AT(p, 448 + (int)gi, 0);
       }
