@@ -187,6 +187,52 @@ def test_gemm_workload_sampled(cfg):
 
 # ------------------------------------------------------- failure detection --
 
+@pytest.mark.parametrize("M,N,K", [(16, 12288, 4096), (256, 4096, 14336)])
+def test_gemm_exact_across_alternating_inputs(M, N, K):
+    """Repeated calls that alternate between two input sets (different weights
+    and activations), with a call that times out on purpose now and then:
+    every int32 accumulator must equal that input set's first result, bit for
+    bit.  Any pipeline wait that passes before its data is ready reads what
+    the previous call left in shared or tensor memory, which here always
+    belongs to the other input set."""
+    mod = q()
+    t = gc.torch()
+    sets = []
+    for seed in (81, 82):
+        packed, s1 = mod.qoq_pack_weights(gc.to_dev_f16(synth.weights(N, K, seed)))
+        Xq, sx = mod.qoq_quant_act(gc.to_dev_f16(synth.activations(M, K, seed)))
+        sets.append((Xq, sx, packed, s1))
+    ws = t.zeros(mod.qoq_gemm_workspace_bytes(M, N, K), dtype=t.uint8, device="cuda")
+    refs = []
+    for Xq, sx, packed, s1 in sets:
+        acc = t.empty((M, N), dtype=t.int32, device="cuda")
+        mod.qoq_w4a8_gemm(Xq, sx, packed, s1, N, acc_debug=acc, workspace=ws)
+        refs.append(acc)
+    # a small call that times out on purpose (test hook), with its own workspace
+    Mt, Nt, Kt = 16, 128 * 152, 4096  # 32 groups per CTA: the hook (group 17) fires
+    pt, s1t = mod.qoq_pack_weights(gc.to_dev_f16(synth.weights(Nt, Kt, 83)))
+    Xqt, sxt = mod.qoq_quant_act(gc.to_dev_f16(synth.activations(Mt, Kt, 83)))
+    wst = t.zeros(mod.qoq_gemm_workspace_bytes(Mt, Nt, Kt), dtype=t.uint8, device="cuda")
+    acc = t.empty((M, N), dtype=t.int32, device="cuda")
+    bad = []
+    for i in range(120):
+        if i % 20 == 19:
+            try:
+                mod.qoq_set_debug(2_000_000, 1)
+                mod.qoq_w4a8_gemm(Xqt, sxt, pt, s1t, Nt, workspace=wst)
+                mod.qoq_last_device_status(wst)
+            finally:
+                mod.qoq_set_debug(0, 0)
+            wst.zero_()
+        j = i % 2
+        acc.fill_(-1)
+        mod.qoq_w4a8_gemm(*sets[j], N, acc_debug=acc, workspace=ws)
+        if not t.equal(acc, refs[j]):
+            bad.append(i)
+    assert mod.qoq_last_device_status(ws) == 0
+    assert not bad, f"calls {bad} differ from their input set's first result"
+
+
 def test_device_wait_timeout_is_reported_and_context_survives():
     """A producer that skips one pipeline stage (test hook) makes the waits
     downstream run out after a short limit; the kernel returns, the status
