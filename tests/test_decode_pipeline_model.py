@@ -5,28 +5,25 @@ The kernel's roles hand work to each other through mbarriers whose waits test
 only the parity of a phase, so a wait is right only if it starts after the
 phase before the one it wants has completed, and before the phase after it
 can complete.  The model runs each role as a sequence of waits and arrivals,
-exactly as the kernel orders them, under adversarial scheduling (some copies
-land only when nothing else can move), and counts phases exactly:
+in the order the kernel takes them, under adversarial scheduling (some copies
+land only when nothing else can move), and counts phases exactly.  Each wait
+names the phase it means (n, counted from 0; -1 for "none yet") and tests its
+parity n & 1, which is what the kernel's parity expressions evaluate to.
 
-Each wait names the phase it means (n, counted from 0; -1 for "none yet")
-and tests its parity n & 1, which is what the kernel's parity expressions
-evaluate to.
-
-  * producer: per group one copy into the owning slot's sub-ring of weight
-    stages; from the second lap on it first waits for the stage's release;
-  * dequant slot j: the groups at batch positions t = j (mod NSLOT) in each
-    unit, plus the empty second place of a one-group batch it owns (a dummy
-    that only waits for the A buffer and arrives); per group: wait for the
-    stage, release it, wait for the A buffer, arrive on the batch;
-  * MMA warp: per fold chunk of 8 groups it waits for an accumulator, per
-    batch of two groups for the batch, then commits the A buffer, and at the
-    chunk's end the accumulator;
+  * producers: group gi (in the CTA's order) belongs to slot gi % NSLOT and
+    goes to that slot's sub-ring of SPS stages; from a stage's second lap on,
+    the copy first waits for the stage's release;
+  * dequant slot j, per fold chunk (up to 8 * NSLOT consecutive groups of a
+    unit): it waits for the chunk's accumulator to be free (also when it has
+    no group in the chunk, then it only arrives); per own group it waits for
+    the stage, releases it, waits until its previous group's MMAs are done,
+    issues the group's MMAs, which complete on its MMA-done barrier, and after
+    its last group of the chunk, on the chunk's accumulator barrier;
   * epilogue: waits for each chunk's accumulator and releases it.
 
 Every parity wait must pass exactly on the phase it means, and no schedule may
-deadlock.  The same model with the earlier protocol (one ring shared by all
-slots; a one-group batch's slot arriving twice instead of a dummy) shows a
-wait passing a lap early, which is the race that protocol had on the GPU.
+deadlock.  A planted mistake -- a slot skipping the accumulator wait in chunks
+where it has no group -- must show up as a wait passing a lap early.
 """
 import random
 
@@ -76,84 +73,64 @@ def schedule(M, N, K, P0=152):
     return G, T, 0, max(1, min(P0, (T * G + 3) // 4))
 
 
-def run(units, nslot, stages, nbatch, old=False, hold=(), seed=0):
+def run(units, nslot, stages, skip_idle_wait=False, hold=(), seed=0):
     """Returns (deadlocked, list of wrong passes)."""
     rng = random.Random(seed)
     sps = stages // nslot
+    ch_len = FOLD * nslot
     bars = {}
     for s in range(stages):
         bars["full", s], bars["empty", s] = Bar(1), Bar(4)
-    for a in range(nbatch):
-        bars["afull", a], bars["aempty", a] = Bar(8), Bar(1)
+    for j in range(nslot):
+        bars["mmadone", j] = Bar(1)
     for b in range(NACC):
-        bars["accfull", b], bars["accempty", b] = Bar(1), Bar(NEPI)
-    entries, t0, gi = [], 0, 0  # (t, gi or None for a dummy, nb)
+        bars["accfull", b], bars["accempty", b] = Bar(nslot), Bar(NEPI)
+    chunks, gi = [], 0  # (first group index, length)
     for _, g0, g1 in units:
-        n = g1 - g0
-        for off in range(n + n % 2):
-            pos = off & 1
-            real = off < n
-            entries.append(dict(t=t0 + off, gi=gi if real else None, nb=min(2, n - (off - pos))))
-            gi += real
-        t0 += n + n % 2
-    real = [e for e in entries if e["gi"] is not None]
-    place = {}  # gi -> (stage, lap)
-    count = [0] * nslot
-    for e in real:
-        j = e["t"] % nslot
-        if old:
-            place[e["gi"]] = (e["gi"] % stages, e["gi"] // stages)
-        else:
-            place[e["gi"]] = (j * sps + count[j] % sps, count[j] // sps)
-        count[j] += 1
+        for c0 in range(g0, g1, ch_len):
+            n = min(ch_len, g1 - c0)
+            chunks.append((gi, n))
+            gi += n
+    place = {g: ((g % nslot) * sps + (g // nslot) % sps, (g // nslot) // sps) for g in range(gi)}
     inflight, issued = [], set()
 
     def producer():
-        for e in real:
-            s, lap = place[e["gi"]]
+        for g in range(gi):
+            s, lap = place[g]
             if lap:
                 yield "wait", ("empty", s), lap - 1
-            inflight.append((s, e["gi"]))
-            issued.add(e["gi"])
+            inflight.append((s, g))
+            issued.add(g)
             yield "step",
 
     def slot(j):
-        for e in entries:
-            if e["t"] % nslot != j or (old and e["gi"] is None):
-                continue
-            bi = e["t"] >> 1
-            a, lap_a = bi % nbatch, bi // nbatch
-            if e["gi"] is not None:
-                yield "issued", e["gi"]
-                s, lap = place[e["gi"]]
-                yield "wait", ("full", s), lap
-                yield "arrive", ("empty", s), 4
-            yield "wait", ("aempty", a), lap_a - 1
-            yield "arrive", ("afull", a), 8 if (old and e["nb"] == 1) else 4
-
-    def mma():
-        bi = chunk = 0
-        for _, g0, g1 in units:
-            for c0 in range(g0, g1, FOLD):
-                b, lap_b = chunk % NACC, chunk // NACC
+        nown = 0
+        for ch, (gc0, n) in enumerate(chunks):
+            b, lap_b = ch % NACC, ch // NACC
+            mine = [gc0 + off for off in range(n) if (gc0 + off) % nslot == j]
+            if mine or not skip_idle_wait:
                 yield "wait", ("accempty", b), lap_b - 1
-                for _ in range(c0, min(g1, c0 + FOLD), 2):
-                    yield "wait", ("afull", bi % nbatch), bi // nbatch
-                    yield "arrive", ("aempty", bi % nbatch), 1
-                    bi += 1
+            if not mine:
                 yield "arrive", ("accfull", b), 1
-                chunk += 1
+                continue
+            for k, g in enumerate(mine):
+                yield "issued", g
+                s, lap = place[g]
+                yield "wait", ("full", s), lap
+                yield "wait", ("mmadone", j), nown - 1
+                yield "arrive", ("empty", s), 4
+                yield "arrive", ("mmadone", j), 1
+                if k == len(mine) - 1:
+                    yield "arrive", ("accfull", b), 1
+                nown += 1
 
     def epilogue():
-        chunk = 0
-        for _, g0, g1 in units:
-            for _ in range(g0, g1, FOLD):
-                b, lap_b = chunk % NACC, chunk // NACC
-                yield "wait", ("accfull", b), lap_b
-                yield "arrive", ("accempty", b), NEPI
-                chunk += 1
+        for ch in range(len(chunks)):
+            b, lap_b = ch % NACC, ch // NACC
+            yield "wait", ("accfull", b), lap_b
+            yield "arrive", ("accempty", b), NEPI
 
-    roles = [producer(), mma(), epilogue()] + [slot(j) for j in range(nslot)]
+    roles = [producer(), epilogue()] + [slot(j) for j in range(nslot)]
     current = [None] * len(roles)
     finished = [False] * len(roles)
     wrong = []
@@ -196,36 +173,36 @@ def run(units, nslot, stages, nbatch, old=False, hold=(), seed=0):
 
 
 def config(M):
+    """(NSLOT, STAGES) of the kernel's configuration for M tokens."""
     bn = 16 if M <= 16 else 32 if M <= 32 else 64
     nslot = 2 if bn == 64 else 4
-    stages = 16 if bn < 64 else 15
-    nbatch = (512 - (2 * bn + 63) // 64 * 64) // 128
-    return nslot, stages - stages % nslot, nbatch
+    b_bytes = bn * 128 * 2
+    fit = (227 * 1024 - 2048 - nslot * b_bytes) // 8448
+    return nslot, min(fit, 24) // nslot * nslot
 
 
 @pytest.mark.parametrize("M,N,K", [(16, 12288, 4096), (40, 1664, 1152), (64, 22016, 4096), (16, 19456, 8192),
-                                   (1, 384, 1152), (32, 1280, 384)])
+                                   (1, 384, 1152), (32, 1280, 384), (16, 4096, 14336)])
 def test_protocol_has_no_wrong_pass_and_no_deadlock(M, N, K):
-    nslot, stages, nbatch = config(M)
+    nslot, stages = config(M)
     G, T, T_dp, P = schedule(M, N, K)
     for b in sorted({0, 1, P // 2, P - 1} | set(range(0, P, max(1, P // 12)))):
         units = cta_units(b, P, T, G, T_dp)
         ngroups = sum(g1 - g0 for _, g0, g1 in units)
         for seed, hold in [(0, ()), (1, ())] + [(2, (h,)) for h in range(min(ngroups, 8))]:
-            dead, wrong = run(units, nslot, stages, nbatch, hold=hold, seed=seed)
+            dead, wrong = run(units, nslot, stages, hold=hold, seed=seed)
             assert not dead, f"CTA {b} units {units} hold {hold}: deadlock"
             assert not wrong, f"CTA {b} units {units} hold {hold}: {wrong[:3]}"
 
 
-def test_model_catches_the_earlier_protocol():
-    """A CTA of the 16 x 12288 x 4096 decode schedule whose range is two
-    odd-length units (groups 23..31 of one tile, 0..10 of the next): with one
-    ring shared by the slots and a double arrival for one-group batches, a
-    copy that lands late lets a slot's waits pass a lap early."""
-    nslot, stages, nbatch = config(16)
-    G, T, T_dp, P = schedule(16, 12288, 4096)
-    units = cta_units(17, P, T, G, T_dp)
-    assert [(g0, g1) for _, g0, g1 in units] == [(23, 32), (0, 11)]
-    found = any(run(units, nslot, stages, nbatch, old=True, hold=(0,), seed=s)[1] for s in range(4))
+def test_model_catches_a_skipped_accumulator_wait():
+    """One-group units: each chunk has one group, so a slot is idle in three
+    of every four chunks.  A slot that skipped the accumulator wait in its idle
+    chunks would wait a lap ahead on an accumulator buffer when it next has a
+    group, and pass early while the epilogue is still behind."""
+    nslot, stages = config(16)
+    units = [(t, 0, 1) for t in range(12)]
+    found = any(run(units, nslot, stages, skip_idle_wait=True, hold=(h,), seed=s)[1]
+                for s in range(8) for h in range(6))
     assert found
-    assert not any(run(units, nslot, stages, nbatch, hold=(0,), seed=s)[1] for s in range(4))
+    assert not any(run(units, nslot, stages, hold=(h,), seed=s)[1] for s in range(8) for h in range(6))

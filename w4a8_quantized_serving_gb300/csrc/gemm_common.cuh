@@ -316,6 +316,52 @@ __device__ __forceinline__ void mma_role(const GemmParams& p, uint32_t tmem, uin
 }
 
 // ---------------------------------------------------------------- epilogue --
+// End of a unit for the NEPI epilogue warps: a whole-K tile is written; a
+// split tile's int32 partial sums are added into the workspace, and the last
+// contributor writes Y and leaves the workspace zeroed.  `run` holds tokens
+// tok0 .. tok0 + TOK - 1 of weight row `row` (output channel n; first token m0).
+template <int BN, int NEPI, int TOK>
+__device__ __forceinline__ void finish_unit(const GemmParams& p, const Unit& u, int32_t (&run)[TOK], int m0, int n,
+                                            int tok0, int row, int etid, bool ok, volatile int* last_flag,
+                                            bool tracer, int unit_no) {
+  (void)tracer;
+  (void)unit_no;
+  if (u.g0 == 0 && u.g1 == p.G) {
+    if (ok) write_tile_out<TOK>(p, run, m0, n);
+    return;
+  }
+  const int sk = u.tile - p.T_dp;
+  int32_t* part = p.sk_acc + (size_t)sk * BN * kTileN + (size_t)tok0 * kTileN;
+  if (ok) {
+#pragma unroll
+    for (int i = 0; i < TOK; ++i) red_add_relaxed(part + i * kTileN + row, run[i]);
+  }
+  // The barrier orders every epilogue thread's partial sums before one
+  // thread's acq_rel count update (release is cumulative over the barrier);
+  // the last contributor's acquire makes the other CTAs' sums visible, and the
+  // second barrier passes that on to its warps.
+  if (tracer) QOQ_TRACE_AT(p, 960 + 4 * (unit_no & 7) + 0, 0);
+  named_bar_sync<NEPI * 32>();
+  if (etid == 0) {
+    int last = 0;
+    if (ok) {
+      const int add = u.g1 - u.g0;
+      last = (atom_add_acq_rel(p.sk_cnt + sk, add) + add == p.G) ? 1 : 0;
+      if (last) p.sk_cnt[sk] = 0;  // every contributor has counted: reset for the next call
+    }
+    *last_flag = last;
+  }
+  named_bar_sync<NEPI * 32>();
+  if (tracer) QOQ_TRACE_AT(p, 960 + 4 * (unit_no & 7) + 2, 0);
+  if (ok && *last_flag) {
+#pragma unroll
+    for (int i = 0; i < TOK; ++i) run[i] = __ldcg(part + i * kTileN + row);
+#pragma unroll
+    for (int i = 0; i < TOK; ++i) __stcg(part + i * kTileN + row, 0);  // leave it zeroed
+    write_tile_out<TOK>(p, run, m0, n);
+  }
+}
+
 // NEPI warps (a multiple of 4: warp w reads TMEM lanes 32 (w % 4) ..); warp e
 // owns tokens (e / 4) * TOK .. + TOK of the tile for weight row 32 (w % 4) +
 // lane.  Per fold chunk: read the fp32 accumulator, convert to int32 (exact),
@@ -365,40 +411,8 @@ __device__ __forceinline__ void epilogue_role(const GemmParams& p, uint32_t tmem
         if (e == 0 && lane == 0) QOQ_TRACE_AT(p, 576 + (int)chunk, 0);
       }
     }
-    if (u.g0 == 0 && u.g1 == p.G) {
-      if (ok) write_tile_out<TOK>(p, run, mt * BN + tok0, n);
-    } else {
-      const int sk = u.tile - p.T_dp;
-      int32_t* part = p.sk_acc + (size_t)sk * BN * kTileN + (size_t)tok0 * kTileN;
-      if (ok) {
-#pragma unroll
-        for (int i = 0; i < TOK; ++i) red_add_relaxed(part + i * kTileN + row, run[i]);
-      }
-      // The barrier orders every epilogue thread's partial sums before one
-      // thread's acq_rel count update (release is cumulative over the
-      // barrier); the last contributor's acquire makes the other CTAs' sums
-      // visible, and the second barrier passes that on to its warps.
-      if (e == 0 && lane == 0) QOQ_TRACE_AT(p, 960 + 4 * (unit_no & 7) + 0, 0);
-      named_bar_sync<NEPI * 32>();
-      if (etid == 0) {
-        int last = 0;
-        if (ok) {
-          const int add = u.g1 - u.g0;
-          last = (atom_add_acq_rel(p.sk_cnt + sk, add) + add == p.G) ? 1 : 0;
-          if (last) p.sk_cnt[sk] = 0;  // every contributor has counted: reset for the next call
-        }
-        *last_flag = last;
-      }
-      named_bar_sync<NEPI * 32>();
-      if (e == 0 && lane == 0) QOQ_TRACE_AT(p, 960 + 4 * (unit_no & 7) + 2, 0);
-      if (ok && *last_flag) {
-#pragma unroll
-        for (int i = 0; i < TOK; ++i) run[i] = __ldcg(part + i * kTileN + row);
-#pragma unroll
-        for (int i = 0; i < TOK; ++i) __stcg(part + i * kTileN + row, 0);  // leave it zeroed
-        write_tile_out<TOK>(p, run, mt * BN + tok0, n);
-      }
-    }
+    finish_unit<BN, NEPI, TOK>(p, u, run, mt * BN + tok0, n, tok0, row, etid, ok, last_flag, e == 0 && lane == 0,
+                                unit_no);
     if (e == 0 && lane == 0) QOQ_TRACE_AT(p, 640 + unit_no, 0);
     ++unit_no;
   }

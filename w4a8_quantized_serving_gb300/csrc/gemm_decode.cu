@@ -4,21 +4,35 @@
 // Lecture 15 notes, section 15.5: at decode sizes the weight stream is the
 // floor, and the dequant instructions per weight decide whether the kernel
 // reaches it.  Roles:
-//   warp 0        producer: per 128-channel group one bulk copy of the packed
-//                 weight tile (8448 B) into a 16-stage shared-memory ring.
-//   warp 1        MMA issuer (gemm_common.cuh mma_role): per group 8 x
-//                 tcgen05.mma M=128 (weight rows), N=BN (tokens), K=16.
-//   warps 2..     dequant: NSLOT slots of 4 warps (one per TMEM lane quadrant);
-//                 slot j takes every NSLOT-th group of the CTA's work.  The
-//                 slot's 128 threads read the group's int8 activation slice
-//                 from L2 (issued before their stage wait, so the latency
-//                 overlaps it) and write it as the fp16 B tile into shared
-//                 memory; thread r expands weight row r's 64 code bytes from the
-//                 ring with one mask and one FMA per pair (exact) into the TMEM
-//                 A buffer (tcgen05.st).  Dequantized weights never touch
-//                 shared memory.
-//   last NEPI     epilogue (gemm_common.cuh epilogue_role).
-// The A buffer index also names the B tile, so one A-empty commit frees both.
+//   warps 0, 1    producers (lane 0 of each): per 128-channel group one bulk
+//                 copy of the packed weight tile (8448 B) into shared memory.
+//                 Group gi of the CTA's work belongs to dequant slot
+//                 gi % NSLOT, which owns a sub-ring of SPS stages; each
+//                 producer serves half of the slots.  Warp 1 also allocates
+//                 tensor memory (and frees it at the end).
+//   warps 2..     NSLOT dequant slots of 4 warps, one per TMEM lane quadrant.
+//                 Per group a slot's 128 threads read the group's int8
+//                 activation slice from L2 (issued before their stage wait) and
+//                 write it as the fp16 B tile into the slot's shared buffer;
+//                 thread r expands weight row r's 64 code bytes with one mask
+//                 and one FMA per pair (exact) into the slot's TMEM A buffer.
+//                 After a named barrier of the slot, one elected thread issues
+//                 the group's 8 tcgen05.mma (M=128 weight rows, N=BN tokens,
+//                 K=16) into the slot's own accumulator.  Each slot issues its
+//                 own MMAs: no MMA warp serialises the groups, and no hand-off
+//                 of A buffers between warps is needed.
+//   last NEPI     epilogue: per fold chunk (up to 8 groups per slot) it sums
+//                 the slots' accumulators into int32, and at a unit's end
+//                 writes Y or adds the split-K partial sums
+//                 (gemm_common.cuh finish_unit).
+//
+// Barrier protocol.  mbarrier waits test only the parity of a phase, so each
+// wait must start after the phase before the one it wants has completed, and
+// before the phase after it can complete.  Here every barrier's waiters take
+// part in each of its phases: a weight stage has one producer and one
+// consumer slot, both in order; a slot's MMA-done barrier is waited on only
+// by that slot; every slot waits for and arrives on every fold chunk's
+// accumulator barriers, also in chunks where it has no group.
 #include <mutex>
 
 #include "gemm_common.cuh"
@@ -28,121 +42,53 @@ namespace {
 
 template <int BN>
 struct DecCfg {
-  static constexpr int NSLOT = BN == 64 ? 2 : 4;  // dequant slots (one group each at a time)
+  static constexpr int NSLOT = BN == 64 ? 2 : 4;
   static constexpr int NDQ = 4 * NSLOT;
   static constexpr int NEPI = BN == 64 ? 8 : 4;
   static constexpr int DQ_WARP0 = 2;
   static constexpr int EPI_WARP0 = 2 + NDQ;
   static constexpr int THREADS = (2 + NDQ + NEPI) * 32;
   static constexpr int NACC = 2;
-  static constexpr int ACOL0 = (NACC * BN + 63) / 64 * 64;
-  // MMA hand-off in batches of 2 groups (16 MMAs per wait and commit): each
-  // batch buffer is 2 x 64 TMEM columns of A plus 2 fp16 B tiles.
-  static constexpr int NBATCH = (kTmemCols - ACOL0) / 128;
-  static constexpr int B_BYTES = BN * kGroup * 2;
-  static constexpr int B_TILES = 2 * NBATCH;
-  static constexpr int STAGES_FIT = (kSmemBudget - 2048 - B_TILES * B_BYTES) / kWTileBytes;
-  static constexpr int STAGES = STAGES_FIT > 16 ? 16 : STAGES_FIT;
-  // Each slot has a sub-ring of SPS stages: one producer and one consumer per
-  // stage, both in order, so a phase-parity wait can never be a lap ahead.
-  static constexpr int SPS = STAGES / NSLOT;
-  static constexpr int W_OFF = B_TILES * B_BYTES;
+  // Fold chunk: up to CH consecutive groups of a unit, so at most 8 groups of
+  // each slot go into one fp32 accumulator (exact below 2^24).
+  static constexpr int CH = kFoldGroups * NSLOT;
+  // TMEM columns: accumulator b of slot j at (j * NACC + b) * BN; slot j's A
+  // buffer (128 rows x 128 fp16 = 64 columns) at ACOL0 + 64 j.
+  static constexpr int ACOL0 = (NSLOT * NACC * BN + 63) / 64 * 64;
+  static constexpr int B_BYTES = BN * kGroup * 2;  // slot j's B tile at j * B_BYTES
+  static constexpr int W_OFF = NSLOT * B_BYTES;
+  static constexpr int STAGES_FIT = (kSmemBudget - 2048 - W_OFF) / kWTileBytes;
+  static constexpr int STAGES = (STAGES_FIT > 24 ? 24 : STAGES_FIT) / NSLOT * NSLOT;
+  static constexpr int SPS = STAGES / NSLOT;  // stages per slot
   static constexpr int BAR_OFF = W_OFF + STAGES * kWTileBytes;
-  static constexpr int NBARS = 2 * STAGES + 2 * NBATCH + 2 * NACC + 1;
+  static constexpr int NBARS = 2 * STAGES + NSLOT + 2 * NACC;
   static constexpr int TMEM_SLOT_OFF = BAR_OFF + NBARS * 8;
   static constexpr int FLAG_OFF = TMEM_SLOT_OFF + 8;
   static constexpr int SMEM_BYTES = FLAG_OFF + 8 + 1024;  // + slack for 1024-B alignment
   static_assert(BN == 16 || BN == 32 || BN == 64, "decode tiles");
-  static_assert(NBATCH >= 2 && ACOL0 + 128 * NBATCH <= kTmemCols, "TMEM columns");
-  static_assert(NSLOT % 2 == 0, "slot pairs fill a batch");
-  static_assert(SPS >= 2, "pipeline depth per slot");
+  static_assert(ACOL0 + 64 * NSLOT <= kTmemCols, "TMEM columns");
+  static_assert(SPS >= 2 && STAGES <= 32, "pipeline depth per slot, stage masks");
   static_assert(B_BYTES % 1024 == 0, "1024-B aligned B tiles");
   static_assert(SMEM_BYTES <= kSmemBudget, "shared memory");
 };
 
-// Position of a group in the batch sequence: batches of 2 consecutive groups
-// start at each unit's first group (units and fold chunks have even group
-// offsets, so no batch crosses either), and the last batch of an odd-sized
-// unit holds one group.
-struct BatchPos {
-  uint32_t bi;  // global batch index in the CTA's work
-  int pos;      // 0 or 1 within the batch
-  int nb;       // groups in the batch (1 or 2)
-};
+// Copy-issuing threads: lane 0 of warps 0 .. kProducers - 1 (warp 1 also
+// allocates tensor memory).
+constexpr int kProducers = 2;
 
-// Per-slot counters of the producer (registers, no indexed local array).
-template <int NSLOT>
-struct SlotCounters {
-  uint32_t c[4] = {0, 0, 0, 0};
-  __device__ __forceinline__ uint32_t take(int slot) {
-    uint32_t v = 0;
-#pragma unroll
-    for (int i = 0; i < NSLOT; ++i)
-      if (i == slot) v = c[i]++;
-    return v;
-  }
-  __device__ __forceinline__ uint32_t count(int slot) const {
-    uint32_t v = 0;
-#pragma unroll
-    for (int i = 0; i < NSLOT; ++i)
-      if (i == slot) v = c[i];
-    return v;
-  }
-};
+// Named barrier ID of dequant slot j (0: __syncthreads, 1: the epilogue).
+constexpr int kSlotBar0 = 2;
 
-// Walks the groups of one dequant slot.  Within a unit, group g has batch
-// position t = t0 + (g - g0), where t0 = 2 x (batches before the unit); its
-// batch is t / 2, its place in the batch t % 2, and it belongs to slot
-// t % NSLOT.  So a slot steps NSLOT positions at a time and only recomputes
-// at unit boundaries (stepping through the other slots' groups one by one
-// cost ~0.1 us per step on a sub-partition busy with dequant work).
-// A unit of odd length ends with a one-group batch; its empty second place
-// t0 + len is walked too, as a dummy entry: the slot that owns it waits for
-// the batch's A buffer and arrives on it without writing.  So every slot takes
-// part in every batch of its class (every NSLOT / 2-th batch), and its waits
-// on an A buffer's phase parity always follow its own wait for the lap before
-// (a slot that skipped a batch could otherwise pass a wait a lap early).
+// Slot j's first group in a chunk whose first group has CTA index gc0.
 template <int NSLOT>
-struct SlotWalk {
-  UnitIter it;
-  Unit u;
-  bool have;
-  int g, g_end, slot;  // g_end: end of the unit's positions, rounded up to a full batch
-  uint32_t gi0, t0;    // index of the unit's first group; its batch position
-  __device__ __forceinline__ void enter_unit() {
-    g_end = u.g0 + 2 * ((u.g1 - u.g0 + 1) / 2);
-    g = u.g0 + (int)(((uint32_t)slot - t0) & (NSLOT - 1));
-  }
-  __device__ __forceinline__ void init(const GemmParams& p, int slot_) {
-    slot = slot_;
-    it.init(p);
-    gi0 = t0 = 0;
-    have = it.next(p, u);
-    if (have) enter_unit();
-  }
-  // dummy: the empty second place of a one-group batch (gi, tile, gg unused).
-  __device__ __forceinline__ bool next(const GemmParams& p, int& tile, int& gg, uint32_t& gi, BatchPos& bp,
-                                       bool& dummy) {
-    while (have && g >= g_end) {
-      const uint32_t len = (uint32_t)(u.g1 - u.g0);
-      gi0 += len;
-      t0 += 2 * ((len + 1) / 2);
-      have = it.next(p, u);
-      if (have) enter_unit();
-    }
-    if (!have) return false;
-    const int off = g - u.g0;
-    dummy = g >= u.g1;
-    bp.pos = off & 1;
-    bp.bi = (t0 + (uint32_t)off) >> 1;
-    bp.nb = min(2, u.g1 - (g - bp.pos));
-    tile = u.tile;
-    gg = g;
-    gi = gi0 + (uint32_t)off;
-    g += NSLOT;
-    return true;
-  }
-};
+__device__ __forceinline__ int slot_first(int slot, uint32_t gc0) {
+  return (int)(((uint32_t)slot - gc0) & (NSLOT - 1));
+}
+
+// Named barrier among the 4 warps (128 threads) of one slot, whole warps.
+__device__ __forceinline__ void slot_bar_sync(int slot) {
+  asm volatile("bar.sync %0, 128;" ::"r"(kSlotBar0 + slot) : "memory");
+}
 
 template <int BN>
 __global__ void __launch_bounds__(DecCfg<BN>::THREADS, 1) gemm_decode_kernel(const __grid_constant__ GemmParams p) {
@@ -153,25 +99,20 @@ __global__ void __launch_bounds__(DecCfg<BN>::THREADS, 1) gemm_decode_kernel(con
   const uint32_t sbase = smem_addr(smem);
   const uint32_t bars = sbase + C::BAR_OFF;
   const uint32_t bar_full = bars, bar_empty = bars + 8 * C::STAGES;
-  const uint32_t bar_afull = bars + 8 * (2 * C::STAGES), bar_aempty = bar_afull + 8 * C::NBATCH;
-  const uint32_t bar_accfull = bar_aempty + 8 * C::NBATCH, bar_accempty = bar_accfull + 8 * C::NACC;
-  const uint32_t bar_drain = bar_accempty + 8 * C::NACC;
+  const uint32_t bar_mmadone = bar_empty + 8 * C::STAGES;  // per slot: its MMAs of a group completed
+  const uint32_t bar_accfull = bar_mmadone + 8 * C::NSLOT, bar_accempty = bar_accfull + 8 * C::NACC;
 
   if (threadIdx.x == 0) {
     QOQ_TRACE_AT(p, 0, 0);
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, 4);  // the 4 warps of the dequant slot that read the stage
+      mbar_init(bar_empty + 8 * s, 4);  // the 4 warps of the slot that owns the stage
     }
-    for (int a = 0; a < C::NBATCH; ++a) {
-      mbar_init(bar_afull + 8 * a, 8);  // 4 warps x 2 places (the empty place of a one-group batch too)
-      mbar_init(bar_aempty + 8 * a, 1);
-    }
+    for (int j = 0; j < C::NSLOT; ++j) mbar_init(bar_mmadone + 8 * j, 1);
     for (int b = 0; b < C::NACC; ++b) {
-      mbar_init(bar_accfull + 8 * b, 1);
+      mbar_init(bar_accfull + 8 * b, C::NSLOT);  // one arrival per slot and chunk
       mbar_init(bar_accempty + 8 * b, C::NEPI);
     }
-    mbar_init(bar_drain, 1);
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(sbase + C::TMEM_SLOT_OFF, kTmemCols);
@@ -181,177 +122,208 @@ __global__ void __launch_bounds__(DecCfg<BN>::THREADS, 1) gemm_decode_kernel(con
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + C::TMEM_SLOT_OFF);
   if (threadIdx.x == 0) QOQ_TRACE_AT(p, 1, 0);
 
-  if (warp == 0) {
+  if (warp < kProducers) {
     // ------------------------------------------------------------ producer --
     // Weights only: they do not depend on the preceding kernel, so the ring
-    // fills while it runs.
+    // fills while it runs.  Producer warp w copies the groups of the slots
+    // j with j % kProducers == w (two issuing threads: a copy takes ~0.2-0.3
+    // us to issue while the SM is busy with dequant work).
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();  // each weight tile is read once
       const uint8_t* const packed = p.packed;     // one token tile: weight tile index = tile
       const size_t tile_stride = (size_t)p.G * kWTileBytes;
       const uint32_t w_base = sbase + C::W_OFF;
-      SlotCounters<C::NSLOT> taken;  // groups handed to each slot so far
+      uint32_t issued_mask = 0, issued_par = 0;  // per stage: a copy in its latest lap; its parity
       UnitIter iter;
       iter.init(p);
       Unit u;
-      uint32_t gi = 0, t0 = 0;  // group index; batch position of the unit's first group
+      uint32_t gi = 0;
       bool ok = true;
       while (ok && iter.next(p, u)) {
         const uint8_t* src = packed + (size_t)u.tile * tile_stride + (size_t)u.g0 * kWTileBytes;
         for (int g = u.g0; g < u.g1; ++g, ++gi, src += kWTileBytes) {
-          const int slot = (int)((t0 + (uint32_t)(g - u.g0)) % C::NSLOT);
-          const uint32_t k = taken.take(slot);  // the slot's k-th group
+          const int slot = (int)(gi % C::NSLOT);
+          if (slot % kProducers != warp) continue;
+          const uint32_t k = gi / C::NSLOT;  // the slot's k-th group
           const int s = slot * C::SPS + (int)(k % C::SPS);
-          if (k >= (uint32_t)C::SPS && !wait_bar(bar_empty + 8 * s, ((k / C::SPS) & 1) ^ 1, p)) {
+          const uint32_t ph = (k / C::SPS) & 1;
+          if (k >= (uint32_t)C::SPS && !wait_bar(bar_empty + 8 * s, ph ^ 1, p)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(bar_full + 8 * s, kWTileBytes);
-          bulk_g2s(w_base + s * kWTileBytes, src, kWTileBytes, bar_full + 8 * s, pol);
+          if (!(p.fault == 1 && gi == 17)) {  // test hook: one copy is never issued
+            mbar_arrive_expect_tx(bar_full + 8 * s, kWTileBytes);
+            bulk_g2s(w_base + s * kWTileBytes, src, kWTileBytes, bar_full + 8 * s, pol);
+            issued_mask |= 1u << s;
+            issued_par = (issued_par & ~(1u << s)) | (ph << s);
+          } else {
+            issued_mask &= ~(1u << s);
+          }
           QOQ_TRACE_AT(p, 16 + (int)gi, 0);
         }
-        t0 += 2 * (uint32_t)((u.g1 - u.g0 + 1) / 2);
       }
-      // Let every copy still in flight land before the CTA may exit: the last
-      // min(k, SPS) copies of each slot, one per stage of its sub-ring.
-      for (int slot = 0; slot < C::NSLOT; ++slot) {
-        const uint32_t n = taken.count(slot);
-        for (uint32_t k = n > (uint32_t)C::SPS ? n - C::SPS : 0; k < n; ++k)
-          wait_bar(bar_full + 8 * (slot * C::SPS + (int)(k % C::SPS)), (k / C::SPS) & 1, p, false);
-      }
+      // Let every copy still in flight land before the CTA may exit.
+      for (int s = 0; s < C::STAGES; ++s)
+        if (issued_mask & (1u << s)) wait_bar(bar_full + 8 * s, (issued_par >> s) & 1, p, false);
     }
-    __syncwarp();
-  } else if (warp == 1) {
-    // ---------------------------------------------------------- MMA issuer --
-    // One converged warp, one wait and one commit per batch of 2 groups
-    // (16 MMAs): the hand-off costs ~200 cycles, the 16 MMAs ~300.
-    grid_dep_wait();
-    constexpr uint32_t kIdesc = mma_idesc(BN);
-    UnitIter iter;
-    iter.init(p);
-    Unit u;
-    uint32_t bi = 0, chunk = 0;
-    bool ok = true;
-    while (ok && iter.next(p, u)) {
-      for (int c0 = u.g0; c0 < u.g1; c0 += kFoldGroups) {
-        const int c1 = min(u.g1, c0 + kFoldGroups);
-        const int b = chunk % C::NACC;
-        if (!warp_wait_bar(bar_accempty + 8 * b, ((chunk / C::NACC) & 1) ^ 1, p)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t d_tmem = tmem + b * BN;
-        for (int g = c0; g < c1; g += 2, ++bi) {
-          const int nb = min(2, c1 - g);
-          const int a = bi % C::NBATCH;
-          if (!warp_wait_bar(bar_afull + 8 * a, (bi / C::NBATCH) & 1, p)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          if (lane == 0) QOQ_TRACE_AT(p, 128 + (int)bi, 0);
-          if (elect_one()) {
-            for (int q = 0; q < nb; ++q) {
-              const uint32_t b_lo = desc_sw128_lo(sbase + (uint32_t)((2 * a + q) * C::B_BYTES));
-              const uint32_t a_col = tmem + C::ACOL0 + a * 128 + q * 64;
-#pragma unroll
-              for (int j = 0; j < 8; ++j)  // K step j: 64-channel half j / 4, 32-byte chunk j % 4
-                tc_mma_ts(d_tmem, a_col + 8 * j, b_lo + (j >> 2) * (BN * 8) + (j & 3) * 2, kDescSw128Hi, kIdesc,
-                           (g > c0 || q > 0 || j > 0) ? 1u : 0u);
-            }
-            tc_commit(bar_aempty + 8 * a);
-          }
-          __syncwarp();
-        }
-        if (!ok) break;
-        if (elect_one()) tc_commit(bar_accfull + 8 * b);
-        __syncwarp();
-        ++chunk;
-      }
-    }
-    // all MMAs issued by this warp complete before TMEM is released
-    if (elect_one()) tc_commit(bar_drain);
-    __syncwarp();
-    if (lane == 0) wait_bar(bar_drain, 0, p, false);
     __syncwarp();
   } else if (warp < C::EPI_WARP0) {
-    // ------------------------------------------------------------- dequant --
+    // ------------------------------------------------------ dequant + MMA --
     grid_dep_wait();  // Xq comes from the preceding kernel
     const int slot = (warp - C::DQ_WARP0) >> 2;
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     const int stid = ((warp - C::DQ_WARP0) & 3) * 32 + lane;  // 0..127 within the slot
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-    SlotWalk<C::NSLOT> walk;
-    walk.init(p, slot);
-    int tile, g;
-    uint32_t gi, nown = 0;  // groups of this slot so far: its position in its sub-ring
-    BatchPos bp;
-    bool dummy;
-    while (walk.next(p, tile, g, gi, bp, dummy)) {
-      const int a = bp.bi % C::NBATCH;
-      if (dummy) {  // the empty place of a one-group batch: take part without data
-        if (!wait_bar(bar_aempty + 8 * a, ((bp.bi / C::NBATCH) & 1) ^ 1, p)) break;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_afull + 8 * a);
-        continue;
-      }
-      const int s = slot * C::SPS + (int)(nown % C::SPS);
-      const uint32_t sph = (nown / C::SPS) & 1;
-      ++nown;
-      // int8 activation slice: 16-byte chunk q of the [BN][128] tile is row
-      // q / 8, channels 16 (q % 8) .. +15; rows past M read as zero
-      uint4 xv[BN / 16];
+    const bool issuer = quad == (slot & 3);  // the slots' MMA issuers sit on different sub-partitions
+    constexpr uint32_t kIdesc = mma_idesc(BN);
+    const uint32_t a_col = tmem + C::ACOL0 + 64 * slot;
+    const uint32_t b_lo = desc_sw128_lo(sbase + (uint32_t)(slot * C::B_BYTES));
+    uint8_t* const btile = smem + slot * C::B_BYTES;
+    UnitIter iter;
+    iter.init(p);
+    Unit u;
+    uint32_t gi_u = 0, ch = 0, nown = 0;  // CTA index of the unit's first group; chunk; own groups
+    uint32_t nissued = 0;                 // groups whose MMAs this slot issued
+    // After a wait runs out, a warp keeps the slot's control flow (so that the
+    // slot's other warps never wait at its named barrier for it) but skips its
+    // waits and work, and the kernel winds down.
+    bool ok = true;
+    while (iter.next(p, u)) {
+      for (int c0 = u.g0; c0 < u.g1; c0 += C::CH, ++ch) {
+        const int len = min(C::CH, u.g1 - c0);
+        const uint32_t gc0 = gi_u + (uint32_t)(c0 - u.g0);
+        const int b = ch % C::NACC;
+        const uint32_t d_tmem = tmem + (uint32_t)((slot * C::NACC + b) * BN);
+        // Every slot waits for every chunk's accumulator, with or without a
+        // group in it (see the protocol note above).
+        if (ok) ok = wait_bar(bar_accempty + 8 * b, ((ch / C::NACC) & 1) ^ 1, p);
+        const int f = slot_first<C::NSLOT>(slot, gc0);
+        if (f >= len) {  // no group of this slot in the chunk
+          __syncwarp();
+          if (ok && issuer && lane == 0) mbar_arrive(bar_accfull + 8 * b);
+          continue;
+        }
+        for (int off = f; off < len; off += C::NSLOT, ++nown) {
+          const int g = c0 + off;
+          const uint32_t gi = gc0 + (uint32_t)off;  // the group's index in the CTA's work (traces)
+          (void)gi;
+          const int s = slot * C::SPS + (int)(nown % C::SPS);
+          // int8 activation slice: 16-byte chunk q of the [BN][128] tile is
+          // row q / 8, channels 16 (q % 8) .. +15; rows past M read as zero
+          uint4 xv[BN / 16];
 #pragma unroll
-      for (int i = 0; i < BN / 16; ++i) {
-        const int q = stid + i * 128;
-        const int m = q >> 3;  // one token tile: rows 0 .. BN-1
-        xv[i] = m < p.M ? __ldcg(reinterpret_cast<const uint4*>(p.xq + (size_t)m * p.K + g * kGroup + (q & 7) * 16))
-                        : make_uint4(0, 0, 0, 0);
-      }
-      if (quad == 0 && lane == 0) QOQ_TRACE_AT(p, 192 + (int)gi, 0);
-      if (!wait_bar(bar_full + 8 * s, sph, p)) break;
-      if (quad == 0 && lane == 0) QOQ_TRACE_AT(p, 320 + (int)gi, 0);
-      if (!wait_bar(bar_aempty + 8 * a, ((bp.bi / C::NBATCH) & 1) ^ 1, p)) break;
-      tc_fence_after();  // the MMAs that read this batch buffer are complete
-      if (quad == 0 && lane == 0) QOQ_TRACE_AT(p, 256 + (int)gi, 0);
-      const uint8_t* wt = smem + C::W_OFF + s * kWTileBytes;
-      const uint4 wv0 = *reinterpret_cast<const uint4*>(wt + kWNibOffset + 0 * kWChunkBytes + row * 16);
-      const uint4 wv1 = *reinterpret_cast<const uint4*>(wt + kWNibOffset + 1 * kWChunkBytes + row * 16);
-      const uint4 wv2 = *reinterpret_cast<const uint4*>(wt + kWNibOffset + 2 * kWChunkBytes + row * 16);
-      const uint4 wv3 = *reinterpret_cast<const uint4*>(wt + kWNibOffset + 3 * kWChunkBytes + row * 16);
-      const DequantConsts k = dequant_consts(wt[row], wt[128 + row]);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_empty + 8 * s);  // the weight tile is in registers
-      uint8_t* btile = smem + (2 * a + bp.pos) * C::B_BYTES;
+          for (int i = 0; i < BN / 16; ++i) {
+            const int q = stid + i * 128;
+            const int m = q >> 3;  // one token tile: rows 0 .. BN-1
+            xv[i] = m < p.M ? __ldcg(reinterpret_cast<const uint4*>(p.xq + (size_t)m * p.K + g * kGroup + (q & 7) * 16))
+                            : make_uint4(0, 0, 0, 0);
+          }
+          if (quad == 0 && lane == 0) QOQ_TRACE_AT(p, 192 + (int)gi, 0);
+          if (ok) ok = wait_bar(bar_full + 8 * s, (nown / C::SPS) & 1, p);
+          if (quad == 0 && lane == 0) QOQ_TRACE_AT(p, 320 + (int)gi, 0);
+          // The slot's previous MMAs have read its A buffer and B tile.
+          if (ok) ok = wait_bar(bar_mmadone + 8 * slot, (nown & 1) ^ 1, p);
+          if (ok) {
+            tc_fence_after();
+            if (quad == 0 && lane == 0) QOQ_TRACE_AT(p, 256 + (int)gi, 0);
+            const uint8_t* wt = smem + C::W_OFF + s * kWTileBytes;
+            uint4 wv[4];
 #pragma unroll
-      for (int i = 0; i < BN / 16; ++i) {
-        const int q = stid + i * 128;
-        store_b_chunk(btile, BN, q >> 3, q & 7, xv[i]);
-      }
-      fence_proxy_async_smem();  // generic-proxy writes -> the MMA's async-proxy reads
-      const uint4 wv[4] = {wv0, wv1, wv2, wv3};
+            for (int c = 0; c < 4; ++c) wv[c] = *reinterpret_cast<const uint4*>(wt + kWNibOffset + c * kWChunkBytes + row * 16);
+            const DequantConsts kc = dequant_consts(wt[row], wt[128 + row]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_empty + 8 * s);  // the weight tile is in registers
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t out[16];
-        dequant_chunk(wv[c], k, out);
-        tmem_st16(tmem + lane_base + C::ACOL0 + a * 128 + bp.pos * 64 + c * 16, out);
+            for (int i = 0; i < BN / 16; ++i) {
+              const int q = stid + i * 128;
+              store_b_chunk(btile, BN, q >> 3, q & 7, xv[i]);
+            }
+            fence_proxy_async_smem();  // generic-proxy writes -> the MMA's async-proxy reads
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              uint32_t out[16];
+              dequant_chunk(wv[c], kc, out);
+              tmem_st16(tmem + lane_base + C::ACOL0 + 64 * slot + c * 16, out);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+          }
+          slot_bar_sync(slot);  // the slot's 4 quadrants and its B tile are written
+          if (ok && issuer) {
+            tc_fence_after();
+            if (elect_one()) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j)  // K step j: 64-channel half j / 4, 32-byte chunk j % 4
+                tc_mma_ts(d_tmem, a_col + 8 * j, b_lo + (j >> 2) * (BN * 8) + (j & 3) * 2, kDescSw128Hi, kIdesc,
+                          (off > f || j > 0) ? 1u : 0u);
+              tc_commit(bar_mmadone + 8 * slot);
+              if (off + C::NSLOT >= len) tc_commit(bar_accfull + 8 * b);  // the slot's last group of the chunk
+            }
+            __syncwarp();
+            ++nissued;
+          }
+          if (quad == 0 && lane == 0) QOQ_TRACE_AT(p, 384 + (int)gi, 0);
+        }
       }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if (!(p.fault == 1 && gi == 17)) mbar_arrive(bar_afull + 8 * a);  // test hook: one group never arrives
-        if (quad == 0) QOQ_TRACE_AT(p, 384 + (int)gi, 0);
-        if (quad == 3) QOQ_TRACE_AT(p, 448 + (int)gi, 0);
-      }
+      gi_u += (uint32_t)(u.g1 - u.g0);
     }
+    // the slot's MMAs complete before its tensor memory is released
+    if (issuer && nissued > 0 && lane == 0) wait_bar(bar_mmadone + 8 * slot, (nissued - 1) & 1, p, false);
+    __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue --
     grid_dep_wait();
-    epilogue_role<BN, C::NEPI, C::NACC>(p, tmem, C::EPI_WARP0, bar_accfull, bar_accempty,
-                                        reinterpret_cast<volatile int*>(smem + C::FLAG_OFF));
+    constexpr int TOK = BN / (C::NEPI / 4);
+    static_assert(TOK % 16 == 0, "epilogue loads 16 columns at a time");
+    const int e = warp - C::EPI_WARP0;
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const int tok0 = (e >> 2) * TOK;
+    const int etid = threadIdx.x - C::EPI_WARP0 * 32;
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    volatile int* last_flag = reinterpret_cast<volatile int*>(smem + C::FLAG_OFF);
+    UnitIter iter;
+    iter.init(p);
+    Unit u;
+    uint32_t gi_u = 0, ch = 0;
+    int unit_no = 0;
+    bool ok = true;  // once false, keep the control flow (named barriers) but do no work
+    while (iter.next(p, u)) {
+      int32_t run[TOK];
+#pragma unroll
+      for (int i = 0; i < TOK; ++i) run[i] = 0;
+      for (int c0 = u.g0; c0 < u.g1; c0 += C::CH, ++ch) {
+        const int len = min(C::CH, u.g1 - c0);
+        const uint32_t gc0 = gi_u + (uint32_t)(c0 - u.g0);
+        const int b = ch % C::NACC;
+        if (ok) ok = wait_bar(bar_accfull + 8 * b, (ch / C::NACC) & 1, p);
+        if (e == 0 && lane == 0) QOQ_TRACE_AT(p, 512 + (int)ch, 0);
+        if (ok) {
+          tc_fence_after();
+#pragma unroll
+          for (int j = 0; j < C::NSLOT; ++j) {
+            if (slot_first<C::NSLOT>(j, gc0) >= len) continue;  // slot j had no group here
+#pragma unroll
+            for (int piece = 0; piece < TOK / 16; ++piece) {
+              uint32_t v[16];
+              tmem_ld16_wait(tmem + lane_base + (uint32_t)((j * C::NACC + b) * BN) + tok0 + piece * 16, v);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) run[piece * 16 + i] += __float2int_rn(__uint_as_float(v[i]) * kAccScale);
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_accempty + 8 * b);
+          if (e == 0 && lane == 0) QOQ_TRACE_AT(p, 576 + (int)ch, 0);
+        }
+      }
+      finish_unit<BN, C::NEPI, TOK>(p, u, run, tok0, u.tile * kTileN + row, tok0, row, etid, ok, last_flag,
+                                    e == 0 && lane == 0, unit_no);
+      if (e == 0 && lane == 0) QOQ_TRACE_AT(p, 640 + unit_no, 0);
+      ++unit_no;
+      gi_u += (uint32_t)(u.g1 - u.g0);
+    }
   }
 
   tc_fence_before();
