@@ -301,15 +301,24 @@ __global__ void __launch_bounds__(DecCfg<BN>::THREADS, 1) gemm_decode_kernel(con
         if (e == 0 && lane == 0) QOQ_TRACE_AT(p, 512 + (int)ch, 0);
         if (ok) {
           tc_fence_after();
+          // Slots without a group in the chunk left their accumulator unwritten:
+          // their loads go to a written one and count zero.
+          auto acc_col = [&](int j, int piece) {
+            return tmem + lane_base + (uint32_t)((j * C::NACC + b) * BN) + tok0 + piece * 16;
+          };
 #pragma unroll
-          for (int j = 0; j < C::NSLOT; ++j) {
-            if (slot_first<C::NSLOT>(j, gc0) >= len) continue;  // slot j had no group here
+          for (int piece = 0; piece < TOK / 16; ++piece) {
 #pragma unroll
-            for (int piece = 0; piece < TOK / 16; ++piece) {
-              uint32_t v[16];
-              tmem_ld16_wait(tmem + lane_base + (uint32_t)((j * C::NACC + b) * BN) + tok0 + piece * 16, v);
+            for (int j = 0; j < C::NSLOT; j += 2) {
+              const bool u0 = slot_first<C::NSLOT>(j, gc0) < len, u1 = slot_first<C::NSLOT>(j + 1, gc0) < len;
+              uint32_t v[16], w[16];
+              tmem_ld16x2_wait(acc_col(u0 ? j : j + 1, piece), acc_col(u1 ? j + 1 : j, piece), v, w);
 #pragma unroll
-              for (int i = 0; i < 16; ++i) run[piece * 16 + i] += __float2int_rn(__uint_as_float(v[i]) * kAccScale);
+              for (int i = 0; i < 16; ++i) {
+                const int a0 = u0 ? __float2int_rn(__uint_as_float(v[i]) * kAccScale) : 0;
+                const int a1 = u1 ? __float2int_rn(__uint_as_float(w[i]) * kAccScale) : 0;
+                run[piece * 16 + i] += a0 + a1;
+              }
             }
           }
           tc_fence_before();
