@@ -89,12 +89,14 @@ size_t qoq_packed_weight_bytes(int N, int K, int g);
 
 /*
  * Bytes of device workspace that qoq_w4a8_gemm needs for (M, N, K, g)
- * (host-only; 0 for an unsupported shape).  It holds a status header, the
- * split-K partial sums and tile counters, and (for M > 64) an fp16 copy of Xq
+ * (host-only; 0 for an unsupported shape).  It holds a status header and
+ * the split-K state: for M <= 64 one slot per CTA of partial sums tagged with
+ * the call (BN x 128 x 8 bytes, BN = 16, 32 or 64 as M needs, 160 slots);
+ * for M > 64 tile counters and int32 partial sums, and an fp16 copy of Xq
  * laid out for the tensor-core B operand.
  * The caller zero-fills the workspace once after allocating it (e.g.
- * cudaMemsetAsync); every call that completes leaves it zeroed again, so no
- * per-call clearing is needed.  After a call that reported
+ * cudaMemsetAsync); every call that completes leaves it fit for the next, so
+ * no per-call clearing is needed.  After a call that reported
  * QOQ_ERR_DEVICE_TIMEOUT, zero-fill it again before reuse.  Two calls in
  * flight at the same time must not share one workspace.
  */
@@ -165,15 +167,15 @@ qoq_status qoq_w4a8_gemm(int M, int N, int K, int g, const int8_t* Xq, const uin
  *
  * Arguments, results and argument errors are those of qoq_w4a8_gemm, with no
  * workspace.  The workspace lives in a static device array of
- * QOQ_NO_ALLOC_SCRATCH_BYTES (8 MiB), which every GPU that loads the library's
+ * QOQ_NO_ALLOC_SCRATCH_BYTES (16 MiB), which every GPU that loads the library's
  * device code holds until the process exits.  This entry point allocates
  * nothing and calls no allocating routine.
  *
  * Limit: a shape whose qoq_gemm_workspace_bytes(M, N, K, g) exceeds
  * QOQ_NO_ALLOC_SCRATCH_BYTES returns QOQ_ERR_WORKSPACE before any device
- * access.  With K up to 131072, every N fits for M <= 16.  N <= 65408 fits
- * for M <= 32, and N <= 32640 for M <= 64.  Larger M fits only for small
- * problems.
+ * access.  Every shape with M <= 64 fits (2.5 MiB for M <= 16, 5 MiB for
+ * M <= 32, 10 MiB for M <= 64, whatever N and K).  Larger M fits only for
+ * small problems.
  *
  * The first call on a device (with that device current) looks up the array's
  * device address once and checks the architecture.  Make that first call
@@ -188,7 +190,7 @@ qoq_status qoq_w4a8_gemm(int M, int N, int K, int g, const int8_t* Xq, const uin
  * qoq_last_device_status needs a workspace pointer.  Y is then undefined, and
  * the next call starts from a cleared array.
  */
-#define QOQ_NO_ALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+#define QOQ_NO_ALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 qoq_status qoq_w4a8_gemm_no_alloc(int M, int N, int K, int g, const int8_t* Xq,
                                   const uint16_t* sx_f16, const uint8_t* packed,
                                   const uint16_t* s1_f16, uint16_t* Y_f16, int32_t* acc_debug,

@@ -306,6 +306,7 @@ cudaError_t launch_gemm(int M, int N, int K, const int8_t* Xq, const uint16_t* s
   p.status = reinterpret_cast<int*>(w);
   p.sk_cnt = reinterpret_cast<int32_t*>(w + L.cnt_off);
   p.sk_acc = reinterpret_cast<int32_t*>(w + L.acc_off);
+  p.sk_slot = reinterpret_cast<unsigned long long*>(w + L.slot_off);
   p.xh = reinterpret_cast<const uint16_t*>(w + L.xh_off);
   p.xq = Xq;
   p.packed = packed;

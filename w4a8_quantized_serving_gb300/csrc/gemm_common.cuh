@@ -221,6 +221,21 @@ __device__ __forceinline__ bool wait_seq(uint32_t addr, uint32_t want, const Gem
   return wait_seq_slow(addr, want, p);
 }
 
+// For spin loops on global memory: false once the call's wait limit has run
+// out (recorded as a timeout) or another thread of the call recorded one.
+// t0: 0 before the first check.
+__device__ __noinline__ inline bool spin_ok(const GemmParams& p, uint64_t& t0) {
+  const uint64_t now = global_timer_ns();
+  if (t0 == 0) t0 = now;
+  if (*reinterpret_cast<volatile unsigned*>(p.status + 1) == p.call_id) return false;
+  if (now - t0 > p.timeout_ns) {
+    atomicExch(p.status, kStatusTimeout);
+    atomicExch(reinterpret_cast<unsigned*>(p.status + 1), p.call_id);
+    return false;
+  }
+  return true;
+}
+
 // Lane 0 waits, the warp learns the outcome (keeps the warp converged).
 __device__ __forceinline__ bool warp_wait_bar(uint32_t bar, uint32_t parity, const GemmParams& p) {
   int ok = 1;

@@ -23,8 +23,8 @@
 //                 of A buffers between warps is needed.
 //   last NEPI     epilogue: per fold chunk (up to 8 groups per slot) it sums
 //                 the slots' accumulators into int32, and at a unit's end
-//                 writes Y or adds the split-K partial sums
-//                 (gemm_common.cuh finish_unit).
+//                 writes Y, or hands a split tile's part to the tile's owner
+//                 (see slot_store / slot_gather).
 //
 // Barrier protocol.  mbarrier waits test only the parity of a phase, so each
 // wait must start after the phase before the one it wants has completed, and
@@ -63,8 +63,7 @@ struct DecCfg {
   static constexpr int BAR_OFF = W_OFF + STAGES * kWTileBytes;
   static constexpr int NBARS = 2 * STAGES + NSLOT + 2 * NACC;
   static constexpr int TMEM_SLOT_OFF = BAR_OFF + NBARS * 8;
-  static constexpr int FLAG_OFF = TMEM_SLOT_OFF + 8;
-  static constexpr int SMEM_BYTES = FLAG_OFF + 8 + 1024;  // + slack for 1024-B alignment
+  static constexpr int SMEM_BYTES = TMEM_SLOT_OFF + 8 + 1024;  // + slack for 1024-B alignment
   static_assert(BN == 16 || BN == 32 || BN == 64, "decode tiles");
   static_assert(ACOL0 + 64 * NSLOT <= kTmemCols, "TMEM columns");
   static_assert(SPS >= 2 && STAGES <= 32, "pipeline depth per slot, stage masks");
@@ -88,6 +87,54 @@ __device__ __forceinline__ int slot_first(int slot, uint32_t gc0) {
 // Named barrier among the 4 warps (128 threads) of one slot, whole warps.
 __device__ __forceinline__ void slot_bar_sync(int slot) {
   asm volatile("bar.sync %0, 128;" ::"r"(kSlotBar0 + slot) : "memory");
+}
+
+// The CTA whose stream-K range holds group iteration it (CTA b's range is
+// [floor(b I / P), floor((b + 1) I / P)) of the I = T_sk G iterations).
+__device__ __forceinline__ int sk_cta_of(const GemmParams& p, uint32_t it) {
+  return (int)(((it + 1) * (uint32_t)p.P - 1) / p.I_sk);
+}
+
+// Split-K hand-off of the decode kernel.  A split tile is finished by its
+// owner, the CTA holding the tile's first group: that part is the last unit
+// of its range, so it comes last in time.  Every other contributor holds a
+// later part of the tile as the first unit of its range, and stores it into
+// its own slot as {int32 partial sum, call id} pairs, which are single-copy
+// atomic: the owner reads the slots of the CTAs after it and retries only
+// while an entry does not carry this call's id yet.  No counter, fence or
+// clearing is involved.
+template <int BN, int TOK>
+__device__ __forceinline__ void slot_store(const GemmParams& p, int tok0, int row, const int32_t (&run)[TOK]) {
+  unsigned long long* sl = p.sk_slot + (size_t)blockIdx.x * BN * kTileN;
+  const unsigned long long tag = (unsigned long long)p.call_id << 32;
+#pragma unroll
+  for (int i = 0; i < TOK; ++i) st_relaxed_b64(sl + (tok0 + i) * kTileN + row, tag | (uint32_t)run[i]);
+}
+
+// Pieces of 16 tokens: all 16 loads in flight at once, without holding more
+// registers than that beside the running sums.
+template <int BN, int TOK>
+__device__ __forceinline__ bool slot_gather(const GemmParams& p, int c, int tok0, int row, int32_t (&run)[TOK]) {
+  const unsigned long long* sl = p.sk_slot + (size_t)c * BN * kTileN;
+  uint64_t t0 = 0;
+#pragma unroll
+  for (int piece = 0; piece < TOK; piece += 16) {
+    int32_t part[16];
+    for (uint32_t tries = 1;; ++tries) {
+      bool all = true;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const unsigned long long v = ld_relaxed_b64(sl + (tok0 + piece + i) * kTileN + row);
+        part[i] = (int32_t)(uint32_t)v;
+        all &= (uint32_t)(v >> 32) == p.call_id;
+      }
+      if (all) break;
+      if ((tries & 15) == 0 && !spin_ok(p, t0)) return false;
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) run[piece + i] += part[i];
+  }
+  return true;
 }
 
 template <int BN>
@@ -280,15 +327,13 @@ __global__ void __launch_bounds__(DecCfg<BN>::THREADS, 1) gemm_decode_kernel(con
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     const int tok0 = (e >> 2) * TOK;
-    const int etid = threadIdx.x - C::EPI_WARP0 * 32;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-    volatile int* last_flag = reinterpret_cast<volatile int*>(smem + C::FLAG_OFF);
     UnitIter iter;
     iter.init(p);
     Unit u;
     uint32_t gi_u = 0, ch = 0;
     int unit_no = 0;
-    bool ok = true;  // once false, keep the control flow (named barriers) but do no work
+    bool ok = true;  // once false, do no more work
     while (iter.next(p, u)) {
       int32_t run[TOK];
 #pragma unroll
@@ -327,8 +372,18 @@ __global__ void __launch_bounds__(DecCfg<BN>::THREADS, 1) gemm_decode_kernel(con
           if (e == 0 && lane == 0) QOQ_TRACE_AT(p, 576 + (int)ch, 0);
         }
       }
-      finish_unit<BN, C::NEPI, TOK>(p, u, run, tok0, u.tile * kTileN + row, tok0, row, etid, ok, last_flag,
-                                    e == 0 && lane == 0, unit_no);
+      const int n = u.tile * kTileN + row;  // one token tile: weight tile index = tile
+      if (u.g0 == 0 && u.g1 == p.G) {  // whole tile
+        if (ok) write_tile_out<TOK>(p, run, tok0, n);
+      } else if (u.g0 > 0) {  // a later part of a split tile: its owner adds it
+        if (ok) slot_store<BN, TOK>(p, tok0, row, run);
+      } else {  // the split tile's owner: add the parts of the CTAs after it, then write
+        if (e == 0 && lane == 0) QOQ_TRACE_AT(p, 960 + 4 * (unit_no & 7) + 0, 0);
+        const int b1 = sk_cta_of(p, (uint32_t)(u.tile - p.T_dp) * (uint32_t)p.G + (uint32_t)p.G - 1);
+        for (int c = (int)blockIdx.x + 1; ok && c <= b1; ++c) ok = slot_gather<BN, TOK>(p, c, tok0, row, run);
+        if (e == 0 && lane == 0) QOQ_TRACE_AT(p, 960 + 4 * (unit_no & 7) + 2, 0);
+        if (ok) write_tile_out<TOK>(p, run, tok0, n);
+      }
       if (e == 0 && lane == 0) QOQ_TRACE_AT(p, 640 + unit_no, 0);
       ++unit_no;
       gi_u += (uint32_t)(u.g1 - u.g0);

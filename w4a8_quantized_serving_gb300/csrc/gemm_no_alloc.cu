@@ -108,7 +108,7 @@ extern "C" qoq_status qoq_w4a8_gemm_no_alloc(int M, int N, int K, int g, const i
   // The array keeps whatever the previous call left (normally zeros, but not
   // after a call that ran out of its wait limit), so clear the zero-start part
   // on the stream before every GEMM.
-  const size_t zero_bytes = qoq::gemm_ws_layout(M, N, K).xh_off;
+  const size_t zero_bytes = qoq::gemm_ws_layout(M, N, K).zero_bytes;
   const size_t n16 = zero_bytes / 16;
   size_t blocks = (n16 + 255) / 256;
   if (blocks > 1024) blocks = 1024;

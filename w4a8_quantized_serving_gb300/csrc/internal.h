@@ -18,7 +18,7 @@ constexpr int kWChunkBytes = 2048; // one 32-channel chunk for all 128 rows
 constexpr int kFoldGroups = 8;     // fp32 TMEM partials are folded to int32 every 8 groups
                                    // (1024 channels: 127*127*1024 < 2^24, exact in fp32)
 constexpr int kMaxSkTiles = 512;   // upper bound of split-K tiles per call (workspace sizing)
-constexpr int kMaxGrid = 256;      // upper bound of persistent CTAs per call
+constexpr int kMaxGrid = 160;      // upper bound of persistent CTAs per call (GB300: 152 SMs)
 
 constexpr int kWsHeaderBytes = 256;  // [0] sticky status, [1] id of a call that aborted
 
@@ -33,30 +33,44 @@ inline int gemm_bn_for_m(int M) {
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Workspace partition for (M, N, K); device independent.
+//   token tiles of <= 64 (one tile): header, then one split-K slot per CTA
+//     ([BN][128] entries of {int32 partial sum, uint32 call id});
+//   128-token tiles: header, split-K tile counters, int32 partial tiles, and
+//     the fp16 B-operand copy of Xq.
+// zero_bytes: the prefix that must be zero before the first call.
 struct WsLayout {
-  size_t cnt_off, acc_off, xh_off, total;
+  size_t cnt_off, acc_off, slot_off, xh_off, zero_bytes, total;
 };
 
-// Header, split-K tile counters, split-K int32 partial tiles, and (128-token
-// tiles only) the fp16 B-operand copy of Xq.
 inline WsLayout gemm_ws_layout(int M, int N, int K) {
   const int BN = gemm_bn_for_m(M);
   const long long MT = (M + BN - 1) / BN;
   const long long T = MT * (N / kTileN);
   const long long skmax = T < kMaxSkTiles ? T : kMaxSkTiles;
   WsLayout L;
+  if (BN <= 64) {
+    L.cnt_off = L.acc_off = 0;  // unused
+    L.slot_off = kWsHeaderBytes;
+    L.xh_off = align_up(L.slot_off + (size_t)kMaxGrid * BN * kTileN * 8, 1024);
+    L.zero_bytes = kWsHeaderBytes;
+    L.total = L.xh_off;
+    return L;
+  }
+  L.slot_off = 0;  // unused
   L.cnt_off = kWsHeaderBytes;
   L.acc_off = align_up(L.cnt_off + (size_t)skmax * 4, 256);
   L.xh_off = align_up(L.acc_off + (size_t)skmax * BN * kTileN * 4, 1024);
-  const size_t xh_bytes = BN > 64 ? (size_t)MT * K * BN * 2 : 0;
-  L.total = align_up(L.xh_off + xh_bytes, 256);
+  L.zero_bytes = L.xh_off;
+  L.total = align_up(L.xh_off + (size_t)MT * K * BN * 2, 256);
   return L;
 }
 
 // --------------------------------------------------------------- schedule --
 // Tiles: tile t -> weight tile nt = t / MT, token tile mt = t % MT.
-// Split-K state lives in the workspace and is left zeroed by every call that
-// completes (the last contributor of a tile clears its partial sums and count).
+// Split-K state lives in the workspace.  128-token tiles: int32 sums and
+// counts that every completed call leaves zeroed (the last contributor clears
+// them).  Decode tiles: each CTA's slot holds its partial sums tagged with the
+// call id, so stale slots never need clearing.
 // Tiles [0, T_dp) are processed whole, round-robin over the P CTAs; the
 // remaining T_sk tiles are split along K: their T_sk * G group-iterations are
 // cut into P equal contiguous ranges (stream-K), and partial int32 sums meet
@@ -69,8 +83,9 @@ struct GemmParams {
   const uint16_t* s1;
   uint16_t* Y;
   int32_t* acc_debug;
-  int32_t* sk_acc;  // [T_sk][BN][128]
-  int32_t* sk_cnt;  // [T_sk]
+  int32_t* sk_acc;  // [T_sk][BN][128]  (128-token tiles)
+  int32_t* sk_cnt;  // [T_sk]           (128-token tiles)
+  unsigned long long* sk_slot;  // [P][BN][128] {int32 partial, uint32 call id} (decode tiles)
   int* status;      // workspace header
   int M, N, K, G, MT, NT, T, T_dp, T_sk, P;
   uint32_t I_sk;  // T_sk * G <= 511 * 1024, so 32-bit schedule arithmetic suffices

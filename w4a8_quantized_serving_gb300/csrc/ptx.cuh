@@ -205,6 +205,16 @@ __device__ __forceinline__ void tmem_ld16x2_wait(uint32_t taddr0, uint32_t taddr
       : "memory");
 }
 
+// 64-bit global accesses at gpu scope: single-copy atomic when 8-byte aligned.
+__device__ __forceinline__ void st_relaxed_b64(unsigned long long* addr, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(addr), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_relaxed_b64(const unsigned long long* addr) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(addr) : "memory");
+  return v;
+}
+
 // --------------------------------------------------------- exact rounding --
 
 // rint(x / s) with ties to even, for fp16-valued x and s > 0, without a divide.
