@@ -129,6 +129,9 @@ qoq_status qoq_pack_weights(int N, int K, int g, const uint16_t* W_f16, uint8_t*
  *   an all-zero row gets s_x = 0, Xq = 0.
  * In:  X_f16 [M][K] fp16 bits.  Out: Xq [M][K] int8, sx_f16 [M] fp16 bits.
  * Shape rules as above except that N and g are not involved.
+ * Launched with programmatic dependent launch: it may become resident while
+ * the preceding kernel runs and waits for that kernel to complete before it
+ * reads X or writes Xq and s_x.
  */
 qoq_status qoq_quant_act(int M, int K, const uint16_t* X_f16, int8_t* Xq, uint16_t* sx_f16,
                          qoq_stream_t stream);
@@ -147,7 +150,13 @@ qoq_status qoq_quant_act(int M, int K, const uint16_t* X_f16, int8_t* Xq, uint16
  *      at a time.
  * The kernels are launched with programmatic dependent launch: the GEMM
  * starts streaming weights while the preceding kernel on the stream (e.g.
- * qoq_quant_act) finishes, and waits for it before reading Xq and s_x.
+ * qoq_quant_act) finishes, and waits for it before reading Xq and s_x and
+ * before touching Y, acc_debug or the workspace.  packed and s1_f16 are read
+ * before that wait, so they must not be written by a kernel that can still be
+ * running when this call starts (pack weights once, at load time).  For
+ * M <= 64 the GEMM in turn lets the next kernel on the stream launch as soon
+ * as it starts; that kernel (qoq_quant_act, another qoq_w4a8_gemm) waits for
+ * the GEMM to complete before it reads or writes anything the GEMM uses.
  * A device-side pipeline stall that exceeds the wait limit ends the kernel
  * early, leaves Y undefined and records QOQ_ERR_DEVICE_TIMEOUT in the
  * workspace header, which qoq_last_device_status returns.

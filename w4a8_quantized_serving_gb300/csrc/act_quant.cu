@@ -9,13 +9,16 @@
 // An all-zero row gets s_x = 0 and Xq = 0.
 //
 // Each token row is owned by T threads (T a power of two, 32..1024), each
-// holding up to 16 vectors of 8 fp16 values in registers, so X is read from
-// HBM once; the row max-abs is reduced with warp shuffles (and shared memory
-// when T > 32).  CTAs have 128 threads when T <= 128 (several rows each) so
-// that they fit beside the GEMM's persistent CTAs: the kernel lets the
-// dependent GEMM launch at once (programmatic dependent launch), and the GEMM
-// streams its weights while this kernel runs.  HBM bound: 2 bytes read and
-// 1 byte written per element.
+// holding up to MAXV (4, 8 or 16, fixed at compile time) vectors of 8 fp16
+// values in registers, so X is read from HBM once; the row max-abs is reduced
+// with warp shuffles (and shared memory when T > 32).  CTAs have 128 threads
+// when T <= 128 (several rows each) so that they fit beside the decode GEMM's
+// persistent CTAs.  Both kernels chain by programmatic dependent launch: this
+// kernel lets the dependent GEMM launch at once, and the GEMM streams its
+// weights while this kernel runs; it is itself launched as a dependent, so it
+// can sit resident beside a preceding GEMM and starts reading X the moment
+// that kernel completes.  HBM bound: 2 bytes read and 1 byte written per
+// element.
 #include <cuda_fp16.h>
 
 #include "internal.h"
@@ -23,8 +26,6 @@
 
 namespace qoq {
 namespace {
-
-constexpr int kMaxVecPerThread = 16;  // K <= 131072 with T = 1024
 
 __device__ __forceinline__ float absmax8(uint4 v, float m) {
   const __half2* h = reinterpret_cast<const __half2*>(&v);
@@ -46,11 +47,13 @@ __device__ __forceinline__ uint32_t quant4(const __half* h, float sf, float rf) 
   return r;
 }
 
+template <int MAXV>
 __global__ void __launch_bounds__(1024) act_quant_kernel(const uint16_t* __restrict__ X,
                                                          int8_t* __restrict__ Xq,
                                                          uint16_t* __restrict__ sx, int M, int K,
                                                          int T) {
   grid_dep_launch_dependents();
+  grid_dep_wait();  // X may come from the preceding kernel; Xq and s_x may still be read by it
   __shared__ float warp_max[32];
   const int rows_per_cta = blockDim.x / T;
   const int row = blockIdx.x * rows_per_cta + threadIdx.x / T;
@@ -59,13 +62,13 @@ __global__ void __launch_bounds__(1024) act_quant_kernel(const uint16_t* __restr
   const int nvec = K / 8;
   const bool live = row < M;
   const uint4* xr = reinterpret_cast<const uint4*>(X + (size_t)(live ? row : 0) * K);
-  uint4 v[kMaxVecPerThread];
+  uint4 v[MAXV];
   float amax = 0.0f;
 #pragma unroll
-  for (int i = 0; i < kMaxVecPerThread; ++i) {
+  for (int i = 0; i < MAXV; ++i) {
     const int idx = t + i * T;
     if (live && idx < nvec) {
-      v[i] = __ldg(xr + idx);
+      v[i] = __ldcg(xr + idx);  // L2: X may have been written by the preceding kernel
       amax = absmax8(v[i], amax);
     }
   }
@@ -88,7 +91,7 @@ __global__ void __launch_bounds__(1024) act_quant_kernel(const uint16_t* __restr
 
   uint2* qr = reinterpret_cast<uint2*>(Xq + (size_t)row * K);
 #pragma unroll
-  for (int i = 0; i < kMaxVecPerThread; ++i) {
+  for (int i = 0; i < MAXV; ++i) {
     const int idx = t + i * T;
     if (idx < nvec) {
       uint2 out = make_uint2(0, 0);
@@ -112,8 +115,18 @@ cudaError_t launch_act_quant(int M, int K, const uint16_t* X, int8_t* Xq, uint16
   const int threads = T < 128 ? 128 : T;
   const int rows_per_cta = threads / T;
   const int grid = (M + rows_per_cta - 1) / rows_per_cta;
-  act_quant_kernel<<<grid, threads, 0, s>>>(X, Xq, sx, M, K, T);
-  return cudaGetLastError();
+  const int vpt = (nvec + T - 1) / T;  // <= 4 unless T = 1024; <= 16 for K <= 131072
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(threads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1] = {pdl_attr()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (vpt <= 4) return cudaLaunchKernelEx(&cfg, act_quant_kernel<4>, X, Xq, sx, M, K, T);
+  if (vpt <= 8) return cudaLaunchKernelEx(&cfg, act_quant_kernel<8>, X, Xq, sx, M, K, T);
+  if (vpt <= 16) return cudaLaunchKernelEx(&cfg, act_quant_kernel<16>, X, Xq, sx, M, K, T);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace qoq

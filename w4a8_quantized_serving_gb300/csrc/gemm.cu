@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(256) convert_kernel(const ConvertParams c) {
     const int m = (int)(idx / kc_per_row);
     const int k0 = (int)(idx % kc_per_row) * 16;
     uint4 raw = make_uint4(0, 0, 0, 0);
-    if (m < c.M) raw = __ldg(reinterpret_cast<const uint4*>(c.Xq + (size_t)m * c.K + k0));
+    if (m < c.M) raw = __ldcg(reinterpret_cast<const uint4*>(c.Xq + (size_t)m * c.K + k0));  // L2: from the preceding kernel
     const int g = k0 / kGroup, kc = (k0 % kGroup) / 16;
     const int mt = m / c.BN, r = m % c.BN;
     store_b_chunk(reinterpret_cast<uint8_t*>(c.xh + (size_t)(mt * G + g) * c.BN * kGroup), c.BN, r, kc, raw);

@@ -446,11 +446,5 @@ cudaError_t set_smem_attr_once(Kernel kernel, int bytes, uint64_t& done_mask) {
   return e;
 }
 
-inline cudaLaunchAttribute pdl_attr() {
-  cudaLaunchAttribute a;
-  a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  a.val.programmaticStreamSerializationAllowed = 1;
-  return a;
-}
 
 }  // namespace qoq

@@ -149,6 +149,10 @@ __global__ void __launch_bounds__(DecCfg<BN>::THREADS, 1) gemm_decode_kernel(con
   const uint32_t bar_mmadone = bar_empty + 8 * C::STAGES;  // per slot: its MMAs of a group completed
   const uint32_t bar_accfull = bar_mmadone + 8 * C::NSLOT, bar_accempty = bar_accfull + 8 * C::NACC;
 
+  // The next kernel on the stream may launch now: it waits for this one to
+  // complete before it touches anything this call reads or writes, and its
+  // CTAs take SMs as this call's CTAs leave them.
+  grid_dep_launch_dependents();
   if (threadIdx.x == 0) {
     QOQ_TRACE_AT(p, 0, 0);
     for (int s = 0; s < C::STAGES; ++s) {
@@ -172,9 +176,11 @@ __global__ void __launch_bounds__(DecCfg<BN>::THREADS, 1) gemm_decode_kernel(con
   if (warp < kProducers) {
     // ------------------------------------------------------------ producer --
     // Weights only: they do not depend on the preceding kernel, so the ring
-    // fills while it runs.  Producer warp w copies the groups of the slots
-    // j with j % kProducers == w (two issuing threads: a copy takes ~0.2-0.3
-    // us to issue while the SM is busy with dequant work).
+    // fills while it runs.  Before its first wait for a stage to be released
+    // (timed, like every wait) the producer waits for that kernel too, so the
+    // wait measures this call alone.  Producer warp w copies the groups of the
+    // slots j with j % kProducers == w (two issuing threads: a copy takes
+    // ~0.2-0.3 us to issue while the SM is busy with dequant work).
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();  // each weight tile is read once
       const uint8_t* const packed = p.packed;     // one token tile: weight tile index = tile
@@ -194,6 +200,7 @@ __global__ void __launch_bounds__(DecCfg<BN>::THREADS, 1) gemm_decode_kernel(con
           const uint32_t k = gi / C::NSLOT;  // the slot's k-th group
           const int s = slot * C::SPS + (int)(k % C::SPS);
           const uint32_t ph = (k / C::SPS) & 1;
+          if (k == (uint32_t)C::SPS) grid_dep_wait();
           if (k >= (uint32_t)C::SPS && !wait_bar(bar_empty + 8 * s, ph ^ 1, p)) {
             ok = false;
             break;
@@ -217,6 +224,7 @@ __global__ void __launch_bounds__(DecCfg<BN>::THREADS, 1) gemm_decode_kernel(con
   } else if (warp < C::EPI_WARP0) {
     // ------------------------------------------------------ dequant + MMA --
     grid_dep_wait();  // Xq comes from the preceding kernel
+    if (warp == C::DQ_WARP0 && lane == 0) QOQ_TRACE_AT(p, 3, 0);
     const int slot = (warp - C::DQ_WARP0) >> 2;
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
@@ -296,7 +304,9 @@ __global__ void __launch_bounds__(DecCfg<BN>::THREADS, 1) gemm_decode_kernel(con
             tmem_wait_st();
             tc_fence_before();
           }
+          if (quad == 0 && lane == 0) QOQ_TRACE_AT(p, 832 + (int)gi, 0);
           slot_bar_sync(slot);  // the slot's 4 quadrants and its B tile are written
+          if (quad == 0 && lane == 0) QOQ_TRACE_AT(p, 896 + (int)gi, 0);
           if (ok && issuer) {
             tc_fence_after();
             if (elect_one()) {

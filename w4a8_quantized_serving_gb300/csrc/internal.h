@@ -97,11 +97,13 @@ struct GemmParams {
 
 // Event tracing for pipeline studies: compiled in only with -DQOQ_TRACE.
 // Per CTA kTraceSlots 64-bit slots of %globaltimer (ns, common to all warps):
-// [0], [1] start, [2] end; producer issue of group i at 16+i; MMA issue at
-// 128+i; dequant start/end (slot 0..3, quadrant 0) at 256+i / 384+i; epilogue
-// chunk ready/folded at 512+c / 576+c; unit done at 640+u; per-warp final
-// barrier arrive/depart at 700+2w / 701+2w; MMA warp group start/end at
-// 800+i / 900+i; split-K hand-off steps at 960+4u+{0,1,2}.
+// [0], [1] start, [2] end, [3] dependency wait passed (decode dequant);
+// producer issue of group i at 16+i; MMA issue at 128+i; dequant slice load,
+// stage full, start, end (quadrant 0 of the group's slot) at 192+i, 320+i,
+// 256+i, 384+i; epilogue chunk ready/folded at 512+c / 576+c; unit done at
+// 640+u; per-warp final barrier arrive/depart at 700+2w / 701+2w; MMA warp
+// group start/end at 800+i / 900+i; decode A tile stored / slot barrier
+// passed at 832+i / 896+i; split-K hand-off steps at 960+4u+{0,1,2}.
 constexpr int kTraceSlots = 1024;
 #ifdef QOQ_TRACE
 #define QOQ_TRACE_AT(p, slot, value)                                                     \
@@ -124,6 +126,18 @@ struct ConvertParams {
   uint16_t* xh;
   int M, K, BN, MT;
 };
+
+// Launch attribute for programmatic dependent launch: the kernel may start
+// before the preceding kernel on the stream has finished, once that kernel
+// has triggered (griddepcontrol.launch_dependents) or exited; it must execute
+// griddepcontrol.wait before touching anything the preceding kernels write
+// or read.
+inline cudaLaunchAttribute pdl_attr() {
+  cudaLaunchAttribute a;
+  a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a.val.programmaticStreamSerializationAllowed = 1;
+  return a;
+}
 
 // ---------------------------------------------------------------- launchers --
 cudaError_t launch_act_quant(int M, int K, const uint16_t* X, int8_t* Xq, uint16_t* sx,
