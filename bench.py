@@ -44,10 +44,10 @@ UNIT = "TOPS"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
-def algorithmic_bytes(M: int, N: int, K: int) -> dict:
+def algorithmic_bytes(M: int, N: int, K: int, g: int = 128) -> dict:
     """Bytes the GEMM call must move at least once: q4 nibbles, per-group s2 and
     z, s1, Xq, s_x, and the fp16 output; plus the activation quantizer's."""
-    gemm = N * K // 2 + 2 * N * (K // 128) + 2 * N + M * K + 2 * M + 2 * M * N
+    gemm = N * K // 2 + 2 * N * (K // g) + 2 * N + M * K + 2 * M + 2 * M * N
     act = 2 * M * K + M * K + 2 * M
     return {"gemm": gemm, "act": act, "step": gemm + act}
 
@@ -168,13 +168,13 @@ def oracle_step_timing(c: dict, budget_s: float, n_sample: int | None = None) ->
     n_sample = min(N, n_sample)
     W = synth.weights(n_sample, K, c["seed"])  # the first n_sample output channels
     X = synth.activations(M, K, c["seed"])
-    wq = oracle.weight_quant(synth.bits(W), 128)
+    wq = oracle.weight_quant(synth.bits(W), c.get("g", 128))
     times = []
     t_end = time.perf_counter() + budget_s
     while True:
         t0 = time.perf_counter()
         Xq, sx = oracle.act_quant(synth.bits(X))
-        oracle.gemm(Xq, sx, wq["q4"], wq["s2"], wq["z"], wq["s1"], 128, want_acc=False)
+        oracle.gemm(Xq, sx, wq["q4"], wq["s2"], wq["z"], wq["s1"], c.get("g", 128), want_acc=False)
         times.append(time.perf_counter() - t0)
         if time.perf_counter() >= t_end or len(times) >= 50:
             break
@@ -196,11 +196,11 @@ def run_reference(args, c: dict) -> None:
     n_sample = min(N, 512)
     W = synth.weights(n_sample, K, c["seed"])
     X = synth.activations(M, K, c["seed"])
-    wq = oracle.weight_quant(synth.bits(W), 128)
+    wq = oracle.weight_quant(synth.bits(W), c.get("g", 128))
 
     def step():
         Xq, sx = oracle.act_quant(synth.bits(X))
-        oracle.gemm(Xq, sx, wq["q4"], wq["s2"], wq["z"], wq["s1"], 128, want_acc=False)
+        oracle.gemm(Xq, sx, wq["q4"], wq["s2"], wq["z"], wq["s1"], c.get("g", 128), want_acc=False)
 
     for _ in range(args.warmup):
         step()
@@ -222,7 +222,7 @@ def run_reference(args, c: dict) -> None:
 
 
 def config_dict(c: dict, extra: dict | None = None) -> dict:
-    d = {"workload": c["name"], "M": c["M"], "N": c["N"], "K": c["K"], "g": 128, "seed": c["seed"]}
+    d = {"workload": c["name"], "M": c["M"], "N": c["N"], "K": c["K"], "g": c.get("g", 128), "seed": c["seed"]}
     if extra:
         d.update(extra)
     return d
@@ -250,19 +250,20 @@ def run_ours(args, c: dict) -> None:
     # weights: generated once, packed on the GPU (timed separately), cloned into a pool
     W = torch.from_numpy(synth.weights(N, K, c["seed"])).to(dev)
     X = torch.from_numpy(synth.activations(M, K, c["seed"] + rank)).to(dev)
-    packed, s1 = q.qoq_pack_weights(W)
+    G = c.get("g", 128)
+    packed, s1 = q.qoq_pack_weights(W, g=G)
     torch.cuda.synchronize()
     pk_ev0, pk_ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     pk_ev0.record()
     for _ in range(3):
-        q.qoq_pack_weights(W, packed=packed, s1=s1)
+        q.qoq_pack_weights(W, g=G, packed=packed, s1=s1)
     pk_ev1.record()
     torch.cuda.synchronize()
     pack_ms = pk_ev0.elapsed_time(pk_ev1) / 3
     del W
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    ws_bytes = q.qoq_gemm_workspace_bytes(M, N, K)
+    ws_bytes = q.qoq_gemm_workspace_bytes(M, N, K, G)
     set_bytes = packed.numel() + 2 * N + 2 * M * K + M * K + 2 * M + 2 * M * N + ws_bytes
     nsets = max(2, int(np.ceil(3 * l2 / set_bytes)))
     sets = []
@@ -278,7 +279,7 @@ def run_ours(args, c: dict) -> None:
     def step(i: int):
         s = sets[i % nsets]
         q.qoq_quant_act(s["X"], Xq=s["Xq"], sx=s["sx"])
-        q.qoq_w4a8_gemm(s["Xq"], s["sx"], s["packed"], s["s1"], N, Y=s["Y"], workspace=s["ws"])
+        q.qoq_w4a8_gemm(s["Xq"], s["sx"], s["packed"], s["s1"], N, g=G, Y=s["Y"], workspace=s["ws"])
 
     for i in range(max(3, args.warmup)):
         step(i)
@@ -291,7 +292,7 @@ def run_ours(args, c: dict) -> None:
     # launch-bound at decode sizes; graphs remove the host from the loop).
     def gemm_only(i: int):
         s = sets[i % nsets]
-        q.qoq_w4a8_gemm(s["Xq"], s["sx"], s["packed"], s["s1"], N, Y=s["Y"], workspace=s["ws"])
+        q.qoq_w4a8_gemm(s["Xq"], s["sx"], s["packed"], s["s1"], N, g=G, Y=s["Y"], workspace=s["ws"])
 
     use_graph = not args.no_graph
     g_step = g_gemm = None
@@ -359,7 +360,7 @@ def run_ours(args, c: dict) -> None:
         s = sets[i % nsets]
         s["X"].copy_(Xh, non_blocking=True)
         q.qoq_quant_act(s["X"], Xq=s["Xq"], sx=s["sx"])
-        q.qoq_w4a8_gemm(s["Xq"], s["sx"], s["packed"], s["s1"], N, Y=s["Y"], workspace=s["ws"])
+        q.qoq_w4a8_gemm(s["Xq"], s["sx"], s["packed"], s["s1"], N, g=G, Y=s["Y"], workspace=s["ws"])
         Yh[i % 2].copy_(s["Y"], non_blocking=True)
 
     for i in range(3):
@@ -382,7 +383,7 @@ def run_ours(args, c: dict) -> None:
         ms_per_step, e2e_ms, gemm_ms = (float(v) for v in tt.tolist())
 
     ops = 2.0 * M * N * K
-    nbytes = algorithmic_bytes(M, N, K)
+    nbytes = algorithmic_bytes(M, N, K, G)
     value = world * ops / (ms_per_step * 1e-3) / 1e12
     peaks, peak_src = load_peaks()
     intensity = ops / nbytes["gemm"]
@@ -399,7 +400,10 @@ def run_ours(args, c: dict) -> None:
                 "frac": achieved / pk, "traffic": args.traffic,
                 "peak_source": f"{peak_src} bf16 dense (fp16 operands run at the bf16 rate)"}
     if roof["traffic"] is None:
-        roof["traffic"], roof["traffic_source"] = recorded_traffic(c["name"])
+        if G == 128:
+            roof["traffic"], roof["traffic_source"] = recorded_traffic(c["name"])
+        else:
+            roof["traffic_source"] = f"no ncu record at g = {G}"
     roof["kernel"] = "qoq_w4a8_gemm call (the GEMM kernel; + B-operand convert for M > 64), timed alone over K launches"
     roof["algorithmic_bytes_per_launch"] = nbytes["gemm"]
     roof["ms_per_launch"] = gemm_ms
@@ -447,6 +451,8 @@ def main() -> None:
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=1, help="workload index 0..4 (default 1)")
+    ap.add_argument("--g", type=int, default=128,
+                    help="level-2 group size: 32, 64 or a multiple of 128 dividing K (default 128, the pages' g128)")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle CPU timing")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="time direct launches instead of a CUDA graph")
@@ -454,7 +460,9 @@ def main() -> None:
                     help="DRAM bytes per GEMM launch from an ncu capture of this build, if known")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
-    c = synth.WORKLOADS[args.config]
+    c = dict(synth.WORKLOADS[args.config])
+    if args.g != 128:
+        c["g"] = args.g
     if args.impl == "reference":
         run_reference(args, c)
     else:

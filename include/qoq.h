@@ -1,7 +1,8 @@
 /*
- * qoq.h -- C ABI of the GB300 (sm_103a) W4A8 g128 linear layer of QServe's
- * QoQ scheme: progressive group quantization of the weights, per-token int8
- * activations, and the integer GEMM with an fp16 epilogue.
+ * qoq.h -- C ABI of the GB300 (sm_103a) W4A8 linear layer of QServe's QoQ
+ * scheme (g128, and the other group sizes below): progressive group
+ * quantization of the weights, per-token int8 activations, and the integer
+ * GEMM with an fp16 epilogue.
  *
  * Sources (web pages on W4A8 serving):
  *  [QS]  QServe talk write-up (greptalks.ai, MLSys'25), "Technical Deep Dive":
@@ -28,8 +29,10 @@
  *  - Argument checks happen on the host before any launch and return an error
  *    code without touching the device; launch failures return QOQ_ERR_CUDA.
  *    The library never aborts, prints or throws across this boundary.
- *  - Requirements shared by the compute calls: g == 128 (else
- *    QOQ_ERR_UNSUPPORTED); N % 128 == 0 and K % 128 == 0 (else QOQ_ERR_SHAPE);
+ *  - Requirements shared by the compute calls: N % 128 == 0 and K % 128 == 0
+ *    (else QOQ_ERR_SHAPE); the level-2 group size g is 32, 64, or a multiple
+ *    of 128 that divides K (128 is the pages' g128; g = K is one group per
+ *    output channel) (else QOQ_ERR_UNSUPPORTED);
  *    1 <= M <= 2^24, 128 <= N <= 2^24, 128 <= K <= 131072 (the int32
  *    accumulator bound 127 * 127 * K < 2^31); pointers 16-byte aligned
  *    (else QOQ_ERR_MISALIGNED); a compute capability 10.3 device (else
@@ -53,7 +56,7 @@ typedef enum {
   QOQ_OK = 0,
   QOQ_ERR_NULL = 1,          /* a required pointer is NULL */
   QOQ_ERR_SHAPE = 2,         /* M, N or K out of range or not a multiple of 128 */
-  QOQ_ERR_UNSUPPORTED = 3,   /* group size other than 128 */
+  QOQ_ERR_UNSUPPORTED = 3,   /* group size g not 32, 64 or a multiple of 128 dividing K */
   QOQ_ERR_MISALIGNED = 4,    /* a pointer is not 16-byte aligned */
   QOQ_ERR_WORKSPACE = 5,     /* workspace NULL or smaller than qoq_gemm_workspace_bytes */
   QOQ_ERR_CUDA = 6,          /* a CUDA runtime call or kernel launch failed */
@@ -73,17 +76,21 @@ int qoq_version(void);
  *
  * Layout ([QS] "compute-aware weight reordering": weights are stored in the
  * order the GEMM consumes them, so one contiguous copy serves one pipeline
- * stage): (N/128) x (K/128) tiles of 8448 bytes, tile (nt, j) at offset
- * (nt * (K/128) + j) * 8448, each holding output rows 128*nt .. 128*nt+127
+ * stage): (N/128) x (K/128) k-tiles of T = 256 * S + 8192 bytes, where
+ * S = 128 / g scale sets for g = 32 or 64 and S = 1 for g >= 128 (T = 8448
+ * for g >= 128, 8704 for g = 64, 9216 for g = 32).  Tile (nt, j) sits at
+ * offset (nt * (K/128) + j) * T and holds output rows 128*nt .. 128*nt+127
  * and input channels 128*j .. 128*j+127:
- *   bytes    0..127 : s2[r], the level-2 integer scale of row r (1..16)
- *   bytes  128..255 : z[r],  the level-2 zero point of row r (0..15)
- *   bytes 256..8447 : four 2048-byte chunks c = 0..3 (k = 32c .. 32c+31);
+ *   bytes 256u ..      256u + 127 : s2[r] of scale set u (1..16), u < S
+ *   bytes 256u + 128 .. 256u + 255 : z[r]  of scale set u (0..15)
+ *     (scale set u covers channels 128*j + u*g .. +g-1 when g < 128; for
+ *     g >= 128 the one set repeats the scales of the group the tile lies in)
+ *   bytes 256S .. T-1 : four 2048-byte chunks c = 0..3 (k = 32c .. 32c+31);
  *                     chunk c holds row r's 16 bytes at offset 16 r; inside,
  *                     32-bit word w (k = 32c + 8w .. +7) carries the code of
  *                     k = 32c + 8w + 2i in bits 4i..4i+3 and that of
  *                     k = 32c + 8w + 2i + 1 in bits 16+4i..16+4i+3 (i = 0..3).
- * That is 4 + 16/128 bits per weight plus the fp16 s1 per row.
+ * That is 4 + 16 S/128 bits per weight plus the fp16 s1 per row.
  */
 size_t qoq_packed_weight_bytes(int N, int K, int g);
 
@@ -109,7 +116,7 @@ size_t qoq_gemm_workspace_bytes(int M, int N, int K, int g);
  *     s1[n] = fp16_rn(fp32(max_k |W[n,k]|) / 119)   (IEEE fp32 divide),
  *     Q8[n,k] = clamp(rint(W[n,k] / s1[n]), -119, 119) (fp32 divide, ties even);
  *     an all-zero row, or one whose s1 underflows to 0, gets s1 = 0, Q8 = 0;
- *   level 2, per group of 128 input channels (asymmetric uint4):
+ *   level 2, per group of g input channels (asymmetric uint4):
  *     lo = min(0, min Q8), hi = max(0, max Q8),
  *     s2 = max(1, ceil((hi - lo) / 15)), z = rne(-lo / s2),
  *     q4 = clamp(rne(Q8 / s2) + z, 0, 15)   (exact integer, ties to even),
@@ -140,7 +147,7 @@ qoq_status qoq_quant_act(int M, int K, const uint16_t* X_f16, int8_t* Xq, uint16
  * The W4A8 GEMM ([QS] "Quantized Matrix Multiplication (GEMM) Kernel on
  * GPUs": 4-bit weights are dequantized to 8 bits before the tensor cores,
  * the per-channel scales are applied in the epilogue):
- *   acc[m,n] = sum_k Xq[m,k] * ((q4[n,k] - z[n,k/128]) * s2[n,k/128])  (exact int32),
+ *   acc[m,n] = sum_k Xq[m,k] * ((q4[n,k] - z[n,k/g]) * s2[n,k/g])  (exact int32),
  *   Y[m,n]   = fp16_rn(float(acc[m,n]) * (float(s_x[m]) * float(s1[n]))).
  * In:  Xq [M][K] int8 and sx_f16 [M] (from qoq_quant_act); packed and s1_f16
  *      (from qoq_pack_weights).

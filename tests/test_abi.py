@@ -57,7 +57,17 @@ def test_packed_weight_bytes_closed_form():
         assert nb == N * K // 2 + 2 * N * (K // 128)
         assert nb * 8 / (N * K) == pytest.approx(4.125)
     assert q.qoq_packed_weight_bytes(100, 128, 128) == 0
-    assert q.qoq_packed_weight_bytes(128, 128, 64) == 0
+    assert q.qoq_packed_weight_bytes(128, 128, 96) == 0  # not 32, 64 or a multiple of 128
+    assert q.qoq_packed_weight_bytes(128, 384, 256) == 0  # g must divide K
+
+
+def test_packed_weight_bytes_other_group_sizes():
+    # one uint8 scale and one uint8 zero per group for g < 128; for g >= 128
+    # every 128-channel k-tile repeats its group's scale pair
+    N, K = 256, 1024
+    for g, bits in [(32, 4 + 16 / 32), (64, 4 + 16 / 64), (128, 4.125), (256, 4.125), (1024, 4.125)]:
+        nb = q.qoq_packed_weight_bytes(N, K, g)
+        assert nb * 8 / (N * K) == pytest.approx(bits), g
 
 
 def test_workspace_bytes_host_pure_and_monotone():
@@ -89,7 +99,7 @@ def test_quant_act_validation():
 def test_pack_validation():
     L = _lib()
     assert L.qoq_pack_weights(128, 256, 128, FAKE, None, FAKE, None) == 1
-    assert L.qoq_pack_weights(128, 256, 64, FAKE, FAKE, FAKE, None) == 3
+    assert L.qoq_pack_weights(128, 256, 96, FAKE, FAKE, FAKE, None) == 3
     assert L.qoq_pack_weights(100, 256, 128, FAKE, FAKE, FAKE, None) == 2
     assert L.qoq_pack_weights(128, 256, 128, FAKE, MIS, FAKE, None) == 4
 
@@ -105,7 +115,7 @@ def test_gemm_validation():
 
     assert call(Xq=None) == 1
     assert call(Y=None) == 1
-    assert call(g=32) == 3
+    assert call(g=48) == 3
     assert call(N=200) == 2
     assert call(K=131072 + 128) == 2
     assert call(M=0) == 2

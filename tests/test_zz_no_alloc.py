@@ -56,7 +56,8 @@ def test_no_alloc_rejects_before_touching_the_device():
 
     assert call(Xq=None) == 1
     assert call(Y=None) == 1
-    assert call(g=64) == 3
+    assert call(g=96) == 3
+    assert call(K=384, g=256) == 3  # g must divide K
     assert call(N=200) == 2
     assert call(M=0) == 2
     assert call(K=131072 + 128) == 2

@@ -90,24 +90,24 @@ const char* qoq_status_str(int s) {
 int qoq_version(void) { return 100; }
 
 size_t qoq_packed_weight_bytes(int N, int K, int g) {
-  if (g != kGroup || !shape_ok_nk(N, K)) return 0;
-  return (size_t)(N / qoq::kTileN) * (size_t)(K / kGroup) * qoq::kWTileBytes;
+  if (!shape_ok_nk(N, K) || !qoq::group_size_ok(K, g)) return 0;
+  return (size_t)(N / qoq::kTileN) * (size_t)(K / kGroup) * (size_t)qoq::w_tile_bytes(qoq::gpt_for_group(g));
 }
 
 size_t qoq_gemm_workspace_bytes(int M, int N, int K, int g) {
-  if (g != kGroup || !shape_ok_mk(M, K) || !shape_ok_nk(N, K)) return 0;
+  if (!shape_ok_mk(M, K) || !shape_ok_nk(N, K) || !qoq::group_size_ok(K, g)) return 0;
   return qoq::gemm_ws_layout(M, N, K).total;
 }
 
 qoq_status qoq_pack_weights(int N, int K, int g, const uint16_t* W_f16, uint8_t* packed,
                             uint16_t* s1_f16, qoq_stream_t stream) {
   if (!W_f16 || !packed || !s1_f16) return QOQ_ERR_NULL;
-  if (g != kGroup) return QOQ_ERR_UNSUPPORTED;
   if (!shape_ok_nk(N, K)) return QOQ_ERR_SHAPE;
+  if (!qoq::group_size_ok(K, g)) return QOQ_ERR_UNSUPPORTED;
   if (!aligned16(W_f16) || !aligned16(packed) || !aligned16(s1_f16)) return QOQ_ERR_MISALIGNED;
   qoq_status st = device_info(nullptr);
   if (st != QOQ_OK) return st;
-  return from_cuda(qoq::launch_pack(N, K, W_f16, packed, s1_f16, reinterpret_cast<cudaStream_t>(stream)));
+  return from_cuda(qoq::launch_pack(N, K, g, W_f16, packed, s1_f16, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 qoq_status qoq_quant_act(int M, int K, const uint16_t* X_f16, int8_t* Xq, uint16_t* sx_f16,
@@ -125,8 +125,8 @@ qoq_status qoq_w4a8_gemm(int M, int N, int K, int g, const int8_t* Xq, const uin
                          int32_t* acc_debug, void* workspace, size_t ws_bytes,
                          qoq_stream_t stream) {
   if (!Xq || !sx_f16 || !packed || !s1_f16 || !Y_f16) return QOQ_ERR_NULL;
-  if (g != kGroup) return QOQ_ERR_UNSUPPORTED;
   if (!shape_ok_mk(M, K) || !shape_ok_nk(N, K)) return QOQ_ERR_SHAPE;
+  if (!qoq::group_size_ok(K, g)) return QOQ_ERR_UNSUPPORTED;
   if (!aligned16(Xq) || !aligned16(sx_f16) || !aligned16(packed) || !aligned16(s1_f16) ||
       !aligned16(Y_f16) || (acc_debug && !aligned16(acc_debug)))
     return QOQ_ERR_MISALIGNED;
@@ -139,7 +139,7 @@ qoq_status qoq_w4a8_gemm(int M, int N, int K, int g, const int8_t* Xq, const uin
   if (tmo == 0) tmo = kDefaultTimeoutNs;
   unsigned call_id = g_call_id.fetch_add(1) + 1;
   if (call_id == 0) call_id = g_call_id.fetch_add(1) + 1;  // skip 0 on wrap-around
-  return from_cuda(qoq::launch_gemm(M, N, K, Xq, sx_f16, packed, s1_f16, Y_f16, acc_debug, workspace,
+  return from_cuda(qoq::launch_gemm(M, N, K, g, Xq, sx_f16, packed, s1_f16, Y_f16, acc_debug, workspace,
                                     sms, tmo, g_fault.load(), call_id, g_trace.load(),
                                     reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -147,12 +147,12 @@ qoq_status qoq_w4a8_gemm(int M, int N, int K, int g, const int8_t* Xq, const uin
 qoq_status qoq_unpack_weights_debug(int N, int K, int g, const uint8_t* packed, uint8_t* q4,
                                     uint8_t* s2, uint8_t* z, qoq_stream_t stream) {
   if (!packed || !q4 || !s2 || !z) return QOQ_ERR_NULL;
-  if (g != kGroup) return QOQ_ERR_UNSUPPORTED;
   if (!shape_ok_nk(N, K)) return QOQ_ERR_SHAPE;
+  if (!qoq::group_size_ok(K, g)) return QOQ_ERR_UNSUPPORTED;
   if (!aligned16(packed)) return QOQ_ERR_MISALIGNED;
   qoq_status st = device_info(nullptr);
   if (st != QOQ_OK) return st;
-  return from_cuda(qoq::launch_unpack(N, K, packed, q4, s2, z, reinterpret_cast<cudaStream_t>(stream)));
+  return from_cuda(qoq::launch_unpack(N, K, g, packed, q4, s2, z, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 qoq_status qoq_last_device_status(void* workspace, qoq_stream_t stream) {

@@ -2,9 +2,9 @@
 // 128-token tiles (M > 64).
 //
 // Computes, for Xq [M][K] int8 (per-token scale s_x) and the packed weights
-// (level-2 codes q4, integer scale s2, zero z per 128-channel group; level-1
-// fp16 scale s1 per output channel):
-//   acc[m,n] = sum_k Xq[m,k] * ((q4[n,k] - z[n,k/128]) * s2[n,k/128])   (exact)
+// (level-2 codes q4, integer scale s2, zero z per group of g channels;
+// level-1 fp16 scale s1 per output channel):
+//   acc[m,n] = sum_k Xq[m,k] * ((q4[n,k] - z[n,k/g]) * s2[n,k/g])   (exact)
 //   Y[m,n]   = fp16_rn(float(acc) * (float(s_x[m]) * float(s1[n])))
 // QServe talk write-up, "Quantized Matrix Multiplication (GEMM) Kernel on
 // GPUs" and "Challenges and Design Details": the 4-bit weights are
@@ -35,7 +35,12 @@ namespace {
 
 constexpr int kPrefetchStages = 4;  // weight stages issued before waiting on the preceding kernel
 
+// GPT: level-2 scale sets per packed k-tile (g = 128 / GPT, or a multiple of
+// 128 with GPT = 1).
+template <int GPT>
 struct BulkCfg {
+  static constexpr int TILE = w_tile_bytes(GPT);  // packed k-tile bytes
+  static constexpr int NIB = w_nib_offset(GPT);   // offset of its code chunks
   static constexpr int BN = 128;
   static constexpr int NSLOT = 2;   // groups dequantized concurrently
   static constexpr int NDQ = 4 * NSLOT;
@@ -46,10 +51,10 @@ struct BulkCfg {
   static constexpr int ACOL0 = NACC * BN;
   static constexpr int NABUF = (kTmemCols - ACOL0) / 64;
   static constexpr int B_BYTES = BN * kGroup * 2;
-  static constexpr int STAGE_BYTES = B_BYTES + kWTileBytes;
+  static constexpr int STAGE_BYTES = B_BYTES + TILE;
   static constexpr int STAGES = (kSmemBudget - 2048) / STAGE_BYTES;  // 2 KB: barriers + alignment
   static constexpr int W_OFF = STAGES * B_BYTES;
-  static constexpr int BAR_OFF = W_OFF + STAGES * kWTileBytes;
+  static constexpr int BAR_OFF = W_OFF + STAGES * TILE;
   static constexpr int NBARS = 2 * STAGES + 2 * NABUF + 2 * NACC + 1;
   static constexpr int SEQ_OFF = BAR_OFF + NBARS * 8;  // one 32-bit sequence word per stage
   static constexpr int TMEM_SLOT_OFF = SEQ_OFF + ((STAGES * 4 + 7) / 8) * 8;
@@ -60,8 +65,9 @@ struct BulkCfg {
   static_assert(SMEM_BYTES <= kSmemBudget, "shared memory");
 };
 
-__global__ void __launch_bounds__(BulkCfg::THREADS, 1) gemm_bulk_kernel(const __grid_constant__ GemmParams p) {
-  using C = BulkCfg;
+template <int GPT>
+__global__ void __launch_bounds__(BulkCfg<GPT>::THREADS, 1) gemm_bulk_kernel(const __grid_constant__ GemmParams p) {
+  using C = BulkCfg<GPT>;
   constexpr int BN = C::BN;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -111,10 +117,10 @@ __global__ void __launch_bounds__(BulkCfg::THREADS, 1) gemm_bulk_kernel(const __
       bool have = iter.next(p, u);
       int g = have ? u.g0 : 0;
       uint32_t issued_mask = 0, issued_par = 0;  // per stage: last issue and its parity
-      constexpr uint32_t kStageTx = kWTileBytes + C::B_BYTES;
+      constexpr uint32_t kStageTx = C::TILE + C::B_BYTES;
       auto issue_w = [&](int s, int tile, int gg) {
-        const uint8_t* src = p.packed + ((size_t)(tile / p.MT) * p.G + gg) * kWTileBytes;
-        bulk_g2s(sbase + C::W_OFF + s * kWTileBytes, src, kWTileBytes, bar_full + 8 * s, pol);
+        const uint8_t* src = p.packed + ((size_t)(tile / p.MT) * p.G + gg) * C::TILE;
+        bulk_g2s(sbase + C::W_OFF + s * C::TILE, src, C::TILE, bar_full + 8 * s, pol);
       };
       auto issue_x = [&](int s, int tile, int gg) {
         const uint16_t* src = p.xh + ((size_t)(tile % p.MT) * p.G + gg) * (C::B_BYTES / 2);
@@ -196,12 +202,16 @@ __global__ void __launch_bounds__(BulkCfg::THREADS, 1) gemm_bulk_kernel(const __
           break;
         }
         tc_fence_after();  // the MMAs that read this A buffer are complete
-        const uint8_t* wt = smem + C::W_OFF + s * kWTileBytes;
-        const DequantConsts k = dequant_consts(wt[row], wt[128 + row]);
+        const uint8_t* wt = smem + C::W_OFF + s * C::TILE;
+        DequantConsts k = dequant_consts(wt[row], wt[128 + row]);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
+          if (GPT > 1 && c > 0 && c % (4 / GPT) == 0) {  // scale set u covers chunks u * 4 / GPT ..
+            const int u = c / (4 / GPT);
+            k = dequant_consts(wt[u * 256 + row], wt[u * 256 + 128 + row]);
+          }
           uint32_t out[16];
-          dequant_chunk(*reinterpret_cast<const uint4*>(wt + kWNibOffset + c * kWChunkBytes + row * 16), k, out);
+          dequant_chunk(*reinterpret_cast<const uint4*>(wt + C::NIB + c * kWChunkBytes + row * 16), k, out);
           tmem_st16(tmem + lane_base + C::ACOL0 + a * 64 + c * 16, out);
         }
         tmem_wait_st();
@@ -250,29 +260,40 @@ __global__ void __launch_bounds__(256) convert_kernel(const ConvertParams c) {
   }
 }
 
-cudaError_t launch_bulk(const GemmParams& p, cudaStream_t s) {
+template <int GPT>
+cudaError_t launch_bulk_g(const GemmParams& p, cudaStream_t s) {
+  using C = BulkCfg<GPT>;
   static std::mutex mu;
   static uint64_t done_mask = 0;
   cudaError_t e;
   {
     std::lock_guard<std::mutex> lock(mu);
-    e = set_smem_attr_once(gemm_bulk_kernel, BulkCfg::SMEM_BYTES, done_mask);
+    e = set_smem_attr_once(gemm_bulk_kernel<GPT>, C::SMEM_BYTES, done_mask);
   }
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.P);
-  cfg.blockDim = dim3(BulkCfg::THREADS);
-  cfg.dynamicSmemBytes = BulkCfg::SMEM_BYTES;
+  cfg.blockDim = dim3(C::THREADS);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = s;
   cudaLaunchAttribute attr[1] = {pdl_attr()};
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_bulk_kernel, p);
+  return cudaLaunchKernelEx(&cfg, gemm_bulk_kernel<GPT>, p);
+}
+
+cudaError_t launch_bulk(const GemmParams& p, cudaStream_t s) {
+  switch (p.gpt) {
+    case 1: return launch_bulk_g<1>(p, s);
+    case 2: return launch_bulk_g<2>(p, s);
+    case 4: return launch_bulk_g<4>(p, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace
 
-cudaError_t launch_gemm(int M, int N, int K, const int8_t* Xq, const uint16_t* sx,
+cudaError_t launch_gemm(int M, int N, int K, int g, const int8_t* Xq, const uint16_t* sx,
                         const uint8_t* packed, const uint16_t* s1, uint16_t* Y, int32_t* acc_debug,
                         void* ws, int num_sms, unsigned long long timeout_ns, int fault,
                         unsigned call_id, unsigned long long* trace, cudaStream_t s) {
@@ -283,6 +304,7 @@ cudaError_t launch_gemm(int M, int N, int K, const int8_t* Xq, const uint16_t* s
   p.N = N;
   p.K = K;
   p.G = K / kGroup;
+  p.gpt = gpt_for_group(g);
   p.MT = (M + BN - 1) / BN;
   p.NT = N / kTileN;
   p.T = p.MT * p.NT;

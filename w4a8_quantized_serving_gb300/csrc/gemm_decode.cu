@@ -40,8 +40,12 @@
 namespace qoq {
 namespace {
 
-template <int BN>
+// BN: token tile width; GPT: level-2 scale sets per packed k-tile (g = 128 / GPT,
+// or a multiple of 128 with GPT = 1).
+template <int BN, int GPT>
 struct DecCfg {
+  static constexpr int TILE = w_tile_bytes(GPT);  // packed k-tile bytes
+  static constexpr int NIB = w_nib_offset(GPT);   // offset of its code chunks
   static constexpr int NSLOT = BN == 64 ? 2 : 4;
   static constexpr int NDQ = 4 * NSLOT;
   static constexpr int NEPI = BN == 64 ? 8 : 4;
@@ -57,10 +61,10 @@ struct DecCfg {
   static constexpr int ACOL0 = (NSLOT * NACC * BN + 63) / 64 * 64;
   static constexpr int B_BYTES = BN * kGroup * 2;  // slot j's B tile at j * B_BYTES
   static constexpr int W_OFF = NSLOT * B_BYTES;
-  static constexpr int STAGES_FIT = (kSmemBudget - 2048 - W_OFF) / kWTileBytes;
+  static constexpr int STAGES_FIT = (kSmemBudget - 2048 - W_OFF) / TILE;
   static constexpr int STAGES = (STAGES_FIT > 24 ? 24 : STAGES_FIT) / NSLOT * NSLOT;
   static constexpr int SPS = STAGES / NSLOT;  // stages per slot
-  static constexpr int BAR_OFF = W_OFF + STAGES * kWTileBytes;
+  static constexpr int BAR_OFF = W_OFF + STAGES * TILE;
   static constexpr int NBARS = 2 * STAGES + NSLOT + 2 * NACC;
   static constexpr int TMEM_SLOT_OFF = BAR_OFF + NBARS * 8;
   static constexpr int SMEM_BYTES = TMEM_SLOT_OFF + 8 + 1024;  // + slack for 1024-B alignment
@@ -137,9 +141,9 @@ __device__ __forceinline__ bool slot_gather(const GemmParams& p, int c, int tok0
   return true;
 }
 
-template <int BN>
-__global__ void __launch_bounds__(DecCfg<BN>::THREADS, 1) gemm_decode_kernel(const __grid_constant__ GemmParams p) {
-  using C = DecCfg<BN>;
+template <int BN, int GPT>
+__global__ void __launch_bounds__(DecCfg<BN, GPT>::THREADS, 1) gemm_decode_kernel(const __grid_constant__ GemmParams p) {
+  using C = DecCfg<BN, GPT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -184,7 +188,7 @@ __global__ void __launch_bounds__(DecCfg<BN>::THREADS, 1) gemm_decode_kernel(con
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();  // each weight tile is read once
       const uint8_t* const packed = p.packed;     // one token tile: weight tile index = tile
-      const size_t tile_stride = (size_t)p.G * kWTileBytes;
+      const size_t tile_stride = (size_t)p.G * C::TILE;
       const uint32_t w_base = sbase + C::W_OFF;
       uint32_t issued_mask = 0, issued_par = 0;  // per stage: a copy in its latest lap; its parity
       UnitIter iter;
@@ -193,8 +197,8 @@ __global__ void __launch_bounds__(DecCfg<BN>::THREADS, 1) gemm_decode_kernel(con
       uint32_t gi = 0;
       bool ok = true;
       while (ok && iter.next(p, u)) {
-        const uint8_t* src = packed + (size_t)u.tile * tile_stride + (size_t)u.g0 * kWTileBytes;
-        for (int g = u.g0; g < u.g1; ++g, ++gi, src += kWTileBytes) {
+        const uint8_t* src = packed + (size_t)u.tile * tile_stride + (size_t)u.g0 * C::TILE;
+        for (int g = u.g0; g < u.g1; ++g, ++gi, src += C::TILE) {
           const int slot = (int)(gi % C::NSLOT);
           if (slot % kProducers != warp) continue;
           const uint32_t k = gi / C::NSLOT;  // the slot's k-th group
@@ -206,8 +210,8 @@ __global__ void __launch_bounds__(DecCfg<BN>::THREADS, 1) gemm_decode_kernel(con
             break;
           }
           if (!(p.fault == 1 && gi == 17)) {  // test hook: one copy is never issued
-            mbar_arrive_expect_tx(bar_full + 8 * s, kWTileBytes);
-            bulk_g2s(w_base + s * kWTileBytes, src, kWTileBytes, bar_full + 8 * s, pol);
+            mbar_arrive_expect_tx(bar_full + 8 * s, C::TILE);
+            bulk_g2s(w_base + s * C::TILE, src, C::TILE, bar_full + 8 * s, pol);
             issued_mask |= 1u << s;
             issued_par = (issued_par & ~(1u << s)) | (ph << s);
           } else {
@@ -282,11 +286,17 @@ __global__ void __launch_bounds__(DecCfg<BN>::THREADS, 1) gemm_decode_kernel(con
           if (ok) {
             tc_fence_after();
             if (quad == 0 && lane == 0) QOQ_TRACE_AT(p, 256 + (int)gi, 0);
-            const uint8_t* wt = smem + C::W_OFF + s * kWTileBytes;
+            const uint8_t* wt = smem + C::W_OFF + s * C::TILE;
             uint4 wv[4];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) wv[c] = *reinterpret_cast<const uint4*>(wt + kWNibOffset + c * kWChunkBytes + row * 16);
-            const DequantConsts kc = dequant_consts(wt[row], wt[128 + row]);
+            for (int c = 0; c < 4; ++c) wv[c] = *reinterpret_cast<const uint4*>(wt + C::NIB + c * kWChunkBytes + row * 16);
+            uint32_t s2v[GPT], zv[GPT];  // scale set u covers chunks u * 4 / GPT ..
+#pragma unroll
+            for (int u = 0; u < GPT; ++u) {
+              s2v[u] = wt[u * 256 + row];
+              zv[u] = wt[u * 256 + 128 + row];
+            }
+            DequantConsts kc = dequant_consts(s2v[0], zv[0]);
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_empty + 8 * s);  // the weight tile is in registers
 #pragma unroll
@@ -297,6 +307,7 @@ __global__ void __launch_bounds__(DecCfg<BN>::THREADS, 1) gemm_decode_kernel(con
             fence_proxy_async_smem();  // generic-proxy writes -> the MMA's async-proxy reads
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
+              if (GPT > 1 && c > 0 && c % (4 / GPT) == 0) kc = dequant_consts(s2v[c / (4 / GPT)], zv[c / (4 / GPT)]);
               uint32_t out[16];
               dequant_chunk(wv[c], kc, out);
               tmem_st16(tmem + lane_base + C::ACOL0 + 64 * slot + c * 16, out);
@@ -411,15 +422,15 @@ __global__ void __launch_bounds__(DecCfg<BN>::THREADS, 1) gemm_decode_kernel(con
   }
 }
 
-template <int BN>
+template <int BN, int GPT>
 cudaError_t launch_bn(const GemmParams& p, cudaStream_t s) {
-  using C = DecCfg<BN>;
+  using C = DecCfg<BN, GPT>;
   static std::mutex mu;
   static uint64_t done_mask = 0;
   cudaError_t e;
   {
     std::lock_guard<std::mutex> lock(mu);
-    e = set_smem_attr_once(gemm_decode_kernel<BN>, C::SMEM_BYTES, done_mask);
+    e = set_smem_attr_once(gemm_decode_kernel<BN, GPT>, C::SMEM_BYTES, done_mask);
   }
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -430,16 +441,26 @@ cudaError_t launch_bn(const GemmParams& p, cudaStream_t s) {
   cudaLaunchAttribute attr[1] = {pdl_attr()};
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_decode_kernel<BN>, p);
+  return cudaLaunchKernelEx(&cfg, gemm_decode_kernel<BN, GPT>, p);
+}
+
+template <int GPT>
+cudaError_t launch_gemm_decode_g(const GemmParams& p, int BN, cudaStream_t s) {
+  switch (BN) {
+    case 16: return launch_bn<16, GPT>(p, s);
+    case 32: return launch_bn<32, GPT>(p, s);
+    case 64: return launch_bn<64, GPT>(p, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace
 
 cudaError_t launch_gemm_decode(const GemmParams& p, int BN, cudaStream_t s) {
-  switch (BN) {
-    case 16: return launch_bn<16>(p, s);
-    case 32: return launch_bn<32>(p, s);
-    case 64: return launch_bn<64>(p, s);
+  switch (p.gpt) {
+    case 1: return launch_gemm_decode_g<1>(p, BN, s);
+    case 2: return launch_gemm_decode_g<2>(p, BN, s);
+    case 4: return launch_gemm_decode_g<4>(p, BN, s);
     default: return cudaErrorInvalidValue;
   }
 }

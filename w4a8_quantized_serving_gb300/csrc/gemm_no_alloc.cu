@@ -93,9 +93,9 @@ extern "C" qoq_status qoq_w4a8_gemm_no_alloc(int M, int N, int K, int g, const i
   // Argument checks in the order qoq_w4a8_gemm takes them, all before any
   // device access.
   if (!Xq || !sx_f16 || !packed || !s1_f16 || !Y_f16) return QOQ_ERR_NULL;
-  if (g != qoq::kGroup) return QOQ_ERR_UNSUPPORTED;
-  const size_t need = qoq_gemm_workspace_bytes(M, N, K, g);
+  const size_t need = qoq_gemm_workspace_bytes(M, N, K, qoq::kGroup);  // 0: bad shape (any g)
   if (need == 0) return QOQ_ERR_SHAPE;
+  if (!qoq::group_size_ok(K, g)) return QOQ_ERR_UNSUPPORTED;
   if (!aligned16(Xq) || !aligned16(sx_f16) || !aligned16(packed) || !aligned16(s1_f16) ||
       !aligned16(Y_f16) || (acc_debug && !aligned16(acc_debug)))
     return QOQ_ERR_MISALIGNED;

@@ -10,11 +10,21 @@
 namespace qoq {
 
 // ---------------------------------------------------------------- layouts --
-constexpr int kGroup = 128;        // g: input channels per level-2 group
+constexpr int kGroup = 128;        // input channels per k-tile (the GEMM's unit of K)
 constexpr int kTileN = 128;        // output channels per packed tile / MMA M
-constexpr int kWTileBytes = 8448;  // s2[128] + z[128] + 4 chunks x 128 rows x 16 B
-constexpr int kWNibOffset = 256;   // offset of the nibble chunks inside a tile
 constexpr int kWChunkBytes = 2048; // one 32-channel chunk for all 128 rows
+
+// Level-2 group size g: 32, 64, or a multiple of 128 dividing K.  A packed
+// k-tile (128 rows x 128 channels) holds GPT = max(1, 128 / g) scale sets of
+// s2[128] + z[128] (for g > 128, a group's s2 and z are repeated in each of
+// its k-tiles), then the four 32-channel code chunks.
+inline bool group_size_ok(int K, int g) {
+  return g == 32 || g == 64 || (g >= kGroup && g % kGroup == 0 && K % g == 0);
+}
+inline int gpt_for_group(int g) { return g >= kGroup ? 1 : kGroup / g; }
+__host__ __device__ constexpr int w_nib_offset(int gpt) { return 256 * gpt; }
+__host__ __device__ constexpr int w_tile_bytes(int gpt) { return w_nib_offset(gpt) + 4 * kWChunkBytes; }
+constexpr int kWTileBytes = w_tile_bytes(1);  // g >= 128: 8448 bytes
 constexpr int kFoldGroups = 8;     // fp32 TMEM partials are folded to int32 every 8 groups
                                    // (1024 channels: 127*127*1024 < 2^24, exact in fp32)
 constexpr int kMaxSkTiles = 512;   // upper bound of split-K tiles per call (workspace sizing)
@@ -87,7 +97,8 @@ struct GemmParams {
   int32_t* sk_cnt;  // [T_sk]           (128-token tiles)
   unsigned long long* sk_slot;  // [P][BN][128] {int32 partial, uint32 call id} (decode tiles)
   int* status;      // workspace header
-  int M, N, K, G, MT, NT, T, T_dp, T_sk, P;
+  int M, N, K, G, MT, NT, T, T_dp, T_sk, P;  // G: k-tiles (K / 128)
+  int gpt;                                    // scale sets per k-tile (the kernel's template argument)
   uint32_t I_sk;  // T_sk * G <= 511 * 1024, so 32-bit schedule arithmetic suffices
   unsigned long long timeout_ns;
   int fault;
@@ -142,12 +153,12 @@ inline cudaLaunchAttribute pdl_attr() {
 // ---------------------------------------------------------------- launchers --
 cudaError_t launch_act_quant(int M, int K, const uint16_t* X, int8_t* Xq, uint16_t* sx,
                              cudaStream_t s);
-cudaError_t launch_pack(int N, int K, const uint16_t* W, uint8_t* packed, uint16_t* s1,
+cudaError_t launch_pack(int N, int K, int g, const uint16_t* W, uint8_t* packed, uint16_t* s1,
                         cudaStream_t s);
-cudaError_t launch_unpack(int N, int K, const uint8_t* packed, uint8_t* q4, uint8_t* s2, uint8_t* z,
+cudaError_t launch_unpack(int N, int K, int g, const uint8_t* packed, uint8_t* q4, uint8_t* s2, uint8_t* z,
                           cudaStream_t s);
 cudaError_t launch_gemm_decode(const GemmParams& p, int BN, cudaStream_t s);
-cudaError_t launch_gemm(int M, int N, int K, const int8_t* Xq, const uint16_t* sx,
+cudaError_t launch_gemm(int M, int N, int K, int g, const int8_t* Xq, const uint16_t* sx,
                         const uint8_t* packed, const uint16_t* s1, uint16_t* Y, int32_t* acc_debug,
                         void* ws, int num_sms, unsigned long long timeout_ns, int fault,
                         unsigned call_id, unsigned long long* trace, cudaStream_t s);
