@@ -85,6 +85,8 @@ class Oracle:
         lib.qoq_oracle_gemm.restype = i32
         lib.qoq_oracle_gemm_entries.argtypes = [i32, P, P, i32, i32, P, P, P, P, P, P, P, P]
         lib.qoq_oracle_gemm_entries.restype = i32
+        lib.qoq_oracle_norm_quant_act.argtypes = [i32, i32, i32, ctypes.c_float, P, P, P, P, P, P, P, P]
+        lib.qoq_oracle_norm_quant_act.restype = i32
         self.lib = lib
         self.path = path
 
@@ -170,6 +172,29 @@ class Oracle:
         return acc, Y
 
 
+    def norm_quant_act(self, X_bits, gamma_bits, beta_bits=None, kind: str = "rms", eps: float = 1e-6):
+        """The norm (RMSNorm, or LayerNorm with beta) fused with the per-token
+        int8 quantizer, on fp16 X [M][K] (uint16 bits).  Returns a dict with
+        Y (the fp16 normalized rows, bits), Xq, sx (bits), r and mu per row
+        (float32) and the exact row sums S1 (units 2^-24) and S2 (units 2^-48,
+        as a Python int per row)."""
+        X = _c(X_bits, np.uint16)
+        M, K = X.shape
+        k = {"rms": 0, "layer": 1}[kind]
+        g = _c(gamma_bits, np.uint16)
+        b = None if beta_bits is None else _c(beta_bits, np.uint16)
+        Y = np.empty((M, K), np.uint16)
+        Xq = np.empty((M, K), np.int8)
+        sx = np.empty(M, np.uint16)
+        rmu = np.empty((M, 2), np.float32)
+        st = np.empty((M, 4), np.int64)
+        _check(self.lib.qoq_oracle_norm_quant_act(M, K, k, float(eps), _p(X), _p(g), None if b is None else _p(b),
+                                                  _p(Y), _p(Xq), _p(sx), _p(rmu), _p(st)), "norm_quant_act")
+        S2 = [int(np.uint64(st[i, 1])) + (int(np.uint64(st[i, 2])) << 64) for i in range(M)]
+        return {"Y": Y, "Xq": Xq, "sx": sx, "r": rmu[:, 0].copy(), "mu": rmu[:, 1].copy(),
+                "S1": st[:, 0].copy(), "S2": S2}
+
+
 _DEFAULT: Oracle | None = None
 
 
@@ -184,6 +209,6 @@ def default() -> Oracle:
 def __getattr__(name):
     # module-level shortcuts: oracle.weight_quant(...) etc. use the default build
     if name in ("half_to_double", "double_to_half", "dequant_code", "dequant_real", "weight_quant",
-                "dequant_weights", "act_quant", "gemm", "gemm_entries"):
+                "dequant_weights", "act_quant", "gemm", "gemm_entries", "norm_quant_act"):
         return getattr(default(), name)
     raise AttributeError(name)

@@ -32,6 +32,8 @@
  *     Xq = clamp(rint(X / s_x), -127, 127).
  *  R4 an all-zero row (or a scale that underflows to fp16 zero) gets scale 0 and
  *     codes 0; its level-2 groups get s2 = 1, z = 0.
+ *  R6, R7 (the norm fused with the activation quantizer): see
+ *     qoq_oracle_norm_quant_act.
  *  R5 acc[m,n] = sum_k Xq[m,k] * ((q4[n,k] - z[n,k/g]) * s2[n,k/g]) in int64;
  *     Y[m,n] = fp16_rn(acc * s_x[m] * s1[n]) with the product taken in double
  *     (exact: 31 + 11 + 11 significant bits fit in 53), rounded once.
@@ -290,5 +292,83 @@ int qoq_oracle_gemm_entries(int count, const int32_t* m_idx, const int32_t* n_id
     if (acc) acc[i] = a;
     if (Y) Y[i] = epilogue(a, sx[m], s1[n]);
   }
+  return QOQ_ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* norm fused with the activation quantizer                                  */
+/* ------------------------------------------------------------------------ */
+
+/* QServe talk write-up, "Precision Data Flow and Activation Quantization
+ * Fusion": a linear layer's input quantization is fused into the preceding
+ * layer, such as LayerNorm, whose output is quantized to 8 bits directly.
+ * The pages give no norm arithmetic; the readings taken:
+ *  R6 the row statistics are exact: S1 = sum_k x_k and S2 = sum_k x_k^2 as
+ *     integers in units of 2^-24 and 2^-48 (every fp16 x is an integer
+ *     multiple of 2^-24), so they do not depend on summation order;
+ *  R7 RMSNorm (kind 0): r = fl32(1 / sqrt(fl64(S2) / K + eps)), each double
+ *     operation rounded to nearest (fl64(S2): the exact sum rounded to double),
+ *     y_k = fp16_rn(fl32(fl32(x_k * r) * gamma_k));
+ *     LayerNorm (kind 1): mu = fl32(fl64(S1) / K),
+ *     var = fl64(K S2 - S1^2) / K^2, r = fl32(1 / sqrt(var + eps)),
+ *     y_k = fp16_rn(fl32(fl32(fl32(fl32(x_k - mu) * r) * gamma_k) + beta_k));
+ *     eps > 0;
+ *  then y is quantized per token exactly as qoq_oracle_act_quant does (R3).
+ * Optional outputs: the fp16 row y (Y) and r and mu per row (rmu, 2 floats). */
+int qoq_oracle_norm_quant_act(int M, int K, int kind, float eps, const uint16_t* X,
+                              const uint16_t* gamma, const uint16_t* beta, uint16_t* Y, int8_t* Xq,
+                              uint16_t* sx, float* rmu, int64_t* stats) {
+  if (M <= 0 || K <= 0 || (kind != 0 && kind != 1) || !(eps > 0.0f) || !X || !gamma ||
+      (kind == 1 && !beta) || !Xq || !sx)
+    return QOQ_ORACLE_EARG;
+  uint16_t* yrow = (uint16_t*)malloc((size_t)K * sizeof(uint16_t));
+  if (!yrow) return QOQ_ORACLE_EARG;
+  for (int m = 0; m < M; ++m) {
+    const uint16_t* xrow = X + (size_t)m * K;
+    int64_t s1 = 0;          /* units of 2^-24 */
+    unsigned __int128 s2 = 0; /* units of 2^-48 */
+    for (int k = 0; k < K; ++k) {
+      int64_t a = (int64_t)(qoq_oracle_half_to_double(xrow[k]) * 16777216.0); /* exact */
+      uint64_t mag = (uint64_t)(a < 0 ? -a : a);
+      s1 += a;
+      s2 += (unsigned __int128)mag * mag;
+    }
+    if (stats) {
+      stats[4 * m + 0] = s1;
+      stats[4 * m + 1] = (int64_t)(uint64_t)s2;
+      stats[4 * m + 2] = (int64_t)(uint64_t)(s2 >> 64);
+      stats[4 * m + 3] = 0;
+    }
+    volatile double spread; /* mean square (kind 0) or variance (kind 1) */
+    float mu = 0.0f;
+    if (kind == 0) {
+      spread = ((double)s2 * 0x1p-48) / (double)K;
+    } else {
+      unsigned __int128 a1 = (unsigned __int128)(uint64_t)(s1 < 0 ? -s1 : s1);
+      unsigned __int128 v = (unsigned __int128)K * s2 - a1 * a1; /* >= 0, exact */
+      spread = ((double)v * 0x1p-48) / ((double)K * (double)K);
+      volatile double mu_d = ((double)s1 * 0x1p-24) / (double)K;
+      mu = (float)mu_d;
+    }
+    volatile double den = spread + (double)eps;
+    volatile double sq = sqrt(den);
+    volatile double rd = 1.0 / sq;
+    const float r = (float)rd;
+    if (rmu) {
+      rmu[2 * m] = r;
+      rmu[2 * m + 1] = mu;
+    }
+    for (int k = 0; k < K; ++k) {
+      float x = (float)qoq_oracle_half_to_double(xrow[k]);
+      volatile float t = kind == 1 ? x - mu : x;
+      volatile float u = t * r;
+      volatile float w = u * (float)qoq_oracle_half_to_double(gamma[k]);
+      if (kind == 1) w = w + (float)qoq_oracle_half_to_double(beta[k]);
+      yrow[k] = qoq_oracle_double_to_half((double)w);
+    }
+    if (Y) memcpy(Y + (size_t)m * K, yrow, (size_t)K * sizeof(uint16_t));
+    symmetric_row(K, yrow, 127, &sx[m], Xq + (size_t)m * K);
+  }
+  free(yrow);
   return QOQ_ORACLE_OK;
 }

@@ -327,9 +327,115 @@ def check_acc_range(o) -> None:
     assert int(acc[0, 0]) == 127 * 120 * K
 
 
+# ------------------------------------------------------------------- norm --
+# The norm fused with the activation quantizer ([QS] "Precision Data Flow and
+# Activation Quantization Fusion").  Pins: exact rational sums, closed forms
+# (constant rows, unit rows), an error bound against the exact normalization
+# computed with rationals, and the composition with the pinned quantizer.
+
+def _ulp16(v: float) -> float:
+    """Spacing of binary16 values at magnitude v (2^-24 in the subnormal range)."""
+    v = abs(v)
+    if v < 2.0 ** -14:
+        return 2.0 ** -24
+    e = int(np.floor(np.log2(v)))
+    return 2.0 ** (e - 10)
+
+
+def _bits16(a) -> np.ndarray:
+    return np.asarray(a, dtype=np.float16).view(np.uint16)
+
+
+def check_norm_exact_stats(o) -> None:
+    """S1 = sum x and S2 = sum x^2 are exact (rationals), even across the full
+    fp16 range in one row."""
+    rng = np.random.default_rng(11)
+    K = 512
+    X = rng.standard_normal((3, K)).astype(np.float16)
+    X[0, :6] = [65504.0, -65504.0, 2.0 ** -24, -(2.0 ** -24), 2.0 ** -14, 3.0 * 2.0 ** -24]
+    X[1, :] = np.float16(2.0 ** -24) * rng.integers(1, 1024, K).astype(np.float16)  # subnormals only
+    X[2, ::7] = np.float16(60000.0)
+    r = o.norm_quant_act(_bits16(X), _bits16(np.ones(K)), kind="rms", eps=1e-3)
+    for m in range(3):
+        xs = [Fraction(float(v)) for v in X[m].astype(np.float64)]
+        s1, s2 = sum(xs), sum(v * v for v in xs)
+        assert int(r["S1"][m]) == s1 * 2 ** 24, m
+        assert r["S2"][m] == s2 * 2 ** 48, m
+
+
+def check_norm_layer_constant_row(o) -> None:
+    """LayerNorm of a constant row: x - mu = 0, so y = beta exactly, whatever gamma."""
+    K = 384
+    rng = np.random.default_rng(12)
+    X = np.full((2, K), 0.75, np.float16)
+    X[1] = np.float16(-3.5)
+    gamma = rng.uniform(0.5, 2.0, K).astype(np.float16)
+    beta = rng.uniform(-1.0, 1.0, K).astype(np.float16)
+    r = o.norm_quant_act(_bits16(X), _bits16(gamma), _bits16(beta), kind="layer", eps=1e-5)
+    assert np.array_equal(r["Y"], np.tile(_bits16(beta), (2, 1)))
+    assert float(r["mu"][0]) == 0.75 and float(r["mu"][1]) == -3.5
+
+
+def check_norm_rms_unit_row(o) -> None:
+    """RMSNorm of a row of +-1 with gamma = 1 and eps = 2^-30: the mean square is
+    1 and 1/sqrt(1 + 2^-30) rounds to 1 in fp32, so y = x."""
+    K = 256
+    rng = np.random.default_rng(13)
+    X = np.where(rng.random((2, K)) < 0.5, -1.0, 1.0).astype(np.float16)
+    r = o.norm_quant_act(_bits16(X), _bits16(np.ones(K)), kind="rms", eps=2.0 ** -30)
+    assert np.all(r["r"] == np.float32(1.0))
+    assert np.array_equal(r["Y"], _bits16(X))
+
+
+def check_norm_error_bound(o) -> None:
+    """y is within half an fp16 ulp plus a few fp32 roundings of the exact
+    normalization, computed with rationals (sqrt to 40 digits).  A large eps
+    keeps it visible in y."""
+    from decimal import Decimal, getcontext
+
+    getcontext().prec = 40
+    rng = np.random.default_rng(14)
+    K = 96
+    X = (rng.standard_normal((4, K)) * np.array([[0.3], [1.0], [0.05], [2.0]])).astype(np.float16)
+    X[3] += np.float16(1.5)  # a row with a mean far from zero
+    gamma = rng.uniform(0.5, 2.0, K).astype(np.float16)
+    beta = rng.uniform(-0.5, 0.5, K).astype(np.float16)
+    for kind, eps in (("rms", 0.25), ("layer", 0.125)):
+        r = o.norm_quant_act(_bits16(X), _bits16(gamma), _bits16(beta) if kind == "layer" else None,
+                             kind=kind, eps=eps)
+        y = r["Y"].view(np.float16).astype(np.float64)
+        for m in range(X.shape[0]):
+            xs = [Fraction(float(v)) for v in X[m].astype(np.float64)]
+            mu = sum(xs) / K if kind == "layer" else Fraction(0)
+            spread = sum((v - mu) ** 2 for v in xs) / K
+            rstar = 1 / (Decimal(spread.numerator) / Decimal(spread.denominator) + Decimal(eps)).sqrt()
+            for k in range(K):
+                c = (Decimal((xs[k] - mu).numerator) / Decimal((xs[k] - mu).denominator)) * rstar * \
+                    Decimal(float(gamma[k]))
+                b = Decimal(float(beta[k])) if kind == "layer" else Decimal(0)
+                ystar = float(c + b)
+                bound = 0.5 * _ulp16(max(abs(ystar), abs(y[m, k]))) + 2.0 ** -24 * (
+                    8 * abs(float(c)) + 2 * abs(float(mu)) * float(rstar) * float(gamma[k]) + 2 * abs(float(b))) + 2.0 ** -40
+                assert abs(y[m, k] - ystar) <= bound, (kind, m, k, y[m, k], ystar)
+
+
+def check_norm_quant_composition(o) -> None:
+    """The fused quantization equals the per-token quantizer applied to the
+    normalized fp16 rows."""
+    rng = np.random.default_rng(15)
+    X = (rng.standard_normal((3, 640)) * 3).astype(np.float16)
+    gamma = rng.uniform(0.5, 2.0, 640).astype(np.float16)
+    beta = rng.uniform(-1, 1, 640).astype(np.float16)
+    for kind in ("rms", "layer"):
+        r = o.norm_quant_act(_bits16(X), _bits16(gamma), _bits16(beta), kind=kind, eps=1e-6)
+        Xq, sx = o.act_quant(r["Y"])
+        assert np.array_equal(Xq, r["Xq"]) and np.array_equal(sx, r["sx"])
+
+
 ALL_CHECKS = [
     check_half_to_double, check_double_to_half, check_appendix_a, check_appendix_a_g128,
     check_fig3_literal, check_level1_bruteforce, check_level2_bruteforce, check_invariants,
     check_error_bounds, check_lossless_grid, check_zero_and_underflow, check_gemm_library,
-    check_acc_range,
+    check_acc_range, check_norm_exact_stats, check_norm_layer_constant_row, check_norm_rms_unit_row,
+    check_norm_error_bound, check_norm_quant_composition,
 ]
