@@ -56,7 +56,7 @@ typedef enum {
   QOQ_OK = 0,
   QOQ_ERR_NULL = 1,          /* a required pointer is NULL */
   QOQ_ERR_SHAPE = 2,         /* M, N or K out of range or not a multiple of 128 */
-  QOQ_ERR_UNSUPPORTED = 3,   /* group size g not 32, 64 or a multiple of 128 dividing K */
+  QOQ_ERR_UNSUPPORTED = 3,   /* group size g not 32, 64 or a multiple of 128 dividing K; bad norm kind or eps */
   QOQ_ERR_MISALIGNED = 4,    /* a pointer is not 16-byte aligned */
   QOQ_ERR_WORKSPACE = 5,     /* workspace NULL or smaller than qoq_gemm_workspace_bytes */
   QOQ_ERR_CUDA = 6,          /* a CUDA runtime call or kernel launch failed */
@@ -142,6 +142,34 @@ qoq_status qoq_pack_weights(int N, int K, int g, const uint16_t* W_f16, uint8_t*
  */
 qoq_status qoq_quant_act(int M, int K, const uint16_t* X_f16, int8_t* Xq, uint16_t* sx_f16,
                          qoq_stream_t stream);
+
+/* Norm kinds of qoq_norm_quant_act. */
+typedef enum { QOQ_NORM_RMS = 0, QOQ_NORM_LAYER = 1 } qoq_norm_kind;
+
+/*
+ * The preceding norm fused with the per-token int8 quantizer ([QS] "Precision
+ * Data Flow and Activation Quantization Fusion": activation quantization is
+ * fused into the preceding layer, such as LayerNorm, whose output is
+ * quantized to 8 bits directly, without writing the normalized fp16 rows).
+ * Per token row x (K fp16 values), with exact row statistics
+ * S1 = sum_k x_k, S2 = sum_k x_k^2 (integers in units of 2^-24 and 2^-48) and
+ * every double operation rounded to nearest:
+ *   QOQ_NORM_RMS:   r = fl32(1 / sqrt(fl64(S2) / K + eps)),
+ *                   y_k = fp16_rn(fl32(fl32(x_k * r) * gamma_k));
+ *   QOQ_NORM_LAYER: mu = fl32(fl64(S1) / K),
+ *                   r = fl32(1 / sqrt(fl64(K S2 - S1^2) / K^2 + eps)),
+ *                   y_k = fp16_rn(fl32(fl32(fl32(fl32(x_k - mu) * r) * gamma_k) + beta_k));
+ * then s_x and Xq of the rows y exactly as qoq_quant_act computes them.
+ * In:  X_f16 [M][K] fp16 bits (finite values), gamma_f16 [K], beta_f16 [K]
+ *      (LayerNorm only; may be NULL for RMSNorm), eps > 0 and finite.
+ * Out: Xq [M][K] int8, sx_f16 [M] fp16 bits.
+ * Errors: QOQ_ERR_UNSUPPORTED for an unknown kind or eps <= 0; otherwise as
+ * qoq_quant_act.  Launched like qoq_quant_act (programmatic dependent launch:
+ * it waits for the preceding kernel before reading X or writing its outputs).
+ */
+qoq_status qoq_norm_quant_act(int M, int K, int kind, float eps, const uint16_t* X_f16,
+                              const uint16_t* gamma_f16, const uint16_t* beta_f16, int8_t* Xq,
+                              uint16_t* sx_f16, qoq_stream_t stream);
 
 /*
  * The W4A8 GEMM ([QS] "Quantized Matrix Multiplication (GEMM) Kernel on

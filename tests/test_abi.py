@@ -96,6 +96,20 @@ def test_quant_act_validation():
     assert L.qoq_quant_act(16, 4096, MIS, FAKE, FAKE, None) == 4
 
 
+def test_norm_quant_act_validation():
+    L = _lib()
+    f = ctypes.c_float
+    assert L.qoq_norm_quant_act(16, 4096, 0, f(1e-6), None, FAKE, None, FAKE, FAKE, None) == 1
+    assert L.qoq_norm_quant_act(16, 4096, 1, f(1e-6), FAKE, FAKE, None, FAKE, FAKE, None) == 1  # LayerNorm needs beta
+    assert L.qoq_norm_quant_act(16, 4096, 2, f(1e-6), FAKE, FAKE, FAKE, FAKE, FAKE, None) == 3
+    assert L.qoq_norm_quant_act(16, 4096, 0, f(0.0), FAKE, FAKE, None, FAKE, FAKE, None) == 3
+    assert L.qoq_norm_quant_act(16, 4096, 0, f(float("nan")), FAKE, FAKE, None, FAKE, FAKE, None) == 3
+    assert L.qoq_norm_quant_act(16, 4096, 0, f(float("inf")), FAKE, FAKE, None, FAKE, FAKE, None) == 3
+    assert L.qoq_norm_quant_act(16, 100, 0, f(1e-6), FAKE, FAKE, None, FAKE, FAKE, None) == 2
+    assert L.qoq_norm_quant_act(16, 4096, 0, f(1e-6), FAKE, MIS, None, FAKE, FAKE, None) == 4
+    assert L.qoq_norm_quant_act(16, 4096, 1, f(1e-6), FAKE, FAKE, MIS, FAKE, FAKE, None) == 4
+
+
 def test_pack_validation():
     L = _lib()
     assert L.qoq_pack_weights(128, 256, 128, FAKE, None, FAKE, None) == 1

@@ -12,7 +12,7 @@ input generator) can be imported without loading the CUDA library.
 _EXPORTS = (
     "QOQ_ERRORS", "QoQError", "QoQLinear", "build", "library_path", "lib",
     "qoq_gemm_workspace_bytes", "qoq_last_device_status", "qoq_pack_weights",
-    "qoq_packed_weight_bytes", "qoq_quant_act", "qoq_set_debug", "qoq_status_str",
+    "qoq_norm_quant_act", "qoq_packed_weight_bytes", "qoq_quant_act", "qoq_set_debug", "qoq_status_str",
     "qoq_unpack_weights_debug", "qoq_version", "qoq_w4a8_gemm", "qoq_w4a8_gemm_no_alloc",
     "workspace_for",
 )

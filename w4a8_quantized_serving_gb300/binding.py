@@ -21,7 +21,7 @@ QOQ_ERRORS = {
 
 EXPORTED = (
     "qoq_status_str", "qoq_version", "qoq_packed_weight_bytes", "qoq_gemm_workspace_bytes",
-    "qoq_pack_weights", "qoq_quant_act", "qoq_w4a8_gemm", "qoq_unpack_weights_debug",
+    "qoq_pack_weights", "qoq_quant_act", "qoq_norm_quant_act", "qoq_w4a8_gemm", "qoq_unpack_weights_debug",
     "qoq_last_device_status", "qoq_set_debug", "qoq_w4a8_gemm_no_alloc",
 )
 
@@ -65,6 +65,8 @@ def lib() -> ctypes.CDLL:
             L.qoq_pack_weights.restype = i32
             L.qoq_quant_act.argtypes = [i32, i32, P, P, P, P]
             L.qoq_quant_act.restype = i32
+            L.qoq_norm_quant_act.argtypes = [i32, i32, i32, ctypes.c_float, P, P, P, P, P, P]
+            L.qoq_norm_quant_act.restype = i32
             L.qoq_w4a8_gemm.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P, sz, P]
             L.qoq_w4a8_gemm.restype = i32
             L.qoq_w4a8_gemm_no_alloc.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P]
@@ -160,6 +162,28 @@ def qoq_quant_act(X, Xq=None, sx=None, stream=None):
         sx = torch.empty(M, dtype=torch.float16, device=X.device)
     _check(lib().qoq_quant_act(M, K, _dev(X, torch.float16, "X"), _dev(Xq, torch.int8, "Xq", (M, K)),
                                _dev(sx, torch.float16, "sx", (M,)), _stream(stream)), "qoq_quant_act")
+    return Xq, sx
+
+
+NORM_KINDS = {"rms": 0, "layer": 1}
+
+
+def qoq_norm_quant_act(X, gamma, beta=None, kind: str = "rms", eps: float = 1e-6, Xq=None, sx=None, stream=None):
+    """RMSNorm (or LayerNorm with beta) fused with the per-token int8 quantizer:
+    X fp16 [M][K], gamma (and beta) fp16 [K] -> (Xq int8 [M][K], sx fp16 [M])."""
+    torch = _torch()
+    M, K = X.shape
+    if kind not in NORM_KINDS:
+        raise ValueError(f"kind must be one of {sorted(NORM_KINDS)}")
+    if Xq is None:
+        Xq = torch.empty((M, K), dtype=torch.int8, device=X.device)
+    if sx is None:
+        sx = torch.empty(M, dtype=torch.float16, device=X.device)
+    bptr = None if beta is None else _dev(beta, torch.float16, "beta", (K,))
+    _check(lib().qoq_norm_quant_act(M, K, NORM_KINDS[kind], float(eps), _dev(X, torch.float16, "X"),
+                                    _dev(gamma, torch.float16, "gamma", (K,)), bptr,
+                                    _dev(Xq, torch.int8, "Xq", (M, K)), _dev(sx, torch.float16, "sx", (M,)),
+                                    _stream(stream)), "qoq_norm_quant_act")
     return Xq, sx
 
 

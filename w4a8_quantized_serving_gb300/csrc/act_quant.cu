@@ -47,31 +47,10 @@ __device__ __forceinline__ uint32_t quant4(const __half* h, float sf, float rf) 
   return r;
 }
 
-template <int MAXV>
-__global__ void __launch_bounds__(1024) act_quant_kernel(const uint16_t* __restrict__ X,
-                                                         int8_t* __restrict__ Xq,
-                                                         uint16_t* __restrict__ sx, int M, int K,
-                                                         int T) {
-  grid_dep_launch_dependents();
-  grid_dep_wait();  // X may come from the preceding kernel; Xq and s_x may still be read by it
-  __shared__ float warp_max[32];
-  const int rows_per_cta = blockDim.x / T;
-  const int row = blockIdx.x * rows_per_cta + threadIdx.x / T;
-  const int t = threadIdx.x % T;
+// Max-abs of a token row held by T threads (thread t has `amax` of its
+// elements), combined over the row's warps through shared memory when T > 32.
+__device__ __forceinline__ float row_absmax(float amax, int T, float* warp_max) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nvec = K / 8;
-  const bool live = row < M;
-  const uint4* xr = reinterpret_cast<const uint4*>(X + (size_t)(live ? row : 0) * K);
-  uint4 v[MAXV];
-  float amax = 0.0f;
-#pragma unroll
-  for (int i = 0; i < MAXV; ++i) {
-    const int idx = t + i * T;
-    if (live && idx < nvec) {
-      v[i] = __ldcg(xr + idx);  // L2: X may have been written by the preceding kernel
-      amax = absmax8(v[i], amax);
-    }
-  }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
   if (T > 32) {  // combine the T/32 warps of this row
@@ -81,14 +60,20 @@ __global__ void __launch_bounds__(1024) act_quant_kernel(const uint16_t* __restr
     amax = 0.0f;
     for (int w = 0; w < T / 32; ++w) amax = fmaxf(amax, warp_max[w0 + w]);
   }
-  if (!live) return;
+  return amax;
+}
 
+// Symmetric int8 quantization of a token row whose values this thread holds
+// as fp16 vectors v[i] (vector t + i T of the row), given the row's max-abs:
+// s_x = fp16_rn(amax / 127) (IEEE fp32 divide), Xq = clamp(rint(x / s_x), +-127).
+template <int MAXV>
+__device__ __forceinline__ void quant_row(const uint4 (&v)[MAXV], float amax, int row, int t, int T, int nvec,
+                                          int K, int8_t* __restrict__ Xq, uint16_t* __restrict__ sx) {
   __half s = __float2half_rn(0.0f);
   if (amax > 0.0f) s = __float2half_rn(__fdiv_rn(amax, 127.0f));
   const float sf = __half2float(s);
   const float rf = sf != 0.0f ? __frcp_rn(sf) : 0.0f;
   if (t == 0) sx[row] = __half_as_ushort(s);
-
   uint2* qr = reinterpret_cast<uint2*>(Xq + (size_t)row * K);
 #pragma unroll
   for (int i = 0; i < MAXV; ++i) {
@@ -104,29 +89,234 @@ __global__ void __launch_bounds__(1024) act_quant_kernel(const uint16_t* __restr
   }
 }
 
+template <int MAXV>
+__global__ void __launch_bounds__(1024) act_quant_kernel(const uint16_t* __restrict__ X,
+                                                         int8_t* __restrict__ Xq,
+                                                         uint16_t* __restrict__ sx, int M, int K,
+                                                         int T) {
+  grid_dep_launch_dependents();
+  grid_dep_wait();  // X may come from the preceding kernel; Xq and s_x may still be read by it
+  __shared__ float warp_max[32];
+  const int rows_per_cta = blockDim.x / T;
+  const int row = blockIdx.x * rows_per_cta + threadIdx.x / T;
+  const int t = threadIdx.x % T;
+  const int nvec = K / 8;
+  const bool live = row < M;
+  const uint4* xr = reinterpret_cast<const uint4*>(X + (size_t)(live ? row : 0) * K);
+  uint4 v[MAXV];
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < MAXV; ++i) {
+    const int idx = t + i * T;
+    if (live && idx < nvec) {
+      v[i] = __ldcg(xr + idx);  // L2: X may have been written by the preceding kernel
+      amax = absmax8(v[i], amax);
+    }
+  }
+  amax = row_absmax(amax, T, warp_max);
+  if (!live) return;
+  quant_row<MAXV>(v, amax, row, t, T, nvec, K, Xq, sx);
+}
+
+// ------------------------------------------------------------------ norm --
+// QServe talk write-up, "Precision Data Flow and Activation Quantization
+// Fusion": the quantizer is fused into the preceding layer, such as
+// LayerNorm, so its output goes to 8 bits without an fp16 round trip
+// through HBM.  The row statistics are exact integers (x = a 2^-24 with a an
+// integer for every fp16 x): S1 = sum a, S2 = sum a^2 (128 bits), so they do
+// not depend on the reduction order.  Then, with every double operation
+// rounded to nearest:
+//   RMSNorm:   r = fl32(1 / sqrt(fl64(S2) 2^-48 / K + eps)),
+//              y = fp16_rn(fl32(fl32(x r) gamma));
+//   LayerNorm: mu = fl32(fl64(S1) 2^-24 / K),
+//              r = fl32(1 / sqrt(fl64(K S2 - S1^2) 2^-48 / K^2 + eps)),
+//              y = fp16_rn(fl32(fl32(fl32(fl32(x - mu) r) gamma) + beta));
+// and y is quantized per token as by act_quant_kernel.
+
+typedef unsigned __int128 u128;
+
+// a = x 2^-24 as an integer magnitude and sign (fp16 finite x).
+__device__ __forceinline__ uint64_t half_units(uint32_t h, bool& neg) {
+  const uint32_t e = (h >> 10) & 31, f = h & 1023;
+  neg = (h >> 15) & 1;
+  return e == 0 ? (uint64_t)f : (uint64_t)(f | 1024) << (e - 1);
+}
+
+// Round-to-nearest-even conversion of a 128-bit unsigned integer to double.
+__device__ __forceinline__ double u128_to_double_rn(u128 v) {
+  const uint64_t hi = (uint64_t)(v >> 64), lo = (uint64_t)v;
+  if (hi == 0) return __ull2double_rn(lo);
+  const int sh = 64 - __clzll((long long)hi);  // v >> sh has its top bit at 63
+  uint64_t top = (uint64_t)(v >> sh);
+  if ((v & (((u128)1 << sh) - 1)) != 0) top |= 1;  // sticky: bit 0 lies below the 53-bit rounding point
+  return __dmul_rn(__ull2double_rn(top), __hiloint2double((1023 + sh) << 20, 0));  // exact scaling by 2^sh
+}
+
+__device__ __forceinline__ u128 shfl_xor_u128(u128 v, int off) {
+  const uint64_t lo = __shfl_xor_sync(0xffffffffu, (unsigned long long)v, off);
+  const uint64_t hi = __shfl_xor_sync(0xffffffffu, (unsigned long long)(v >> 64), off);
+  return ((u128)hi << 64) | lo;
+}
+
+template <int MAXV, bool LN>
+__global__ void __launch_bounds__(1024) norm_quant_kernel(const uint16_t* __restrict__ X,
+                                                          const uint16_t* __restrict__ gamma,
+                                                          const uint16_t* __restrict__ beta,
+                                                          int8_t* __restrict__ Xq, uint16_t* __restrict__ sx,
+                                                          int M, int K, int T, float eps) {
+  grid_dep_launch_dependents();
+  grid_dep_wait();  // X may come from the preceding kernel; Xq and s_x may still be read by it
+  __shared__ float warp_max[32];
+  __shared__ unsigned long long warp_s2[32][2];
+  __shared__ long long warp_s1[32];
+  const int rows_per_cta = blockDim.x / T;
+  const int row = blockIdx.x * rows_per_cta + threadIdx.x / T;
+  const int t = threadIdx.x % T;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nvec = K / 8;
+  const bool live = row < M;
+  const uint4* xr = reinterpret_cast<const uint4*>(X + (size_t)(live ? row : 0) * K);
+  uint4 v[MAXV];
+  u128 s2 = 0;
+  long long s1 = 0;
+#pragma unroll
+  for (int i = 0; i < MAXV; ++i) {
+    const int idx = t + i * T;
+    if (live && idx < nvec) {
+      v[i] = __ldcg(xr + idx);  // L2: X may have been written by the preceding kernel
+      const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        bool neg;
+        const uint64_t a = half_units((w[j >> 1] >> (16 * (j & 1))) & 0xFFFFu, neg);
+        s2 += (u128)a * a;
+        if (LN) s1 += neg ? -(long long)a : (long long)a;
+      }
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    s2 += shfl_xor_u128(s2, off);
+    if (LN) s1 += __shfl_xor_sync(0xffffffffu, s1, off);
+  }
+  if (T > 32) {  // the row's warps, summed in the same order by every thread
+    if (lane == 0) {
+      warp_s2[warp][0] = (unsigned long long)s2;
+      warp_s2[warp][1] = (unsigned long long)(s2 >> 64);
+      warp_s1[warp] = s1;
+    }
+    __syncthreads();
+    const int w0 = (threadIdx.x / T) * (T / 32);
+    s2 = 0;
+    s1 = 0;
+    for (int w = 0; w < T / 32; ++w) {
+      s2 += ((u128)warp_s2[w0 + w][1] << 64) | warp_s2[w0 + w][0];
+      s1 += warp_s1[w0 + w];
+    }
+  }
+
+  double spread;  // mean square (RMSNorm) or variance (LayerNorm)
+  float mu = 0.0f;
+  if (LN) {
+    const u128 a1 = (u128)(unsigned long long)(s1 < 0 ? -s1 : s1);
+    const u128 var_num = (u128)(unsigned)K * s2 - a1 * a1;  // K S2 - S1^2 >= 0, exact
+    spread = __ddiv_rn(__dmul_rn(u128_to_double_rn(var_num), 0x1p-48), (double)K * (double)K);
+    mu = __double2float_rn(__ddiv_rn(__dmul_rn(__ll2double_rn(s1), 0x1p-24), (double)K));
+  } else {
+    spread = __ddiv_rn(__dmul_rn(u128_to_double_rn(s2), 0x1p-48), (double)K);
+  }
+  const float r = __double2float_rn(__ddiv_rn(1.0, __dsqrt_rn(__dadd_rn(spread, (double)eps))));
+
+  // y in place of x (fp16), and its max-abs
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < MAXV; ++i) {
+    const int idx = t + i * T;
+    if (live && idx < nvec) {
+      const uint4 gv = __ldcg(reinterpret_cast<const uint4*>(gamma) + idx);
+      uint4 bv = make_uint4(0, 0, 0, 0);
+      if (LN) bv = __ldcg(reinterpret_cast<const uint4*>(beta) + idx);
+      __half* h = reinterpret_cast<__half*>(&v[i]);
+      const __half* gh = reinterpret_cast<const __half*>(&gv);
+      const __half* bh = reinterpret_cast<const __half*>(&bv);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        float y = __half2float(h[j]);
+        if (LN) y = __fsub_rn(y, mu);
+        y = __fmul_rn(__fmul_rn(y, r), __half2float(gh[j]));
+        if (LN) y = __fadd_rn(y, __half2float(bh[j]));
+        h[j] = __float2half_rn(y);
+        amax = fmaxf(amax, fabsf(__half2float(h[j])));
+      }
+    }
+  }
+  amax = row_absmax(amax, T, warp_max);
+  if (!live) return;
+  quant_row<MAXV>(v, amax, row, t, T, nvec, K, Xq, sx);
+}
+
+}  // namespace
+
+namespace {
+
+// Threads per token row: a power of two, ~4 vectors of 8 values each (latency),
+// at most 16 (T = 1024 for K up to 131072).
+struct RowLayout {
+  int T, threads, grid, vpt;
+};
+
+RowLayout row_layout(int M, int K) {
+  const int nvec = K / 8;
+  RowLayout L;
+  L.T = 32;
+  while (L.T * 4 < nvec && L.T < 1024) L.T *= 2;
+  L.threads = L.T < 128 ? 128 : L.T;
+  const int rows_per_cta = L.threads / L.T;
+  L.grid = (M + rows_per_cta - 1) / rows_per_cta;
+  L.vpt = (nvec + L.T - 1) / L.T;  // <= 4 unless T = 1024; <= 16 for K <= 131072
+  return L;
+}
+
+cudaLaunchConfig_t row_config(const RowLayout& L, cudaStream_t s, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(L.grid);
+  cfg.blockDim = dim3(L.threads);
+  cfg.stream = s;
+  attr[0] = pdl_attr();
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+template <bool LN>
+cudaError_t launch_norm_kind(const RowLayout& L, cudaLaunchConfig_t& cfg, int M, int K, float eps, const uint16_t* X,
+                             const uint16_t* gamma, const uint16_t* beta, int8_t* Xq, uint16_t* sx) {
+  if (L.vpt <= 4) return cudaLaunchKernelEx(&cfg, norm_quant_kernel<4, LN>, X, gamma, beta, Xq, sx, M, K, L.T, eps);
+  if (L.vpt <= 8) return cudaLaunchKernelEx(&cfg, norm_quant_kernel<8, LN>, X, gamma, beta, Xq, sx, M, K, L.T, eps);
+  if (L.vpt <= 16) return cudaLaunchKernelEx(&cfg, norm_quant_kernel<16, LN>, X, gamma, beta, Xq, sx, M, K, L.T, eps);
+  return cudaErrorInvalidValue;
+}
+
 }  // namespace
 
 cudaError_t launch_act_quant(int M, int K, const uint16_t* X, int8_t* Xq, uint16_t* sx,
                              cudaStream_t s) {
-  const int nvec = K / 8;
-  // threads per row: a power of two, ~4 vectors each (latency), at most 16
-  int T = 32;
-  while (T * 4 < nvec && T < 1024) T *= 2;
-  const int threads = T < 128 ? 128 : T;
-  const int rows_per_cta = threads / T;
-  const int grid = (M + rows_per_cta - 1) / rows_per_cta;
-  const int vpt = (nvec + T - 1) / T;  // <= 4 unless T = 1024; <= 16 for K <= 131072
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(threads);
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1] = {pdl_attr()};
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (vpt <= 4) return cudaLaunchKernelEx(&cfg, act_quant_kernel<4>, X, Xq, sx, M, K, T);
-  if (vpt <= 8) return cudaLaunchKernelEx(&cfg, act_quant_kernel<8>, X, Xq, sx, M, K, T);
-  if (vpt <= 16) return cudaLaunchKernelEx(&cfg, act_quant_kernel<16>, X, Xq, sx, M, K, T);
+  const RowLayout L = row_layout(M, K);
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = row_config(L, s, attr);
+  if (L.vpt <= 4) return cudaLaunchKernelEx(&cfg, act_quant_kernel<4>, X, Xq, sx, M, K, L.T);
+  if (L.vpt <= 8) return cudaLaunchKernelEx(&cfg, act_quant_kernel<8>, X, Xq, sx, M, K, L.T);
+  if (L.vpt <= 16) return cudaLaunchKernelEx(&cfg, act_quant_kernel<16>, X, Xq, sx, M, K, L.T);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_norm_quant(int M, int K, int kind, float eps, const uint16_t* X, const uint16_t* gamma,
+                              const uint16_t* beta, int8_t* Xq, uint16_t* sx, cudaStream_t s) {
+  const RowLayout L = row_layout(M, K);
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = row_config(L, s, attr);
+  return kind == 1 ? launch_norm_kind<true>(L, cfg, M, K, eps, X, gamma, beta, Xq, sx)
+                   : launch_norm_kind<false>(L, cfg, M, K, eps, X, gamma, beta, Xq, sx);
 }
 
 }  // namespace qoq

@@ -120,6 +120,22 @@ qoq_status qoq_quant_act(int M, int K, const uint16_t* X_f16, int8_t* Xq, uint16
   return from_cuda(qoq::launch_act_quant(M, K, X_f16, Xq, sx_f16, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+qoq_status qoq_norm_quant_act(int M, int K, int kind, float eps, const uint16_t* X_f16,
+                              const uint16_t* gamma_f16, const uint16_t* beta_f16, int8_t* Xq,
+                              uint16_t* sx_f16, qoq_stream_t stream) {
+  if (!X_f16 || !gamma_f16 || !Xq || !sx_f16 || (kind == QOQ_NORM_LAYER && !beta_f16)) return QOQ_ERR_NULL;
+  if (kind != QOQ_NORM_RMS && kind != QOQ_NORM_LAYER) return QOQ_ERR_UNSUPPORTED;
+  if (!(eps > 0.0f) || !(eps <= 3.4e38f)) return QOQ_ERR_UNSUPPORTED;  // positive and finite
+  if (!shape_ok_mk(M, K)) return QOQ_ERR_SHAPE;
+  if (!aligned16(X_f16) || !aligned16(gamma_f16) || (kind == QOQ_NORM_LAYER && !aligned16(beta_f16)) ||
+      !aligned16(Xq) || !aligned16(sx_f16))
+    return QOQ_ERR_MISALIGNED;
+  qoq_status st = device_info(nullptr);
+  if (st != QOQ_OK) return st;
+  return from_cuda(qoq::launch_norm_quant(M, K, kind, eps, X_f16, gamma_f16, beta_f16, Xq, sx_f16,
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
 qoq_status qoq_w4a8_gemm(int M, int N, int K, int g, const int8_t* Xq, const uint16_t* sx_f16,
                          const uint8_t* packed, const uint16_t* s1_f16, uint16_t* Y_f16,
                          int32_t* acc_debug, void* workspace, size_t ws_bytes,

@@ -153,6 +153,8 @@ inline cudaLaunchAttribute pdl_attr() {
 // ---------------------------------------------------------------- launchers --
 cudaError_t launch_act_quant(int M, int K, const uint16_t* X, int8_t* Xq, uint16_t* sx,
                              cudaStream_t s);
+cudaError_t launch_norm_quant(int M, int K, int kind, float eps, const uint16_t* X, const uint16_t* gamma,
+                              const uint16_t* beta, int8_t* Xq, uint16_t* sx, cudaStream_t s);
 cudaError_t launch_pack(int N, int K, int g, const uint16_t* W, uint8_t* packed, uint16_t* s1,
                         cudaStream_t s);
 cudaError_t launch_unpack(int N, int K, int g, const uint8_t* packed, uint8_t* q4, uint8_t* s2, uint8_t* z,
