@@ -276,9 +276,20 @@ def run_ours(args, c: dict) -> None:
             ws=torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)))
     del packed, s1
 
+    # the step's activation quantizer: the per-token quantizer alone, or fused
+    # with the preceding RMSNorm (gamma drawn once, eps 1e-6)
+    norm_step = args.step == "norm"
+    gamma = torch.from_numpy(np.random.default_rng(c["seed"]).uniform(0.5, 1.5, K).astype(np.float16)).to(dev)
+
+    def quantize(s):
+        if norm_step:
+            q.qoq_norm_quant_act(s["X"], gamma, kind="rms", eps=1e-6, Xq=s["Xq"], sx=s["sx"])
+        else:
+            q.qoq_quant_act(s["X"], Xq=s["Xq"], sx=s["sx"])
+
     def step(i: int):
         s = sets[i % nsets]
-        q.qoq_quant_act(s["X"], Xq=s["Xq"], sx=s["sx"])
+        quantize(s)
         q.qoq_w4a8_gemm(s["Xq"], s["sx"], s["packed"], s["s1"], N, g=G, Y=s["Y"], workspace=s["ws"])
 
     for i in range(max(3, args.warmup)):
@@ -359,7 +370,7 @@ def run_ours(args, c: dict) -> None:
     def e2e_step(i: int):
         s = sets[i % nsets]
         s["X"].copy_(Xh, non_blocking=True)
-        q.qoq_quant_act(s["X"], Xq=s["Xq"], sx=s["sx"])
+        quantize(s)
         q.qoq_w4a8_gemm(s["Xq"], s["sx"], s["packed"], s["s1"], N, g=G, Y=s["Y"], workspace=s["ws"])
         Yh[i % 2].copy_(s["Y"], non_blocking=True)
 
@@ -419,7 +430,8 @@ def run_ours(args, c: dict) -> None:
             "parallelism": f"replicas{world}" if world > 1 else "single",
             "l2_policy": f"rotating pool of {nsets} buffer sets, {nsets * set_bytes / 1e6:.0f} MB "
                          f"(>= 3x L2 {l2 / 1e6:.0f} MB)",
-            "step": "qoq_quant_act + qoq_w4a8_gemm",
+            "step": ("qoq_norm_quant_act (RMSNorm) + qoq_w4a8_gemm" if norm_step
+                     else "qoq_quant_act + qoq_w4a8_gemm"),
             "timing": "CUDA graph of K steps" if use_graph else "direct launches",
             "mma": "tcgen05 kind::f16, exact integer operands, fp32 TMEM folded to int32"}),
         "hbm_gb_per_s_step": world * nbytes["step"] / (ms_per_step * 1e-3) / 1e9,
@@ -453,6 +465,8 @@ def main() -> None:
     ap.add_argument("--config", type=int, default=1, help="workload index 0..4 (default 1)")
     ap.add_argument("--g", type=int, default=128,
                     help="level-2 group size: 32, 64 or a multiple of 128 dividing K (default 128, the pages' g128)")
+    ap.add_argument("--step", choices=["quant", "norm"], default="quant",
+                    help="activation quantizer of the step: qoq_quant_act (default) or qoq_norm_quant_act (RMSNorm fused)")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle CPU timing")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="time direct launches instead of a CUDA graph")

@@ -152,12 +152,13 @@ typedef enum { QOQ_NORM_RMS = 0, QOQ_NORM_LAYER = 1 } qoq_norm_kind;
  * fused into the preceding layer, such as LayerNorm, whose output is
  * quantized to 8 bits directly, without writing the normalized fp16 rows).
  * Per token row x (K fp16 values), with exact row statistics
- * S1 = sum_k x_k, S2 = sum_k x_k^2 (integers in units of 2^-24 and 2^-48) and
- * every double operation rounded to nearest:
- *   QOQ_NORM_RMS:   r = fl32(1 / sqrt(fl64(S2) / K + eps)),
+ * S1 = sum_k x_k, S2 = sum_k x_k^2 (integers in units of 2^-24 and 2^-48),
+ * each rounded once to fp32 (fl32), and every fp32 operation below rounded
+ * to nearest:
+ *   QOQ_NORM_RMS:   r = 1 / sqrt(fl32(S2) / K + eps),
  *                   y_k = fp16_rn(fl32(fl32(x_k * r) * gamma_k));
- *   QOQ_NORM_LAYER: mu = fl32(fl64(S1) / K),
- *                   r = fl32(1 / sqrt(fl64(K S2 - S1^2) / K^2 + eps)),
+ *   QOQ_NORM_LAYER: mu = fl32(S1) / K,
+ *                   r = 1 / sqrt(fl32(K S2 - S1^2) / K^2 + eps),
  *                   y_k = fp16_rn(fl32(fl32(fl32(fl32(x_k - mu) * r) * gamma_k) + beta_k));
  * then s_x and Xq of the rows y exactly as qoq_quant_act computes them.
  * In:  X_f16 [M][K] fp16 bits (finite values), gamma_f16 [K], beta_f16 [K]

@@ -306,11 +306,12 @@ int qoq_oracle_gemm_entries(int count, const int32_t* m_idx, const int32_t* n_id
  *  R6 the row statistics are exact: S1 = sum_k x_k and S2 = sum_k x_k^2 as
  *     integers in units of 2^-24 and 2^-48 (every fp16 x is an integer
  *     multiple of 2^-24), so they do not depend on summation order;
- *  R7 RMSNorm (kind 0): r = fl32(1 / sqrt(fl64(S2) / K + eps)), each double
- *     operation rounded to nearest (fl64(S2): the exact sum rounded to double),
+ *  R7 the rest in fp32, each operation rounded to nearest (fl32(S): the
+ *     exact sum rounded once to fp32):
+ *     RMSNorm (kind 0): ms = fl32(S2) / K, r = 1 / sqrt(ms + eps),
  *     y_k = fp16_rn(fl32(fl32(x_k * r) * gamma_k));
- *     LayerNorm (kind 1): mu = fl32(fl64(S1) / K),
- *     var = fl64(K S2 - S1^2) / K^2, r = fl32(1 / sqrt(var + eps)),
+ *     LayerNorm (kind 1): mu = fl32(S1) / K, var = fl32(K S2 - S1^2) / K^2,
+ *     r = 1 / sqrt(var + eps),
  *     y_k = fp16_rn(fl32(fl32(fl32(fl32(x_k - mu) * r) * gamma_k) + beta_k));
  *     eps > 0;
  *  then y is quantized per token exactly as qoq_oracle_act_quant does (R3).
@@ -339,21 +340,22 @@ int qoq_oracle_norm_quant_act(int M, int K, int kind, float eps, const uint16_t*
       stats[4 * m + 2] = (int64_t)(uint64_t)(s2 >> 64);
       stats[4 * m + 3] = 0;
     }
-    volatile double spread; /* mean square (kind 0) or variance (kind 1) */
-    float mu = 0.0f;
+    volatile float spread; /* mean square (kind 0) or variance (kind 1) */
+    volatile float mu = 0.0f;
     if (kind == 0) {
-      spread = ((double)s2 * 0x1p-48) / (double)K;
+      volatile float s2f = (float)s2 * 0x1p-48f; /* one rounding, then an exact scaling */
+      spread = s2f / (float)K;
     } else {
       unsigned __int128 a1 = (unsigned __int128)(uint64_t)(s1 < 0 ? -s1 : s1);
       unsigned __int128 v = (unsigned __int128)K * s2 - a1 * a1; /* >= 0, exact */
-      spread = ((double)v * 0x1p-48) / ((double)K * (double)K);
-      volatile double mu_d = ((double)s1 * 0x1p-24) / (double)K;
-      mu = (float)mu_d;
+      volatile float vf = (float)v * 0x1p-48f;
+      spread = vf / ((float)K * (float)K); /* K^2 is exact in fp32 for K = 128 j, j <= 1024 */
+      volatile float s1f = (float)s1 * 0x1p-24f;
+      mu = s1f / (float)K;
     }
-    volatile double den = spread + (double)eps;
-    volatile double sq = sqrt(den);
-    volatile double rd = 1.0 / sq;
-    const float r = (float)rd;
+    volatile float den = spread + eps;
+    volatile float sq = sqrtf(den);
+    const float r = 1.0f / sq;
     if (rmu) {
       rmu[2 * m] = r;
       rmu[2 * m + 1] = mu;

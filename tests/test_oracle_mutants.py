@@ -31,11 +31,10 @@ MUTANTS = {
     "act_scale_127_to_119": ("symmetric_row(K, X + (size_t)m * K, 127, &sx[m], Xq + (size_t)m * K);",
                              "symmetric_row(K, X + (size_t)m * K, 119, &sx[m], Xq + (size_t)m * K);"),
     "norm_square_overflow": ("s2 += (unsigned __int128)mag * mag;", "s2 += (unsigned __int128)(mag * mag);"),
-    "norm_missing_eps": ("volatile double den = spread + (double)eps;", "volatile double den = spread;"),
+    "norm_missing_eps": ("volatile float den = spread + eps;", "volatile float den = spread;"),
     "layer_no_centering": ("volatile float t = kind == 1 ? x - mu : x;", "volatile float t = x;"),
     "layer_variance_sign": ("(unsigned __int128)K * s2 - a1 * a1;", "(unsigned __int128)K * s2 + a1 * a1;"),
-    "rms_mean_divisor": ("spread = ((double)s2 * 0x1p-48) / (double)K;",
-                         "spread = ((double)s2 * 0x1p-48) / (double)(K + 1);"),
+    "rms_mean_divisor": ("spread = s2f / (float)K;", "spread = s2f / (float)(K + 1);"),
 }
 
 

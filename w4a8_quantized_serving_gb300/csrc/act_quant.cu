@@ -124,32 +124,35 @@ __global__ void __launch_bounds__(1024) act_quant_kernel(const uint16_t* __restr
 // LayerNorm, so its output goes to 8 bits without an fp16 round trip
 // through HBM.  The row statistics are exact integers (x = a 2^-24 with a an
 // integer for every fp16 x): S1 = sum a, S2 = sum a^2 (128 bits), so they do
-// not depend on the reduction order.  Then, with every double operation
-// rounded to nearest:
-//   RMSNorm:   r = fl32(1 / sqrt(fl64(S2) 2^-48 / K + eps)),
+// not depend on the reduction order.  Then, in fp32 with every operation
+// rounded to nearest (fl32(S): the exact integer rounded once):
+//   RMSNorm:   r = 1 / sqrt(fl32(S2) 2^-48 / K + eps),
 //              y = fp16_rn(fl32(fl32(x r) gamma));
-//   LayerNorm: mu = fl32(fl64(S1) 2^-24 / K),
-//              r = fl32(1 / sqrt(fl64(K S2 - S1^2) 2^-48 / K^2 + eps)),
+//   LayerNorm: mu = fl32(S1) 2^-24 / K,
+//              r = 1 / sqrt(fl32(K S2 - S1^2) 2^-48 / K^2 + eps),
 //              y = fp16_rn(fl32(fl32(fl32(fl32(x - mu) r) gamma) + beta));
-// and y is quantized per token as by act_quant_kernel.
+// and y is quantized per token as by act_quant_kernel.  Every thread of a row
+// computes r and mu from the same sums, so no broadcast is needed.
 
 typedef unsigned __int128 u128;
 
-// a = x 2^-24 as an integer magnitude and sign (fp16 finite x).
-__device__ __forceinline__ uint64_t half_units(uint32_t h, bool& neg) {
+// x = +-m 2^(s - 24) for a finite fp16 x: mantissa m < 2^11 and shift s <= 29,
+// so a = x 2^24 = +-m 2^s and a^2 = m^2 2^(2s) < 2^80.
+__device__ __forceinline__ uint32_t half_mantissa(uint32_t h, uint32_t& s, bool& neg) {
   const uint32_t e = (h >> 10) & 31, f = h & 1023;
   neg = (h >> 15) & 1;
-  return e == 0 ? (uint64_t)f : (uint64_t)(f | 1024) << (e - 1);
+  s = e == 0 ? 0 : e - 1;
+  return e == 0 ? f : (f | 1024);
 }
 
-// Round-to-nearest-even conversion of a 128-bit unsigned integer to double.
-__device__ __forceinline__ double u128_to_double_rn(u128 v) {
+// Round-to-nearest-even conversion of a 128-bit unsigned integer (< 2^127) to fp32.
+__device__ __forceinline__ float u128_to_float_rn(u128 v) {
   const uint64_t hi = (uint64_t)(v >> 64), lo = (uint64_t)v;
-  if (hi == 0) return __ull2double_rn(lo);
+  if (hi == 0) return __ull2float_rn(lo);
   const int sh = 64 - __clzll((long long)hi);  // v >> sh has its top bit at 63
   uint64_t top = (uint64_t)(v >> sh);
-  if ((v & (((u128)1 << sh) - 1)) != 0) top |= 1;  // sticky: bit 0 lies below the 53-bit rounding point
-  return __dmul_rn(__ull2double_rn(top), __hiloint2double((1023 + sh) << 20, 0));  // exact scaling by 2^sh
+  if ((v & (((u128)1 << sh) - 1)) != 0) top |= 1;  // sticky: bit 0 lies below the 24-bit rounding point
+  return __fmul_rn(__ull2float_rn(top), __int_as_float((127 + sh) << 23));  // exact scaling by 2^sh
 }
 
 __device__ __forceinline__ u128 shfl_xor_u128(u128 v, int off) {
@@ -177,7 +180,10 @@ __global__ void __launch_bounds__(1024) norm_quant_kernel(const uint16_t* __rest
   const bool live = row < M;
   const uint4* xr = reinterpret_cast<const uint4*>(X + (size_t)(live ? row : 0) * K);
   uint4 v[MAXV];
-  u128 s2 = 0;
+  // this thread's part of S2 as lo + hi 2^32: a^2 = m^2 2^(2s) goes to lo when
+  // 2s < 32 (< 2^52) and to hi as m^2 2^(2s-32) otherwise (< 2^48); at most
+  // 128 terms each, so neither 64-bit sum can wrap
+  uint64_t s2lo = 0, s2hi = 0;
   long long s1 = 0;
 #pragma unroll
   for (int i = 0; i < MAXV; ++i) {
@@ -188,12 +194,21 @@ __global__ void __launch_bounds__(1024) norm_quant_kernel(const uint16_t* __rest
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         bool neg;
-        const uint64_t a = half_units((w[j >> 1] >> (16 * (j & 1))) & 0xFFFFu, neg);
-        s2 += (u128)a * a;
-        if (LN) s1 += neg ? -(long long)a : (long long)a;
+        uint32_t sh;
+        const uint32_t mnt = half_mantissa((w[j >> 1] >> (16 * (j & 1))) & 0xFFFFu, sh, neg);
+        const uint64_t sq = (uint64_t)(mnt * mnt);
+        if (sh >= 16)
+          s2hi += sq << (2 * sh - 32);
+        else
+          s2lo += sq << (2 * sh);
+        if (LN) {
+          const long long a = (long long)((uint64_t)mnt << sh);
+          s1 += neg ? -a : a;
+        }
       }
     }
   }
+  u128 s2 = ((u128)s2hi << 32) + s2lo;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
     s2 += shfl_xor_u128(s2, off);
@@ -215,17 +230,16 @@ __global__ void __launch_bounds__(1024) norm_quant_kernel(const uint16_t* __rest
     }
   }
 
-  double spread;  // mean square (RMSNorm) or variance (LayerNorm)
-  float mu = 0.0f;
+  float spread, mu = 0.0f;  // mean square (RMSNorm) or variance (LayerNorm)
   if (LN) {
     const u128 a1 = (u128)(unsigned long long)(s1 < 0 ? -s1 : s1);
     const u128 var_num = (u128)(unsigned)K * s2 - a1 * a1;  // K S2 - S1^2 >= 0, exact
-    spread = __ddiv_rn(__dmul_rn(u128_to_double_rn(var_num), 0x1p-48), (double)K * (double)K);
-    mu = __double2float_rn(__ddiv_rn(__dmul_rn(__ll2double_rn(s1), 0x1p-24), (double)K));
+    spread = __fdiv_rn(__fmul_rn(u128_to_float_rn(var_num), 0x1p-48f), (float)K * (float)K);
+    mu = __fdiv_rn(__fmul_rn(__ll2float_rn(s1), 0x1p-24f), (float)K);
   } else {
-    spread = __ddiv_rn(__dmul_rn(u128_to_double_rn(s2), 0x1p-48), (double)K);
+    spread = __fdiv_rn(__fmul_rn(u128_to_float_rn(s2), 0x1p-48f), (float)K);
   }
-  const float r = __double2float_rn(__ddiv_rn(1.0, __dsqrt_rn(__dadd_rn(spread, (double)eps))));
+  const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(spread, eps)));
 
   // y in place of x (fp16), and its max-abs
   float amax = 0.0f;
