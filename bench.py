@@ -305,8 +305,11 @@ def run_ours(args, c: dict) -> None:
         s = sets[i % nsets]
         q.qoq_w4a8_gemm(s["Xq"], s["sx"], s["packed"], s["s1"], N, g=G, Y=s["Y"], workspace=s["ws"])
 
+    def act_only(i: int):
+        quantize(sets[i % nsets])
+
     use_graph = not args.no_graph
-    g_step = g_gemm = None
+    g_step = g_gemm = g_act = None
     if use_graph:
         try:
             g_step = torch.cuda.CUDAGraph()
@@ -317,13 +320,18 @@ def run_ours(args, c: dict) -> None:
             with torch.cuda.graph(g_gemm):
                 for i in range(args.steps):
                     gemm_only(i)
+            g_act = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_act):
+                for i in range(args.steps):
+                    act_only(i)
             g_step.replay()  # untimed warm replay
             g_gemm.replay()
+            g_act.replay()
             torch.cuda.synchronize()
         except Exception as exc:  # capture unsupported: time direct launches instead
             print(f"graph capture failed ({exc}); timing direct launches", file=sys.stderr)
             use_graph = False
-            g_step = g_gemm = None
+            g_step = g_gemm = g_act = None
             torch.cuda.synchronize()
 
     # ---- timed region: K steps
@@ -356,6 +364,17 @@ def run_ours(args, c: dict) -> None:
     clocks = sampler.stop()
     ms_total = t0.elapsed_time(t1)
     gemm_ms = g0.elapsed_time(g1) / args.steps
+    # the step's activation quantizer alone (same pool)
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    if use_graph:
+        g_act.replay()
+    else:
+        for i in range(args.steps):
+            act_only(i)
+    a1.record(stream)
+    torch.cuda.synchronize()
+    act_ms = a0.elapsed_time(a1) / args.steps
     for s in sets:
         st = q.qoq_last_device_status(s["ws"])
         if st != 0:
@@ -389,9 +408,9 @@ def run_ours(args, c: dict) -> None:
 
     ms_per_step = ms_total / args.steps
     if dist:
-        tt = torch.tensor([ms_per_step, e2e_ms, gemm_ms], device=dev)
+        tt = torch.tensor([ms_per_step, e2e_ms, gemm_ms, act_ms], device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_per_step, e2e_ms, gemm_ms = (float(v) for v in tt.tolist())
+        ms_per_step, e2e_ms, gemm_ms, act_ms = (float(v) for v in tt.tolist())
 
     ops = 2.0 * M * N * K
     nbytes = algorithmic_bytes(M, N, K, G)
@@ -420,6 +439,14 @@ def run_ours(args, c: dict) -> None:
     roof["ms_per_launch"] = gemm_ms
     roof["gb_per_s_algorithmic"] = nbytes["gemm"] / (gemm_ms * 1e-3) / 1e9
     roof["tops_effective"] = ops / (gemm_ms * 1e-3) / 1e12
+    # the step's activation quantizer alone: 2 bytes read and 1 written per
+    # element, 2 per token for s_x, plus gamma (2K) when the norm is fused
+    act_bytes = nbytes["act"] + (2 * K if norm_step else 0)
+    act_gbs = act_bytes / (act_ms * 1e-3) / 1e9
+    act_roof = {"kernel": "qoq_norm_quant_act (RMSNorm)" if norm_step else "qoq_quant_act",
+                "bound": "hbm", "achieved": act_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": act_gbs / peaks["hbm_gbs"], "algorithmic_bytes_per_launch": act_bytes,
+                "ms_per_launch": act_ms, "timing": "alone, same pool, " + ("CUDA graph" if use_graph else "direct")}
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -436,6 +463,7 @@ def run_ours(args, c: dict) -> None:
             "mma": "tcgen05 kind::f16, exact integer operands, fp32 TMEM folded to int32"}),
         "hbm_gb_per_s_step": world * nbytes["step"] / (ms_per_step * 1e-3) / 1e9,
         "roofline": roof,
+        "act_roofline": act_roof,
         "e2e": {"value": world * ops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                 "h2d_bytes_per_step": 2 * M * K, "d2h_bytes_per_step": 2 * M * N,
                 "ms_per_step": e2e_ms},

@@ -161,8 +161,12 @@ __device__ __forceinline__ u128 shfl_xor_u128(u128 v, int off) {
   return ((u128)hi << 64) | lo;
 }
 
+// At most 32 registers per thread for rows of up to 32768 channels (MAXV 4),
+// like act_quant_kernel: a 128-thread CTA then fits, on every SM
+// sub-partition, beside a decode GEMM CTA, so it becomes resident while that
+// GEMM runs and starts the moment it completes.
 template <int MAXV, bool LN>
-__global__ void __launch_bounds__(1024) norm_quant_kernel(const uint16_t* __restrict__ X,
+__global__ void __launch_bounds__(1024, MAXV == 4 ? 2 : 1) norm_quant_kernel(const uint16_t* __restrict__ X,
                                                           const uint16_t* __restrict__ gamma,
                                                           const uint16_t* __restrict__ beta,
                                                           int8_t* __restrict__ Xq, uint16_t* __restrict__ sx,
