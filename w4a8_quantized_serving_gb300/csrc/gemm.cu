@@ -196,8 +196,11 @@ __global__ void __launch_bounds__(BulkCfg<GPT>::THREADS, 1) gemm_bulk_kernel(con
         if ((int)(gi % C::NSLOT) != slot) continue;
         const int s = gi % C::STAGES;
         const int a = gi % C::NABUF;
-        if (!wait_seq(seq + 4 * s, gi + 1, p) || !wait_bar(bar_full + 8 * s, (gi / C::STAGES) & 1, p) ||
-            !wait_bar(bar_aempty + 8 * a, ((gi / C::NABUF) & 1) ^ 1, p)) {
+        // every lane waits, then the warp votes: it reaches the tensor memory
+        // stores below converged (see conv_wait_bar)
+        const bool got = wait_seq(seq + 4 * s, gi + 1, p) && wait_bar(bar_full + 8 * s, (gi / C::STAGES) & 1, p) &&
+                         wait_bar(bar_aempty + 8 * a, ((gi / C::NABUF) & 1) ^ 1, p);
+        if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
         }

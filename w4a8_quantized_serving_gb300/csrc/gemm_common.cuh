@@ -243,6 +243,17 @@ __device__ __forceinline__ bool warp_wait_bar(uint32_t bar, uint32_t parity, con
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
+// Every lane waits, then the warp votes.  Lanes that spin on their own leave
+// the loop at different times, and nothing else guarantees that the warp is
+// converged again when it reaches a warp-collective instruction (tcgen05.ld /
+// st .sync.aligned, elect.sync); so a wait followed by one, with no
+// __syncwarp in between, takes this form or warp_wait_bar's.  The vote
+// returns the warp converged, with one outcome for all lanes.
+__device__ __forceinline__ bool conv_wait_bar(uint32_t bar, uint32_t parity, const GemmParams& p) {
+  const bool ok = wait_bar(bar, parity, p);
+  return __all_sync(0xffffffffu, ok);
+}
+
 template <int NTHREADS>
 __device__ __forceinline__ void named_bar_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(NTHREADS) : "memory");
@@ -261,6 +272,46 @@ __device__ __forceinline__ void write_tile_out(const GemmParams& p, const int32_
     if (m < p.M) {
       const float sxf = __half2float(__ushort_as_half(p.sx[m]));
       const float y = (float)run[i] * (sxf * s1f);
+      p.Y[(size_t)m * p.N + n] = __half_as_ushort(__float2half_rn(y));
+      if (p.acc_debug) p.acc_debug[(size_t)m * p.N + n] = run[i];
+    }
+  }
+}
+
+// The epilogue scales of a row: s1[n] and s_x of tokens m0 .. m0 + COLS - 1
+// (0 past M), loaded into registers ahead of time, two fp16 per register.
+template <int COLS>
+struct RowScales {
+  uint16_t s1;
+  uint32_t sx2[COLS / 2];
+};
+
+// m0 is a multiple of COLS and s_x is 16-byte aligned, so a pair of s_x
+// values is one aligned 4-byte load; a pair that straddles M loads its first.
+template <int COLS>
+__device__ __forceinline__ RowScales<COLS> load_row_scales(const GemmParams& p, int m0, int n) {
+  static_assert(COLS % 2 == 0, "s_x pairs");
+  RowScales<COLS> r;
+  r.s1 = p.s1[n];
+#pragma unroll
+  for (int i = 0; i < COLS / 2; ++i) {
+    const int m = m0 + 2 * i;
+    r.sx2[i] = m + 1 < p.M ? *reinterpret_cast<const uint32_t*>(p.sx + m) : m < p.M ? (uint32_t)p.sx[m] : 0u;
+  }
+  return r;
+}
+
+// write_tile_out with the scales already loaded.
+template <int COLS>
+__device__ __forceinline__ void write_tile_out(const GemmParams& p, const int32_t (&run)[COLS], int m0, int n,
+                                               const RowScales<COLS>& sc) {
+  const float s1f = __half2float(__ushort_as_half(sc.s1));
+#pragma unroll
+  for (int i = 0; i < COLS; ++i) {
+    const int m = m0 + i;
+    if (m < p.M) {
+      const uint16_t sx = (uint16_t)(sc.sx2[i / 2] >> (16 * (i & 1)));
+      const float y = (float)run[i] * (__half2float(__ushort_as_half(sx)) * s1f);
       p.Y[(size_t)m * p.N + n] = __half_as_ushort(__float2half_rn(y));
       if (p.acc_debug) p.acc_debug[(size_t)m * p.N + n] = run[i];
     }
@@ -409,7 +460,7 @@ __device__ __forceinline__ void epilogue_role(const GemmParams& p, uint32_t tmem
     for (int i = 0; i < TOK; ++i) run[i] = 0;
     for (int c0 = u.g0; c0 < u.g1; c0 += kFoldGroups, ++chunk) {
       const int b = chunk % NACC;
-      if (ok) ok = wait_bar(bar_accfull + 8 * b, (chunk / NACC) & 1, p);
+      if (ok) ok = conv_wait_bar(bar_accfull + 8 * b, (chunk / NACC) & 1, p);
       if (e == 0 && lane == 0) QOQ_TRACE_AT(p, 512 + (int)chunk, 0);
       if (ok) {
         tc_fence_after();

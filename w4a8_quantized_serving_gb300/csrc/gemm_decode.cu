@@ -319,6 +319,7 @@ __global__ void __launch_bounds__(DecCfg<BN, GPT>::THREADS, 1) gemm_decode_kerne
           slot_bar_sync(slot);  // the slot's 4 quadrants and its B tile are written
           if (quad == 0 && lane == 0) QOQ_TRACE_AT(p, 896 + (int)gi, 0);
           if (ok && issuer) {
+            __syncwarp();  // elect.sync wants the whole warp, converged
             tc_fence_after();
             if (elect_one()) {
 #pragma unroll
@@ -363,7 +364,7 @@ __global__ void __launch_bounds__(DecCfg<BN, GPT>::THREADS, 1) gemm_decode_kerne
         const int len = min(C::CH, u.g1 - c0);
         const uint32_t gc0 = gi_u + (uint32_t)(c0 - u.g0);
         const int b = ch % C::NACC;
-        if (ok) ok = wait_bar(bar_accfull + 8 * b, (ch / C::NACC) & 1, p);
+        if (ok) ok = conv_wait_bar(bar_accfull + 8 * b, (ch / C::NACC) & 1, p);
         if (e == 0 && lane == 0) QOQ_TRACE_AT(p, 512 + (int)ch, 0);
         if (ok) {
           tc_fence_after();
@@ -400,10 +401,23 @@ __global__ void __launch_bounds__(DecCfg<BN, GPT>::THREADS, 1) gemm_decode_kerne
         if (ok) slot_store<BN, TOK>(p, tok0, row, run);
       } else {  // the split tile's owner: add the parts of the CTAs after it, then write
         if (e == 0 && lane == 0) QOQ_TRACE_AT(p, 960 + 4 * (unit_no & 7) + 0, 0);
+        // Last contributor first: its part is the first unit of its range and
+        // was stored early, while a CTA whose whole range lies inside the tile
+        // stores its part only as it finishes.  In this order the early part's
+        // round trip overlaps the wait for the late one.
         const int b1 = sk_cta_of(p, (uint32_t)(u.tile - p.T_dp) * (uint32_t)p.G + (uint32_t)p.G - 1);
-        for (int c = (int)blockIdx.x + 1; ok && c <= b1; ++c) ok = slot_gather<BN, TOK>(p, c, tok0, row, run);
+        if constexpr (TOK <= 16) {
+          // the scale loads go out before the gather, so their L2 round trip
+          // overlaps the gather's instead of following it (wider rows would
+          // spill the prefetched scales)
+          const RowScales<TOK> sc = load_row_scales<TOK>(p, tok0, n);
+          for (int c = b1; ok && c > (int)blockIdx.x; --c) ok = slot_gather<BN, TOK>(p, c, tok0, row, run);
+          if (ok) write_tile_out<TOK>(p, run, tok0, n, sc);
+        } else {
+          for (int c = b1; ok && c > (int)blockIdx.x; --c) ok = slot_gather<BN, TOK>(p, c, tok0, row, run);
+          if (ok) write_tile_out<TOK>(p, run, tok0, n);
+        }
         if (e == 0 && lane == 0) QOQ_TRACE_AT(p, 960 + 4 * (unit_no & 7) + 2, 0);
-        if (ok) write_tile_out<TOK>(p, run, tok0, n);
       }
       if (e == 0 && lane == 0) QOQ_TRACE_AT(p, 640 + unit_no, 0);
       ++unit_no;
