@@ -21,6 +21,15 @@
  *    library allocates no device memory and keeps no state beyond a cached
  *    per-device attribute lookup, the debug settings below, and the fixed
  *    device array behind qoq_w4a8_gemm_no_alloc.
+ *  - Host buffers at the two ends of the path: X_f16 (qoq_quant_act,
+ *    qoq_norm_quant_act) and Y_f16 (qoq_w4a8_gemm, qoq_w4a8_gemm_no_alloc)
+ *    may instead point to page-locked host memory that the device can address
+ *    (cudaHostAlloc / cudaHostRegister; with unified addressing the host
+ *    pointer is the device pointer).  The kernels then read X, or write Y,
+ *    directly across the host link, with no staging copy; Y is in host
+ *    memory once the call's work on `stream` has completed.  Any other host
+ *    pointer there is undefined behaviour: the library cannot tell the two
+ *    kinds apart.
  *  - fp16 values cross the ABI as their IEEE binary16 bit patterns (uint16_t).
  *  - Matrices are dense row-major.  W is [N][K] (row n = output channel),
  *    X / Xq are [M][K] (row m = token), Y is [M][N]: Y = X * W^T.

@@ -149,6 +149,20 @@ def test_unpack_and_status_validation():
     assert L.qoq_set_debug(0, 0) == 0
 
 
+def test_binding_refuses_pageable_host_tensors():
+    """Pinned host memory is accepted for X and Y (the kernels access it in
+    place); pageable host memory is refused before any device work."""
+    import torch
+
+    X = torch.zeros((4, 128), dtype=torch.float16)  # pageable
+    with pytest.raises(TypeError, match="pinned host"):
+        q.qoq_quant_act(X)
+    with pytest.raises(TypeError, match="pinned host"):
+        q.qoq_norm_quant_act(X, X[0])
+    with pytest.raises(TypeError, match="CUDA tensor$"):
+        binding._dev(X, torch.float16, "Xq")  # device-only arguments take no host tensor
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(binding, "_LIB", None)
     monkeypatch.setattr(binding._build, "LIB", str(tmp_path / "missing.so"))

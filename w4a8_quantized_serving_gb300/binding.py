@@ -101,10 +101,14 @@ def _stream(stream):
     return stream.cuda_stream
 
 
-def _dev(t, dtype, name: str, shape=None):
+def _dev(t, dtype, name: str, shape=None, host_ok: bool = False):
+    """Device address of tensor t, checked; with host_ok, a pinned (page-locked)
+    host tensor is accepted too and the kernels access it in place."""
     torch = _torch()
-    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+    if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_cuda and not (host_ok and t.device.type == "cpu" and t.is_pinned()):
+        raise TypeError(f"{name} must be a CUDA tensor" + (" or a pinned host tensor" if host_ok else ""))
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
@@ -152,15 +156,23 @@ def qoq_pack_weights(W, g: int = 128, packed=None, s1=None, stream=None):
     return packed, s1
 
 
+def _out_device(t):
+    """Where outputs go by default: t's device, or the current CUDA device for
+    a pinned host tensor."""
+    torch = _torch()
+    return t.device if t.is_cuda else torch.device("cuda", torch.cuda.current_device())
+
+
 def qoq_quant_act(X, Xq=None, sx=None, stream=None):
-    """X fp16 [M][K] -> (Xq int8 [M][K], sx fp16 [M])."""
+    """X fp16 [M][K] (CUDA, or pinned host: read in place) -> (Xq int8 [M][K], sx fp16 [M])."""
     torch = _torch()
     M, K = X.shape
+    xp = _dev(X, torch.float16, "X", host_ok=True)
     if Xq is None:
-        Xq = torch.empty((M, K), dtype=torch.int8, device=X.device)
+        Xq = torch.empty((M, K), dtype=torch.int8, device=_out_device(X))
     if sx is None:
-        sx = torch.empty(M, dtype=torch.float16, device=X.device)
-    _check(lib().qoq_quant_act(M, K, _dev(X, torch.float16, "X"), _dev(Xq, torch.int8, "Xq", (M, K)),
+        sx = torch.empty(M, dtype=torch.float16, device=_out_device(X))
+    _check(lib().qoq_quant_act(M, K, xp, _dev(Xq, torch.int8, "Xq", (M, K)),
                                _dev(sx, torch.float16, "sx", (M,)), _stream(stream)), "qoq_quant_act")
     return Xq, sx
 
@@ -170,17 +182,19 @@ NORM_KINDS = {"rms": 0, "layer": 1}
 
 def qoq_norm_quant_act(X, gamma, beta=None, kind: str = "rms", eps: float = 1e-6, Xq=None, sx=None, stream=None):
     """RMSNorm (or LayerNorm with beta) fused with the per-token int8 quantizer:
-    X fp16 [M][K], gamma (and beta) fp16 [K] -> (Xq int8 [M][K], sx fp16 [M])."""
+    X fp16 [M][K] (CUDA, or pinned host: read in place), gamma (and beta) fp16
+    [K] -> (Xq int8 [M][K], sx fp16 [M])."""
     torch = _torch()
     M, K = X.shape
     if kind not in NORM_KINDS:
         raise ValueError(f"kind must be one of {sorted(NORM_KINDS)}")
+    xp = _dev(X, torch.float16, "X", host_ok=True)
     if Xq is None:
-        Xq = torch.empty((M, K), dtype=torch.int8, device=X.device)
+        Xq = torch.empty((M, K), dtype=torch.int8, device=_out_device(X))
     if sx is None:
-        sx = torch.empty(M, dtype=torch.float16, device=X.device)
+        sx = torch.empty(M, dtype=torch.float16, device=_out_device(X))
     bptr = None if beta is None else _dev(beta, torch.float16, "beta", (K,))
-    _check(lib().qoq_norm_quant_act(M, K, NORM_KINDS[kind], float(eps), _dev(X, torch.float16, "X"),
+    _check(lib().qoq_norm_quant_act(M, K, NORM_KINDS[kind], float(eps), xp,
                                     _dev(gamma, torch.float16, "gamma", (K,)), bptr,
                                     _dev(Xq, torch.int8, "Xq", (M, K)), _dev(sx, torch.float16, "sx", (M,)),
                                     _stream(stream)), "qoq_norm_quant_act")
@@ -189,7 +203,8 @@ def qoq_norm_quant_act(X, gamma, beta=None, kind: str = "rms", eps: float = 1e-6
 
 def qoq_w4a8_gemm(Xq, sx, packed, s1, N: int | None = None, g: int = 128, Y=None, acc_debug=None,
                   workspace=None, stream=None):
-    """Y fp16 [M][N] = W4A8 GEMM of (Xq, sx) with the packed weights (and s1)."""
+    """Y fp16 [M][N] = W4A8 GEMM of (Xq, sx) with the packed weights (and s1).
+    Y may be a pinned host tensor: the kernel writes it in place."""
     torch = _torch()
     M, K = Xq.shape
     if N is None:
@@ -202,7 +217,7 @@ def qoq_w4a8_gemm(Xq, sx, packed, s1, N: int | None = None, g: int = 128, Y=None
     acc_ptr = None if acc_debug is None else _dev(acc_debug, torch.int32, "acc_debug", (M, N))
     code = lib().qoq_w4a8_gemm(M, N, K, g, _dev(Xq, torch.int8, "Xq"), _dev(sx, torch.float16, "sx", (M,)),
                                _dev(packed, torch.uint8, "packed"), _dev(s1, torch.float16, "s1", (N,)),
-                               _dev(Y, torch.float16, "Y", (M, N)), acc_ptr,
+                               _dev(Y, torch.float16, "Y", (M, N), host_ok=True), acc_ptr,
                                _dev(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream))
     _check(code, "qoq_w4a8_gemm")
     return Y
@@ -225,7 +240,7 @@ def qoq_w4a8_gemm_no_alloc(Xq, sx, packed, s1, N: int | None = None, g: int = 12
                                         _dev(sx, torch.float16, "sx", (M,)),
                                         _dev(packed, torch.uint8, "packed"),
                                         _dev(s1, torch.float16, "s1", (N,)),
-                                        _dev(Y, torch.float16, "Y", (M, N)), acc_ptr, _stream(stream))
+                                        _dev(Y, torch.float16, "Y", (M, N), host_ok=True), acc_ptr, _stream(stream))
     _check(code, "qoq_w4a8_gemm_no_alloc")
     return Y
 
