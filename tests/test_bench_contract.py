@@ -1,0 +1,64 @@
+"""bench.py's host logic (CPU): the algorithmic byte count behind the roofline,
+the DRAM-traffic record's source check, and the reference arm's JSON line,
+which runs the oracle on the host cores and needs no GPU."""
+import importlib.util
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def bench():
+    spec = importlib.util.spec_from_file_location("bench_under_test", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def test_algorithmic_bytes_decode_workload(bench):
+    # M=16, N=12288, K=4096, g=128: nibbles N K / 2, one s2 and one z byte per
+    # (row, group), fp16 s1, int8 Xq, fp16 s_x, fp16 Y
+    M, N, K = 16, 12288, 4096
+    b = bench.algorithmic_bytes(M, N, K, 128)
+    assert b["gemm"] == 25165824 + 786432 + 24576 + 65536 + 32 + 393216 == 26435616
+    # the quantizer reads fp16 X, writes int8 Xq and fp16 s_x
+    assert b["act"] == 2 * M * K + M * K + 2 * M
+    assert b["step"] == b["gemm"] + b["act"]
+    # smaller groups carry more scale bytes, larger ones fewer (minimal bytes)
+    assert bench.algorithmic_bytes(M, N, K, 32)["gemm"] - b["gemm"] == 2 * N * (K // 32 - K // 128)
+    assert bench.algorithmic_bytes(M, N, K, 256)["gemm"] < b["gemm"]
+
+
+def test_traffic_record_follows_the_gemm_sources(bench, monkeypatch):
+    rec = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))["decode_qkv_7b"]
+    assert rec["algorithmic_bytes_per_launch"] == bench.algorithmic_bytes(16, 12288, 4096)["gemm"]
+    traffic, src = bench.recorded_traffic("decode_qkv_7b")
+    if rec["source_sha256"] == bench.gemm_source_hash():
+        assert traffic == rec["dram_bytes_per_launch"]
+    else:
+        assert traffic is None
+    # any change to the GEMM sources voids the record
+    monkeypatch.setattr(bench, "gemm_source_hash", lambda: "0" * 64)
+    assert bench.recorded_traffic("decode_qkv_7b")[0] is None
+
+
+def test_reference_arm_json_line(bench):
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                          "--warmup", "3"], capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference"
+    assert d["metric"] == bench.METRIC and d["unit"] == bench.UNIT and d["higher_is_better"] is True
+    assert d["n_gpus"] == 1 and d["steps"] == 1 and d["warmup"] == 3
+    assert d["value"] > 0 and d["ms_per_step"] > 0
+    assert d["config"]["workload"] == "decode_qkv_7b"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
