@@ -585,7 +585,7 @@ def main() -> None:
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="time direct launches instead of a CUDA graph")
     ap.add_argument("--traffic", type=float, default=None,
-                    help="DRAM bytes per GEMM launch from an ncu capture of this build, if known")
+                    help="DRAM bytes per GEMM launch from an ncu capture of the current library, if known")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     c = dict(synth.WORKLOADS[args.config])
