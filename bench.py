@@ -92,6 +92,24 @@ def dist_env() -> tuple[int, int, int]:
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def max_over_ranks(dist, vals: list, device) -> list:
+    """Element-wise maximum of per-rank timings, returned on every rank (the
+    slowest rank sets the job's time); the values themselves without a group."""
+    if dist is None:
+        return [float(v) for v in vals]
+    import torch
+
+    t = torch.tensor([float(v) for v in vals], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def job_tops(world: int, ops: float, ms: float) -> float:
+    """Whole-job throughput: every rank does `ops` per step in `ms` (the max
+    over ranks), so the job does world * ops per step."""
+    return world * ops / (ms * 1e-3) / 1e12
+
+
 # ------------------------------------------------------------------ clocks --
 
 class ClockSampler:
@@ -479,6 +497,9 @@ def run_ours(args, c: dict) -> None:
         st = q.qoq_last_device_status(s["ws"])
         if st != 0:
             raise SystemExit(f"device status: {q.qoq_status_str(st)}")
+    ms_per_step = ms_total / args.steps
+    ms_per_step, gemm_ms, act_ms, copy_ms, direct_ms = max_over_ranks(
+        dist, [ms_per_step, gemm_ms, act_ms, copy_ms, direct_ms], dev)
     if direct_ms <= copy_ms:
         e2e_ms, e2e_how = direct_ms, (
             "public API per step with host buffers: qoq_quant_act reads X in place from pinned host memory and "
@@ -491,15 +512,9 @@ def run_ours(args, c: dict) -> None:
             "streams that overlap the neighbouring steps' kernels; " +
             ("the K steps captured once in a CUDA graph and replayed" if copy_graph else "direct calls"))
 
-    ms_per_step = ms_total / args.steps
-    if dist:
-        tt = torch.tensor([ms_per_step, e2e_ms, gemm_ms, act_ms, copy_ms, direct_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_per_step, e2e_ms, gemm_ms, act_ms, copy_ms, direct_ms = (float(v) for v in tt.tolist())
-
     ops = 2.0 * M * N * K
     nbytes = algorithmic_bytes(M, N, K, G)
-    value = world * ops / (ms_per_step * 1e-3) / 1e12
+    value = job_tops(world, ops, ms_per_step)
     peaks, peak_src = load_peaks()
     intensity = ops / nbytes["gemm"]
     ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
@@ -549,7 +564,7 @@ def run_ours(args, c: dict) -> None:
         "hbm_gb_per_s_step": world * nbytes["step"] / (ms_per_step * 1e-3) / 1e9,
         "roofline": roof,
         "act_roofline": act_roof,
-        "e2e": {"value": world * ops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+        "e2e": {"value": job_tops(world, ops, e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": 2 * M * K, "d2h_bytes_per_step": 2 * M * N,
                 "ms_per_step": e2e_ms, "how": e2e_how,
                 "routes_ms_per_step": {"host_buffers_in_place": direct_ms, "copy_engines": copy_ms}},

@@ -62,3 +62,56 @@ def test_reference_arm_json_line(bench):
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def _max_over_ranks_worker(rank, world, port, q):
+    import torch.distributed as dist
+
+    spec = importlib.util.spec_from_file_location("bench_in_rank", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank, world_size=world)
+    try:
+        mine = [1.0 + rank, 5.0 - rank, 2.5]  # each rank's timings
+        q.put((rank, mod.max_over_ranks(dist, mine, "cpu")))
+        dist.barrier()
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_two_gloo_ranks():
+    """The job's time is the slowest rank's, element by element, on every
+    rank (world size 2, gloo on CPU)."""
+    import socket
+
+    import torch.multiprocessing as mp
+
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_max_over_ranks_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = dict(q.get(timeout=120) for _ in range(2))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert got[0] == got[1] == [2.0, 5.0, 2.5]
+
+
+def test_job_throughput_counts_every_rank(bench):
+    ops = 2.0 * 16 * 12288 * 4096
+    assert bench.job_tops(1, ops, 0.01) == pytest.approx(ops / 1e-5 / 1e12)
+    assert bench.job_tops(4, ops, 0.01) == pytest.approx(4 * bench.job_tops(1, ops, 0.01))
+    assert bench.max_over_ranks(None, [1, 2.5], "cpu") == [1.0, 2.5]
+
+
+def test_reference_arm_other_ranks_print_nothing():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2",
+                          "--steps", "1", "--warmup", "3"], capture_output=True, text=True, timeout=300, cwd=ROOT,
+                         env=env)
+    assert out.returncode == 0, out.stderr[-2000:]
+    assert not [l for l in out.stdout.splitlines() if l.startswith("{")]
