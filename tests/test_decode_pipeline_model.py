@@ -206,3 +206,46 @@ def test_model_catches_a_skipped_accumulator_wait():
                 for s in range(8) for h in range(6))
     assert found
     assert not any(run(units, nslot, stages, hold=(h,), seed=s)[1] for s in range(8) for h in range(6))
+
+
+def sk_cta_of(it, P, I):
+    """The CTA whose stream-K range holds group iteration it (the kernel's
+    formula: CTA b's range is [floor(b I / P), floor((b + 1) I / P)))."""
+    return ((it + 1) * P - 1) // I
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 12288, 4096), (16, 4096, 14336), (64, 22016, 4096), (1, 384, 1152),
+                                   (40, 1664, 1152), (16, 19456, 8192), (8, 256, 512), (32, 128, 131072),
+                                   (16, 38912, 4096)])
+def test_stream_k_schedule_and_hand_off(M, N, K):
+    """The decode kernel's work split covers every (tile, group) exactly once;
+    a split tile's owner is the CTA holding its group 0, that part is the
+    owner's last unit, and the CTAs it gathers from (blockIdx + 1 .. the CTA of
+    the tile's last group) are exactly the other holders, each holding one
+    part of the tile as a unit of its own; every such part is either the
+    first unit of its CTA or that CTA's only unit, and no CTA holds two (one
+    split-K slot per CTA)."""
+    G, T, T_dp, P = schedule(M, N, K)
+    seen = {}
+    units_of = {b: cta_units(b, P, T, G, T_dp) for b in range(P)}
+    for b, units in units_of.items():
+        assert sum(1 for _, g0, _ in units if g0 > 0) <= 1
+        for t, g0, g1 in units:
+            assert 0 <= g0 < g1 <= G
+            for g in range(g0, g1):
+                assert (t, g) not in seen
+                seen[t, g] = b
+    assert len(seen) == T * G
+    I = (T - T_dp) * G
+    for t in range(T_dp, T):
+        holders = sorted({seen[t, g] for g in range(G)})
+        owner = seen[t, 0]
+        if len(holders) == 1:
+            continue
+        assert units_of[owner][-1] == (t, 0, units_of[owner][-1][2])  # the owner's last unit
+        b1 = sk_cta_of((t - T_dp) * G + G - 1, P, I)
+        assert holders == list(range(owner, b1 + 1))
+        for c in holders[1:]:
+            parts = [u for u in units_of[c] if u[0] == t]
+            assert len(parts) == 1 and parts[0][1] > 0
+            assert units_of[c][0] == parts[0] or len(units_of[c]) == 1
