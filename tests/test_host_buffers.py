@@ -64,3 +64,17 @@ def test_host_x_norm_quant_matches_device_x():
         t.cuda.synchronize()
         assert np.array_equal(Xq_h.cpu().numpy(), Xq_d.cpu().numpy()), kind
         assert np.array_equal(gc.f16_bits(sx_h), gc.f16_bits(sx_d)), kind
+
+
+def test_linear_layer_with_host_buffers():
+    """QoQLinear with X and Y in pinned host memory gives the device path's Y."""
+    mod, t = q(), gc.torch()
+    M, N, K = 16, 1280, 1024
+    W = gc.to_dev_f16(synth.weights(N, K, 51))
+    X = synth.activations(M, K, 52)
+    layer = mod.QoQLinear(W)
+    Yd = layer(gc.to_dev_f16(X))
+    Yh = t.empty((M, N), dtype=t.float16, pin_memory=True)
+    assert layer(pinned_f16(X), out=Yh) is Yh
+    t.cuda.synchronize()
+    assert np.array_equal(Yh.numpy().view(np.uint16), gc.f16_bits(Yd))

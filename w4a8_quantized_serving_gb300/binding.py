@@ -273,7 +273,9 @@ def qoq_last_device_status(workspace, stream=None) -> int:
 class QoQLinear:
     """A W4A8 linear layer: weights packed once, Y = X W^T per call.
 
-    Holds the packed weights, s1, and one workspace per token count M.
+    Holds the packed weights, s1, and one workspace per token count M.  X may
+    be a CUDA tensor or a pinned host tensor; `out` (optional) receives Y and
+    may be either as well.
     """
 
     def __init__(self, W, g: int = 128):
@@ -289,7 +291,7 @@ class QoQLinear:
             self._ws[M] = torch.zeros(need, dtype=torch.uint8, device=self.packed.device)
         return self._ws[M]
 
-    def __call__(self, X, stream=None):
+    def __call__(self, X, out=None, stream=None):
         Xq, sx = qoq_quant_act(X, stream=stream)
-        return qoq_w4a8_gemm(Xq, sx, self.packed, self.s1, self.N, self.g,
+        return qoq_w4a8_gemm(Xq, sx, self.packed, self.s1, self.N, self.g, Y=out,
                              workspace=self.workspace(X.shape[0]), stream=stream)
