@@ -502,7 +502,8 @@ def run_ours(args, c: dict) -> None:
         dist, [ms_per_step, gemm_ms, act_ms, copy_ms, direct_ms], dev)
     if direct_ms <= copy_ms:
         e2e_ms, e2e_how = direct_ms, (
-            "public API per step with host buffers: qoq_quant_act reads X in place from pinned host memory and "
+            "public API per step with host buffers: " + ("qoq_norm_quant_act" if norm_step else "qoq_quant_act") +
+            " reads X in place from pinned host memory and "
             "qoq_w4a8_gemm writes Y in place into pinned host memory, every step (unified addressing over the "
             "host link, no staging copy); " + ("the K steps captured once in a CUDA graph and replayed"
                                                if direct_graph else "direct calls"))
