@@ -6,18 +6,22 @@ quantization of the activations (qoq_quant_act) and the W4A8 GEMM
 separately).  Default workload: the 7B fused-QKV decode projection,
 M=16, N=12288, K=4096, g=128 (seed 1).
 
-Timing: W untimed warm-up steps, then K steps between CUDA events on the
-launching stream with a barrier and a device synchronize on both sides.  The
-inputs of consecutive steps rotate through a pool of independent buffer sets
-larger than 3x L2, so every step streams its weights from HBM.
+Timing: W untimed warm-up steps, then timed regions of exactly K steps each
+(a CUDA graph of K steps, replayed), every region between CUDA events on the
+launching stream with a barrier and a device synchronize on both sides; the
+line reports the median region.  The inputs of consecutive steps rotate
+through a pool of independent buffer sets larger than 3x L2, so every step
+streams its weights from HBM.
 
 Output: one JSON line (rank 0).  Keys beyond the metric: roofline of the
-dominant kernel (the GEMM call), the oracle's CPU baseline, the end-to-end
-number through the public API with host buffers, clocks sampled during the
-timed region, and the count of kernel launches inside it.
+dominant kernel (the GEMM call), the oracle's CPU baseline (all host cores and
+one), the end-to-end number through the public API with host buffers, clocks
+sampled during the timed regions, the count of kernel launches inside a
+region, and a per_config block with the same measurements for every workload
+of the metric (M = 8 .. 4096).
 
 --impl reference times the oracle (the plain CPU implementation the tests
-check against) on the host cores instead: it is the reference arm.
+check against) on all host cores instead: it is the reference arm.
 """
 from __future__ import annotations
 
@@ -174,34 +178,56 @@ class ClockSampler:
 
 # ------------------------------------------------------------- CPU oracle --
 
-def oracle_step_timing(c: dict, budget_s: float, n_sample: int | None = None) -> dict:
-    """Time the oracle on a bounded sample of the workload: all M tokens
-    quantized, the GEMM over a sample of output channels (weights quantized
-    beforehand, outside the timing, as on the GPU)."""
+def oracle_sample_channels(c: dict, macs_per_step: float) -> int:
+    """Output channels of a bounded oracle sample: all N when the workload's
+    product is at most `macs_per_step` multiply-adds, else a multiple of 128
+    that keeps it near that size."""
+    M, N, K = c["M"], c["N"], c["K"]
+    if M * N * K <= macs_per_step:
+        return N
+    return max(128, int(macs_per_step / (M * K)) // 128 * 128)
+
+
+def oracle_step_timing(c: dict, budget_s: float, threads: int, n_sample: int | None = None) -> dict:
+    """Time the oracle on a (bounded) sample of the workload: all M tokens
+    quantized, the GEMM over the first n_sample output channels (weights
+    quantized beforehand, outside the timing, as on the GPU).  threads: host
+    threads of the oracle's product (0: all cores; its per-token quantizer is
+    single-threaded)."""
     import oracle
 
     M, N, K = c["M"], c["N"], c["K"]
-    if n_sample is None:
-        n_sample = N
-    n_sample = min(N, n_sample)
+    g = c.get("g", 128)
+    n_sample = min(N, N if n_sample is None else n_sample)
     W = synth.weights(n_sample, K, c["seed"])  # the first n_sample output channels
     X = synth.activations(M, K, c["seed"])
-    wq = oracle.weight_quant(synth.bits(W), c.get("g", 128))
+    wq = oracle.weight_quant(synth.bits(W), g)
+    cores = oracle.host_cores() if threads == 0 else threads
     times = []
     t_end = time.perf_counter() + budget_s
     while True:
         t0 = time.perf_counter()
         Xq, sx = oracle.act_quant(synth.bits(X))
-        oracle.gemm(Xq, sx, wq["q4"], wq["s2"], wq["z"], wq["s1"], c.get("g", 128), want_acc=False)
+        oracle.gemm(Xq, sx, wq["q4"], wq["s2"], wq["z"], wq["s1"], g, want_acc=False, threads=threads)
         times.append(time.perf_counter() - t0)
         if time.perf_counter() >= t_end or len(times) >= 50:
             break
     t = statistics.median(times)
     ops = 2.0 * M * n_sample * K
-    return {"value": ops / t / 1e12, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"act-quant of all {M} tokens + GEMM over {n_sample} of {N} output channels, "
-                      f"K={K}; median of {len(times)} runs of {t:.3f} s (single-threaded C)",
+    what = "the full workload" if n_sample == N else f"GEMM over {n_sample} of {N} output channels"
+    return {"value": ops / t / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"act-quant of all {M} tokens + {what}, K={K}; median of {len(times)} runs of "
+                      f"{t:.4f} s (C oracle, {cores} host thread{'s' if cores > 1 else ''})",
             "seconds_per_sample": t}
+
+
+def cpu_baselines(c: dict, budget_s: float) -> dict:
+    """The oracle on all host cores (the reported baseline) and, on a smaller
+    bounded sample, on one core."""
+    allc = oracle_step_timing(c, budget_s * 0.5, threads=0, n_sample=oracle_sample_channels(c, 2e10))
+    one = oracle_step_timing(c, budget_s * 0.5, threads=1, n_sample=oracle_sample_channels(c, 8e8))
+    allc["single_thread"] = {k: one[k] for k in ("value", "unit", "cores", "sample")}
+    return allc
 
 
 def run_reference(args, c: dict) -> None:
@@ -209,16 +235,17 @@ def run_reference(args, c: dict) -> None:
     if rank != 0:
         return
     M, N, K = c["M"], c["N"], c["K"]
+    g = c.get("g", 128)
     import oracle
 
-    n_sample = min(N, 512)
+    n_sample = oracle_sample_channels(c, 2e10)  # the full workload for M <= 1024-class shapes
     W = synth.weights(n_sample, K, c["seed"])
     X = synth.activations(M, K, c["seed"])
-    wq = oracle.weight_quant(synth.bits(W), c.get("g", 128))
+    wq = oracle.weight_quant(synth.bits(W), g)
 
     def step():
         Xq, sx = oracle.act_quant(synth.bits(X))
-        oracle.gemm(Xq, sx, wq["q4"], wq["s2"], wq["z"], wq["s1"], c.get("g", 128), want_acc=False)
+        oracle.gemm(Xq, sx, wq["q4"], wq["s2"], wq["z"], wq["s1"], g, want_acc=False, threads=0)
 
     for _ in range(args.warmup):
         step()
@@ -227,13 +254,15 @@ def run_reference(args, c: dict) -> None:
         step()
     dt = (time.perf_counter() - t0) / max(1, args.steps)
     value = 2.0 * M * n_sample * K / dt / 1e12
-    sample = f"per step: act-quant of {M} tokens + GEMM over {n_sample} of {N} output channels, K={K}"
+    cores = oracle.host_cores()
+    what = "the full workload" if n_sample == N else f"GEMM over {n_sample} of {N} output channels"
+    sample = f"per step: act-quant of {M} tokens + {what}, K={K}, on {cores} host threads"
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "int64", "data": "synthetic",
         "config": config_dict(c),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -248,27 +277,42 @@ def config_dict(c: dict, extra: dict | None = None) -> dict:
 
 # ------------------------------------------------------------------ GPU arm --
 
-def run_ours(args, c: dict) -> None:
-    import torch
+def roofline_of(M: int, N: int, K: int, g: int, gemm_ms: float, steps: int, peaks: dict, peak_src: str) -> dict:
+    """The GEMM call against the roofline that binds it: HBM below the ridge
+    (algorithmic bytes / time), the tensor pipe above it (2MNK / time)."""
+    ops = 2.0 * M * N * K
+    nbytes = algorithmic_bytes(M, N, K, g)["gemm"]
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if ops / nbytes < ridge:
+        achieved = nbytes / (gemm_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "peak_source": f"{peak_src} hbm_gbs (copy bandwidth)"}
+    else:
+        achieved = ops / (gemm_ms * 1e-3) / 1e12
+        sustained = steps * gemm_ms > 1000
+        pk = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
+        roof = {"bound": "tensor", "achieved": achieved, "peak": pk, "unit": "TFLOP/s", "frac": achieved / pk,
+                "peak_source": f"{peak_src} bf16 dense {'sustained' if sustained else 'burst'} "
+                               "(fp16 operands run at the bf16 rate)"}
+    roof["algorithmic_bytes_per_launch"] = nbytes
+    roof["ms_per_launch"] = gemm_ms
+    roof["gb_per_s_algorithmic"] = nbytes / (gemm_ms * 1e-3) / 1e9
+    roof["tops_effective"] = ops / (gemm_ms * 1e-3) / 1e12
+    return roof
 
-    import w4a8_quantized_serving_gb300 as q
 
-    rank, world, local = dist_env()
-    torch.cuda.set_device(local)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist  # noqa: F811
-
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-
+def bench_workload(q, torch, c: dict, args, dev, stream, dist, rank: int) -> dict:
+    """Every GPU measurement of one workload: the step, the GEMM call alone and
+    the step's quantizer alone (each a CUDA graph of K steps, timed over
+    args.repeats regions of exactly K steps; the median region is reported),
+    and the two end-to-end routes through the public API with host buffers."""
     M, N, K = c["M"], c["N"], c["K"]
-    dev = torch.device("cuda", local)
-    stream = torch.cuda.current_stream()
+    G = c.get("g", 128)
+    K_steps, repeats = args.steps, args.repeats
 
     # weights: generated once, packed on the GPU (timed separately), cloned into a pool
     W = torch.from_numpy(synth.weights(N, K, c["seed"])).to(dev)
     X = torch.from_numpy(synth.activations(M, K, c["seed"] + rank)).to(dev)
-    G = c.get("g", 128)
     packed, s1 = q.qoq_pack_weights(W, g=G)
     torch.cuda.synchronize()
     pk_ev0, pk_ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -285,7 +329,7 @@ def run_ours(args, c: dict) -> None:
     set_bytes = packed.numel() + 2 * N + 2 * M * K + M * K + 2 * M + 2 * M * N + ws_bytes
     nsets = max(2, int(np.ceil(3 * l2 / set_bytes)))
     sets = []
-    for i in range(nsets):
+    for _ in range(nsets):
         sets.append(dict(
             packed=packed.clone(), s1=s1.clone(), X=X.clone(),
             Xq=torch.empty((M, K), dtype=torch.int8, device=dev),
@@ -299,114 +343,89 @@ def run_ours(args, c: dict) -> None:
     norm_step = args.step == "norm"
     gamma = torch.from_numpy(np.random.default_rng(c["seed"]).uniform(0.5, 1.5, K).astype(np.float16)).to(dev)
 
-    def quantize(s):
+    def quantize(s, X_src=None):
+        src = s["X"] if X_src is None else X_src
         if norm_step:
-            q.qoq_norm_quant_act(s["X"], gamma, kind="rms", eps=1e-6, Xq=s["Xq"], sx=s["sx"])
+            q.qoq_norm_quant_act(src, gamma, kind="rms", eps=1e-6, Xq=s["Xq"], sx=s["sx"])
         else:
-            q.qoq_quant_act(s["X"], Xq=s["Xq"], sx=s["sx"])
+            q.qoq_quant_act(src, Xq=s["Xq"], sx=s["sx"])
 
-    def step(i: int):
-        s = sets[i % nsets]
-        quantize(s)
-        q.qoq_w4a8_gemm(s["Xq"], s["sx"], s["packed"], s["s1"], N, g=G, Y=s["Y"], workspace=s["ws"])
+    def gemm(s, Y=None):
+        q.qoq_w4a8_gemm(s["Xq"], s["sx"], s["packed"], s["s1"], N, g=G, Y=s["Y"] if Y is None else Y,
+                        workspace=s["ws"])
 
-    for i in range(max(3, args.warmup)):
-        step(i)
+    def steps_full(n: int):
+        for i in range(n):
+            s = sets[i % nsets]
+            quantize(s)
+            gemm(s)
+
+    def steps_gemm(n: int):
+        for i in range(n):
+            gemm(sets[i % nsets])
+
+    def steps_act(n: int):
+        for i in range(n):
+            quantize(sets[i % nsets])
+
+    steps_full(max(3, args.warmup))
     torch.cuda.synchronize()
     st = q.qoq_last_device_status(sets[0]["ws"])
     if st != 0:
         raise SystemExit(f"device status after warm-up: {q.qoq_status_str(st)}")
 
-    # The timed region replays CUDA graphs of exactly K steps (the step is
-    # launch-bound at decode sizes; graphs remove the host from the loop).
-    def gemm_only(i: int):
-        s = sets[i % nsets]
-        q.qoq_w4a8_gemm(s["Xq"], s["sx"], s["packed"], s["s1"], N, g=G, Y=s["Y"], workspace=s["ws"])
-
-    def act_only(i: int):
-        quantize(sets[i % nsets])
-
     use_graph = not args.no_graph
-    g_step = g_gemm = g_act = None
-    if use_graph:
-        try:
-            g_step = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g_step):
-                for i in range(args.steps):
-                    step(i)
-            g_gemm = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g_gemm):
-                for i in range(args.steps):
-                    gemm_only(i)
-            g_act = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g_act):
-                for i in range(args.steps):
-                    act_only(i)
-            g_step.replay()  # untimed warm replay
-            g_gemm.replay()
-            g_act.replay()
-            torch.cuda.synchronize()
-        except Exception as exc:  # capture unsupported: time direct launches instead
-            print(f"graph capture failed ({exc}); timing direct launches", file=sys.stderr)
-            use_graph = False
-            g_step = g_gemm = g_act = None
-            torch.cuda.synchronize()
 
-    # ---- timed region: K steps
-    sampler = ClockSampler(local)
-    sampler.start()
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    t0.record(stream)
-    if use_graph:
-        g_step.replay()
-    else:
-        for i in range(args.steps):
-            step(i)
-    t1.record(stream)
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    # the dominant call alone, same launch configuration, same pool
-    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    g0.record(stream)
-    if use_graph:
-        g_gemm.replay()
-    else:
-        for i in range(args.steps):
-            gemm_only(i)
-    g1.record(stream)
-    torch.cuda.synchronize()
-    clocks = sampler.stop()
-    ms_total = t0.elapsed_time(t1)
-    gemm_ms = g0.elapsed_time(g1) / args.steps
-    # the step's activation quantizer alone (same pool)
-    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a0.record(stream)
-    if use_graph:
-        g_act.replay()
-    else:
-        for i in range(args.steps):
-            act_only(i)
-    a1.record(stream)
-    torch.cuda.synchronize()
-    act_ms = a0.elapsed_time(a1) / args.steps
+    def timed(run_steps, name: str) -> tuple[list[float], bool]:
+        """ms per step of each of `repeats` timed regions of exactly K steps."""
+        graph = None
+        run_steps(3)
+        torch.cuda.synchronize()
+        if use_graph:
+            try:
+                graph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(graph):
+                    run_steps(K_steps)
+                for _ in range(2):  # untimed warm replays
+                    graph.replay()
+                torch.cuda.synchronize()
+            except Exception as exc:  # capture unsupported: time direct calls instead
+                print(f"{name}: graph capture failed ({exc}); timing direct calls", file=sys.stderr)
+                graph = None
+                torch.cuda.synchronize()
+        out = []
+        for _ in range(repeats):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            if dist:
+                dist.barrier()
+            torch.cuda.synchronize()
+            e0.record(stream)
+            if graph is not None:
+                graph.replay()
+            else:
+                run_steps(K_steps)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if dist:
+                dist.barrier()
+            out.append(e0.elapsed_time(e1) / K_steps)
+        return out, graph is not None
+
+    step_regions, step_graph = timed(steps_full, "step")
+    gemm_regions, _ = timed(steps_gemm, "gemm")
+    act_regions, _ = timed(steps_act, "quantizer")
     for s in sets:
         st = q.qoq_last_device_status(s["ws"])
         if st != 0:
             raise SystemExit(f"device status: {q.qoq_status_str(st)}")
 
-    # ---- end to end through the public API with host buffers.  Each step
-    # copies its input X from pinned host memory and its output Y back to
-    # pinned host memory; the copies run on their own streams so that step
-    # i+1's upload and step i-1's download overlap step i's kernels (events
-    # keep each buffer set's reuse in order).
+    # ---- end to end through the public API with host buffers.  Route 1: each
+    # step copies its X from pinned host memory and its Y back to pinned host
+    # memory on copy streams, so that step i+1's upload and step i-1's
+    # download overlap step i's kernels (events keep each set's reuse in order).
     Xh = torch.empty((M, K), dtype=torch.float16, pin_memory=True)
     Xh.copy_(X.cpu())
     Yh = [torch.empty((M, N), dtype=torch.float16, pin_memory=True) for _ in range(2)]
-    e_steps = args.steps
     h2d, d2h = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     ev = [{k: torch.cuda.Event() for k in ("x_ready", "x_free", "y_ready", "y_free")} for _ in range(nsets)]
     used = [False] * nsets
@@ -425,7 +444,7 @@ def run_ours(args, c: dict) -> None:
             comp.wait_event(e["y_free"])
         quantize(s)
         e["x_free"].record(comp)
-        q.qoq_w4a8_gemm(s["Xq"], s["sx"], s["packed"], s["s1"], N, g=G, Y=s["Y"], workspace=s["ws"])
+        gemm(s)
         e["y_ready"].record(comp)
         with torch.cuda.stream(d2h):
             d2h.wait_event(e["y_ready"])
@@ -444,66 +463,35 @@ def run_ours(args, c: dict) -> None:
         comp.wait_stream(h2d)  # and join them back
         comp.wait_stream(d2h)
 
-    # The second route: the same calls with the host buffers themselves.  The
-    # quantizer reads X in place from pinned host memory and the GEMM writes Y
-    # in place into pinned host memory (unified addressing over the host
-    # link), so no copy engine or cross-stream event sits between the kernels.
+    # Route 2: the same calls with the host buffers themselves.  The quantizer
+    # reads X in place from pinned host memory and the GEMM writes Y in place
+    # into pinned host memory (unified addressing over the host link), so no
+    # copy engine or cross-stream event sits between the kernels.
     Xh2 = [torch.empty((M, K), dtype=torch.float16, pin_memory=True) for _ in range(2)]
     for h in Xh2:
         h.copy_(Xh)
 
-    def direct_step(i: int):
-        s = sets[i % nsets]
-        if norm_step:
-            q.qoq_norm_quant_act(Xh2[i % 2], gamma, kind="rms", eps=1e-6, Xq=s["Xq"], sx=s["sx"])
-        else:
-            q.qoq_quant_act(Xh2[i % 2], Xq=s["Xq"], sx=s["sx"])
-        q.qoq_w4a8_gemm(s["Xq"], s["sx"], s["packed"], s["s1"], N, g=G, Y=Yh[i % 2], workspace=s["ws"])
-
     def direct_steps(n: int):
         for i in range(n):
-            direct_step(i)
+            s = sets[i % nsets]
+            quantize(s, Xh2[i % 2])
+            gemm(s, Y=Yh[i % 2])
 
-    def time_route(run_steps, name: str):
-        run_steps(3)
-        torch.cuda.synchronize()
-        graph = None
-        if use_graph:
-            try:
-                graph = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(graph):
-                    run_steps(e_steps)
-                graph.replay()
-                torch.cuda.synchronize()
-            except Exception as exc:  # capture unsupported: time direct calls instead
-                print(f"{name} graph capture failed ({exc}); timing direct calls", file=sys.stderr)
-                graph = None
-                torch.cuda.synchronize()
-        if dist:
-            dist.barrier()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        if graph is not None:
-            graph.replay()
-        else:
-            run_steps(e_steps)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        return e0.elapsed_time(e1) / e_steps, graph is not None
-
-    copy_ms, copy_graph = time_route(e2e_steps, "e2e (copy engines)")
-    direct_ms, direct_graph = time_route(direct_steps, "e2e (host buffers in place)")
+    copy_regions, copy_graph = timed(e2e_steps, "e2e (copy engines)")
+    direct_regions, direct_graph = timed(direct_steps, "e2e (host buffers in place)")
     for s in sets:
         st = q.qoq_last_device_status(s["ws"])
         if st != 0:
             raise SystemExit(f"device status: {q.qoq_status_str(st)}")
-    ms_per_step = ms_total / args.steps
+
+    med = statistics.median
     ms_per_step, gemm_ms, act_ms, copy_ms, direct_ms = max_over_ranks(
-        dist, [ms_per_step, gemm_ms, act_ms, copy_ms, direct_ms], dev)
+        dist, [med(step_regions), med(gemm_regions), med(act_regions), med(copy_regions), med(direct_regions)],
+        dev)
+    quant_name = "qoq_norm_quant_act" if norm_step else "qoq_quant_act"
     if direct_ms <= copy_ms:
         e2e_ms, e2e_how = direct_ms, (
-            "public API per step with host buffers: " + ("qoq_norm_quant_act" if norm_step else "qoq_quant_act") +
-            " reads X in place from pinned host memory and "
+            f"public API per step with host buffers: {quant_name} reads X in place from pinned host memory and "
             "qoq_w4a8_gemm writes Y in place into pinned host memory, every step (unified addressing over the "
             "host link, no staging copy); " + ("the K steps captured once in a CUDA graph and replayed"
                                                if direct_graph else "direct calls"))
@@ -512,71 +500,136 @@ def run_ours(args, c: dict) -> None:
             "public API per step; X uploaded from and Y read back to pinned host memory every step, on copy "
             "streams that overlap the neighbouring steps' kernels; " +
             ("the K steps captured once in a CUDA graph and replayed" if copy_graph else "direct calls"))
+    out = dict(
+        ms_per_step=ms_per_step, gemm_ms=gemm_ms, act_ms=act_ms, e2e_ms=e2e_ms, e2e_how=e2e_how,
+        copy_ms=copy_ms, direct_ms=direct_ms, pack_ms=pack_ms, use_graph=step_graph,
+        regions={"step": step_regions, "gemm": gemm_regions, "quantizer": act_regions},
+        l2_policy=f"rotating pool of {nsets} buffer sets, {nsets * set_bytes / 1e6:.0f} MB "
+                  f"(>= 3x L2 {l2 / 1e6:.0f} MB)",
+        norm_step=norm_step, quant_name=quant_name)
+    del sets
+    torch.cuda.empty_cache()
+    return out
+
+
+def config_summary(c: dict, r: dict, args, world: int, peaks: dict, peak_src: str) -> dict:
+    """The per-workload entry of the per_config block."""
+    M, N, K = c["M"], c["N"], c["K"]
+    G = c.get("g", 128)
+    ops = 2.0 * M * N * K
+    roof = roofline_of(M, N, K, G, r["gemm_ms"], args.steps, peaks, peak_src)
+    return {
+        "workload": c["name"], "M": M, "N": N, "K": K, "g": G,
+        "value": job_tops(world, ops, r["ms_per_step"]), "unit": UNIT, "ms_per_step": r["ms_per_step"],
+        "ms_per_launch": r["gemm_ms"], "roofline": {k: roof[k] for k in ("bound", "achieved", "peak", "unit",
+                                                                          "frac", "peak_source")},
+        "gemm_tops": roof["tops_effective"], "gemm_gb_per_s": roof["gb_per_s_algorithmic"],
+        "quantizer_ms": r["act_ms"],
+        "e2e": {"value": job_tops(world, ops, r["e2e_ms"]), "unit": UNIT, "ms_per_step": r["e2e_ms"],
+                "h2d_bytes_per_step": 2 * M * K, "d2h_bytes_per_step": 2 * M * N,
+                "routes_ms_per_step": {"host_buffers_in_place": r["direct_ms"], "copy_engines": r["copy_ms"]}},
+        "regions_ms_per_step": {k: [round(v, 6) for v in vs] for k, vs in r["regions"].items()},
+    }
+
+
+def run_ours(args, c: dict) -> None:
+    import torch
+
+    import w4a8_quantized_serving_gb300 as q
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist  # noqa: F811
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    M, N, K = c["M"], c["N"], c["K"]
+    G = c.get("g", 128)
+    peaks, peak_src = load_peaks()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    r = bench_workload(q, torch, c, args, dev, stream, dist, rank)
+    clocks = sampler.stop()
 
     ops = 2.0 * M * N * K
     nbytes = algorithmic_bytes(M, N, K, G)
-    value = job_tops(world, ops, ms_per_step)
-    peaks, peak_src = load_peaks()
-    intensity = ops / nbytes["gemm"]
-    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    if intensity < ridge:
-        achieved = nbytes["gemm"] / (gemm_ms * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "traffic": args.traffic,
-                "peak_source": f"{peak_src} hbm_gbs (copy bandwidth)"}
-    else:
-        achieved = ops / (gemm_ms * 1e-3) / 1e12
-        pk = peaks["bf16_tflops_sustained"] if args.steps * gemm_ms > 1000 else peaks["bf16_tflops"]
-        roof = {"bound": "tensor", "achieved": achieved, "peak": pk, "unit": "TFLOP/s",
-                "frac": achieved / pk, "traffic": args.traffic,
-                "peak_source": f"{peak_src} bf16 dense (fp16 operands run at the bf16 rate)"}
+    value = job_tops(world, ops, r["ms_per_step"])
+    roof = roofline_of(M, N, K, G, r["gemm_ms"], args.steps, peaks, peak_src)
+    roof["traffic"] = args.traffic
     if roof["traffic"] is None:
         if G == 128:
             roof["traffic"], roof["traffic_source"] = recorded_traffic(c["name"])
         else:
             roof["traffic_source"] = f"no ncu record at g = {G}"
-    roof["kernel"] = "qoq_w4a8_gemm call (the GEMM kernel; + B-operand convert for M > 64), timed alone over K launches"
-    roof["algorithmic_bytes_per_launch"] = nbytes["gemm"]
-    roof["ms_per_launch"] = gemm_ms
-    roof["gb_per_s_algorithmic"] = nbytes["gemm"] / (gemm_ms * 1e-3) / 1e9
-    roof["tops_effective"] = ops / (gemm_ms * 1e-3) / 1e12
+    roof["kernel"] = ("qoq_w4a8_gemm call (the GEMM kernel; + B-operand convert for M > 64), timed alone over "
+                      "regions of K launches")
     # the step's activation quantizer alone: 2 bytes read and 1 written per
     # element, 2 per token for s_x, plus gamma (2K) when the norm is fused
-    act_bytes = nbytes["act"] + (2 * K if norm_step else 0)
-    act_gbs = act_bytes / (act_ms * 1e-3) / 1e9
-    act_roof = {"kernel": "qoq_norm_quant_act (RMSNorm)" if norm_step else "qoq_quant_act",
+    act_bytes = nbytes["act"] + (2 * K if r["norm_step"] else 0)
+    act_gbs = act_bytes / (r["act_ms"] * 1e-3) / 1e9
+    act_roof = {"kernel": "qoq_norm_quant_act (RMSNorm)" if r["norm_step"] else "qoq_quant_act",
                 "bound": "hbm", "achieved": act_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": act_gbs / peaks["hbm_gbs"], "algorithmic_bytes_per_launch": act_bytes,
-                "ms_per_launch": act_ms, "timing": "alone, same pool, " + ("CUDA graph" if use_graph else "direct")}
+                "ms_per_launch": r["act_ms"],
+                "timing": "alone, same pool, " + ("CUDA graph" if r["use_graph"] else "direct")}
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": r["ms_per_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int8",
         "data": "synthetic (seeded splitmix64 Gaussians with outlier channels)",
         "config": config_dict(c, {
             "parallelism": f"replicas{world}" if world > 1 else "single",
-            "l2_policy": f"rotating pool of {nsets} buffer sets, {nsets * set_bytes / 1e6:.0f} MB "
-                         f"(>= 3x L2 {l2 / 1e6:.0f} MB)",
-            "step": ("qoq_norm_quant_act (RMSNorm) + qoq_w4a8_gemm" if norm_step
-                     else "qoq_quant_act + qoq_w4a8_gemm"),
-            "timing": "CUDA graph of K steps" if use_graph else "direct launches",
+            "l2_policy": r["l2_policy"],
+            "step": f"{r['quant_name']}{' (RMSNorm)' if r['norm_step'] else ''} + qoq_w4a8_gemm",
+            "timing": (f"{args.repeats} timed regions of exactly K steps each "
+                       f"({'a CUDA graph of K steps, replayed' if r['use_graph'] else 'direct launches'}); "
+                       "median region reported"),
             "mma": "tcgen05 kind::f16, exact integer operands, fp32 TMEM folded to int32"}),
-        "hbm_gb_per_s_step": world * nbytes["step"] / (ms_per_step * 1e-3) / 1e9,
+        "regions_ms_per_step": {k: [round(v, 6) for v in vs] for k, vs in r["regions"].items()},
+        "hbm_gb_per_s_step": world * nbytes["step"] / (r["ms_per_step"] * 1e-3) / 1e9,
         "roofline": roof,
         "act_roofline": act_roof,
-        "e2e": {"value": job_tops(world, ops, e2e_ms), "unit": UNIT,
+        "e2e": {"value": job_tops(world, ops, r["e2e_ms"]), "unit": UNIT,
                 "h2d_bytes_per_step": 2 * M * K, "d2h_bytes_per_step": 2 * M * N,
-                "ms_per_step": e2e_ms, "how": e2e_how,
-                "routes_ms_per_step": {"host_buffers_in_place": direct_ms, "copy_engines": copy_ms}},
+                "ms_per_step": r["e2e_ms"], "how": r["e2e_how"],
+                "routes_ms_per_step": {"host_buffers_in_place": r["direct_ms"], "copy_engines": r["copy_ms"]}},
         "clocks": clocks,
-        # per step: act-quant + GEMM; for M > 64 also the B-operand convert
+        # inside one timed region of K steps: act-quant + GEMM per step, and
+        # for M > 64 also the B-operand convert
         "gpu_launches": (2 if M <= 64 else 3) * args.steps,
-        "pack_ms": pack_ms,
+        "pack_ms": r["pack_ms"],
     }
+
+    # the other workloads of the metric, measured the same way
+    if not args.no_per_config:
+        per = {}
+        for idx, wc in synth.WORKLOADS.items():
+            cc = dict(wc)
+            if G != 128:
+                cc["g"] = G
+            if idx == args.config:
+                entry = config_summary(cc, r, args, world, peaks, peak_src)
+                entry["clocks"] = clocks
+            else:
+                smp = ClockSampler(local)
+                smp.start()
+                rr = bench_workload(q, torch, cc, args, dev, stream, dist, rank)
+                cl = smp.stop()
+                entry = config_summary(cc, rr, args, world, peaks, peak_src)
+                entry["clocks"] = cl
+            if rank == 0 and world == 1 and not args.no_cpu_baseline:
+                entry["cpu_baseline"] = oracle_step_timing(cc, args.cpu_budget_per_config, threads=0,
+                                                           n_sample=oracle_sample_channels(cc, 2e10))
+            per[cc["name"]] = entry
+        line["per_config"] = per
+
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = oracle_step_timing(c, budget_s=args.cpu_budget,
-                                                  n_sample=None if N * M * K <= 2 ** 31 else 2048)
+        line["cpu_baseline"] = cpu_baselines(c, args.cpu_budget)
     elif rank == 0:
         line["cpu_baseline"] = None
     if rank == 0:
@@ -591,19 +644,25 @@ def main() -> None:
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--repeats", type=int, default=5,
+                    help="timed regions of exactly K steps each; the median is reported (default 5)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=1, help="workload index 0..4 (default 1)")
     ap.add_argument("--g", type=int, default=128,
                     help="level-2 group size: 32, 64 or a multiple of 128 dividing K (default 128, the pages' g128)")
     ap.add_argument("--step", choices=["quant", "norm"], default="quant",
                     help="activation quantizer of the step: qoq_quant_act (default) or qoq_norm_quant_act (RMSNorm fused)")
-    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle CPU timing")
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle CPU timing (headline)")
+    ap.add_argument("--cpu-budget-per-config", type=float, default=3.0,
+                    help="seconds of oracle CPU timing per workload in per_config")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true", help="measure the headline workload only")
     ap.add_argument("--no-graph", action="store_true", help="time direct launches instead of a CUDA graph")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per GEMM launch from an ncu capture of the current library, if known")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    args.repeats = max(1, args.repeats)
     c = dict(synth.WORKLOADS[args.config])
     if args.g != 128:
         c["g"] = args.g

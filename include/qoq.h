@@ -106,15 +106,19 @@ size_t qoq_packed_weight_bytes(int N, int K, int g);
 /*
  * Bytes of device workspace that qoq_w4a8_gemm needs for (M, N, K, g)
  * (host-only; 0 for an unsupported shape).  It holds a status header and
- * the split-K state: for M <= 64 one slot per CTA of partial sums tagged with
- * the call (BN x 128 x 8 bytes, BN = 16, 32 or 64 as M needs, 160 slots);
- * for M > 64 tile counters and int32 partial sums, and an fp16 copy of Xq
- * laid out for the tensor-core B operand.
+ * the split-K state: for M <= 64 one slot per CTA of partial sums, each
+ * tagged with an epoch that the kernel keeps in the header and advances at
+ * the end of every launch (BN x 128 x 8 bytes, BN = 16, 32 or 64 as M needs,
+ * 160 slots); for M > 64 tile counters and int32 partial sums, and an fp16
+ * copy of Xq laid out for the tensor-core B operand.
  * The caller zero-fills the workspace once after allocating it (e.g.
- * cudaMemsetAsync); every call that completes leaves it fit for the next, so
- * no per-call clearing is needed.  After a call that reported
- * QOQ_ERR_DEVICE_TIMEOUT, zero-fill it again before reuse.  Two calls in
- * flight at the same time must not share one workspace.
+ * cudaMemsetAsync); every call that completes leaves it fit for the next
+ * call of any shape that it is large enough for, so no per-call clearing is
+ * needed.  This holds for launches replayed from a captured CUDA graph too:
+ * the hand-off tag comes from the device, not from the launch parameters.
+ * After a call that reported QOQ_ERR_DEVICE_TIMEOUT, zero-fill it again
+ * before reuse.  Two calls in flight at the same time must not share one
+ * workspace.
  */
 size_t qoq_gemm_workspace_bytes(int M, int N, int K, int g);
 

@@ -23,14 +23,14 @@ _BUILD = os.path.join(_HERE, "_build")
 LIB_PATH = os.path.join(_BUILD, "liboracle.so")
 _LOCK = threading.Lock()
 
-GCC_FLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math"]
+GCC_FLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-ffp-contract=off", "-fno-fast-math"]
 
 
 def compile_source(src: str, out: str) -> str:
     """gcc one C file into a shared library (portable C11, no target flags)."""
     os.makedirs(os.path.dirname(out), exist_ok=True)
     tmp = out + f".{os.getpid()}.tmp"
-    subprocess.check_call(["gcc", *GCC_FLAGS, src, "-o", tmp, "-lm"])
+    subprocess.check_call(["gcc", *GCC_FLAGS, src, "-o", tmp, "-lm", "-lpthread"])
     os.replace(tmp, out)
     return out
 
@@ -44,6 +44,14 @@ def build(force: bool = False) -> str:
 
 class OracleError(RuntimeError):
     pass
+
+
+def host_cores() -> int:
+    """Host threads this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
 
 
 def _p(a):
@@ -83,6 +91,8 @@ class Oracle:
         lib.qoq_oracle_act_quant.restype = i32
         lib.qoq_oracle_gemm.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P, P]
         lib.qoq_oracle_gemm.restype = i32
+        lib.qoq_oracle_gemm_threads.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P, P, i32]
+        lib.qoq_oracle_gemm_threads.restype = i32
         lib.qoq_oracle_gemm_entries.argtypes = [i32, P, P, i32, i32, P, P, P, P, P, P, P, P]
         lib.qoq_oracle_gemm_entries.restype = i32
         lib.qoq_oracle_norm_quant_act.argtypes = [i32, i32, i32, ctypes.c_float, P, P, P, P, P, P, P, P]
@@ -140,17 +150,23 @@ class Oracle:
         _check(self.lib.qoq_oracle_act_quant(M, K, _p(X), _p(Xq), _p(sx)), "act_quant")
         return Xq, sx
 
-    def gemm(self, Xq, sx, q4, s2, z, s1, g: int = 128, want_acc: bool = True):
-        """acc [M][N] int64 (or None) and Y [M][N] fp16 bits."""
+    def gemm(self, Xq, sx, q4, s2, z, s1, g: int = 128, want_acc: bool = True, threads: int = 1):
+        """acc [M][N] int64 (or None) and Y [M][N] fp16 bits.  threads > 1 runs
+        qoq_oracle_gemm_threads on that many host threads (0: all cores)."""
         Xq = _c(Xq, np.int8)
         q4 = _c(q4, np.uint8)
         M, K = Xq.shape
         N = q4.shape[0]
         acc = np.empty((M, N), np.int64) if want_acc else None
         Y = np.empty((M, N), np.uint16)
-        rc = _check(self.lib.qoq_oracle_gemm(M, N, K, g, _p(Xq), _p(_c(sx, np.uint16)), _p(q4),
-                                             _p(_c(s2, np.uint8)), _p(_c(z, np.uint8)),
-                                             _p(_c(s1, np.uint16)), _p(acc), _p(Y)), "gemm")
+        if threads == 0:
+            threads = host_cores()
+        args = (M, N, K, g, _p(Xq), _p(_c(sx, np.uint16)), _p(q4), _p(_c(s2, np.uint8)), _p(_c(z, np.uint8)),
+                _p(_c(s1, np.uint16)), _p(acc), _p(Y))
+        if threads == 1:
+            rc = _check(self.lib.qoq_oracle_gemm(*args), "gemm")
+        else:
+            rc = _check(self.lib.qoq_oracle_gemm_threads(*args, int(threads)), "gemm_threads")
         if rc == 2:
             raise OracleError("gemm: |acc| reached 2^31")
         return acc, Y

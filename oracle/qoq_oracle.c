@@ -41,9 +41,10 @@
  * fp16 <-> binary64 conversions below are written from the IEEE 754 binary16
  * definition (1 sign bit, 5 exponent bits with bias 15, 10 fraction bits).
  *
- * Build: gcc -O2 -std=c11 -fPIC -shared -ffp-contract=off (no fast-math).
+ * Build: gcc -O2 -std=c11 -fPIC -shared -pthread -ffp-contract=off (no fast-math).
  */
 #include <math.h>
+#include <pthread.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -272,6 +273,83 @@ int qoq_oracle_gemm(int M, int N, int K, int g, const int8_t* Xq, const uint16_t
       if (acc) acc[(size_t)m * N + n] = a;
       if (Y) Y[(size_t)m * N + n] = epilogue(a, sx[m], s1[n]);
     }
+  return rc;
+}
+
+/* The same product on several host threads, for full-size checks.  The
+ * output channels are cut into `threads` contiguous ranges, one per POSIX
+ * thread.  Per output channel n the thread first dequantizes the weight row,
+ * w8[k] = (q4[n,k] - z[n,k/g]) * s2[n,k/g] (the dequantization step, once per
+ * row instead of once per token), then sums Xq[m,k] * w8[k] over k in int64
+ * for every token m and applies the same epilogue.  Integer sums do not
+ * depend on their order, so every acc and Y equals qoq_oracle_gemm's.
+ * Returns QOQ_ORACLE_EARG for bad sizes or a failed thread start or buffer. */
+typedef struct {
+  int M, N, K, g, n0, n1, rc;
+  const int8_t* Xq;
+  const uint16_t* sx;
+  const uint8_t *q4, *s2, *z;
+  const uint16_t* s1;
+  int64_t* acc;
+  uint16_t* Y;
+} gemm_range;
+
+static void* gemm_range_run(void* arg) {
+  gemm_range* r = (gemm_range*)arg;
+  const int K = r->K, G = K / r->g;
+  int16_t* w8 = (int16_t*)malloc((size_t)K * sizeof(int16_t)); /* |w8| <= 240 */
+  if (!w8) {
+    r->rc = QOQ_ORACLE_EARG;
+    return NULL;
+  }
+  r->rc = QOQ_ORACLE_OK;
+  for (int n = r->n0; n < r->n1; ++n) {
+    const uint8_t* q4row = r->q4 + (size_t)n * K;
+    for (int k = 0; k < K; ++k)
+      w8[k] = (int16_t)qoq_oracle_dequant_code(q4row[k], r->z[(size_t)n * G + k / r->g], r->s2[(size_t)n * G + k / r->g]);
+    for (int m = 0; m < r->M; ++m) {
+      const int8_t* xrow = r->Xq + (size_t)m * K;
+      int64_t a = 0;
+      for (int k = 0; k < K; ++k) a += (int64_t)xrow[k] * w8[k];
+      if (a >= ((int64_t)1 << 31) || a < -((int64_t)1 << 31)) r->rc = QOQ_ORACLE_ERANGE;
+      if (r->acc) r->acc[(size_t)m * r->N + n] = a;
+      if (r->Y) r->Y[(size_t)m * r->N + n] = epilogue(a, r->sx[m], r->s1[n]);
+    }
+  }
+  free(w8);
+  return NULL;
+}
+
+int qoq_oracle_gemm_threads(int M, int N, int K, int g, const int8_t* Xq, const uint16_t* sx,
+                            const uint8_t* q4, const uint8_t* s2, const uint8_t* z, const uint16_t* s1,
+                            int64_t* acc, uint16_t* Y, int threads) {
+  if (M <= 0 || N <= 0 || K <= 0 || g <= 0 || K % g != 0 || !Xq || !sx || !q4 || !s2 || !z || !s1 ||
+      threads <= 0)
+    return QOQ_ORACLE_EARG;
+  if (threads > N) threads = N;
+  gemm_range* rs = (gemm_range*)calloc((size_t)threads, sizeof(gemm_range));
+  pthread_t* ts = (pthread_t*)calloc((size_t)threads, sizeof(pthread_t));
+  int* started = (int*)calloc((size_t)threads, sizeof(int));
+  int rc = QOQ_ORACLE_OK;
+  if (!rs || !ts || !started) rc = QOQ_ORACLE_EARG;
+  for (int t = 0; rc == QOQ_ORACLE_OK && t < threads; ++t) {
+    gemm_range r = {M, N, K, g, (int)((int64_t)N * t / threads), (int)((int64_t)N * (t + 1) / threads),
+                    QOQ_ORACLE_OK, Xq, sx, q4, s2, z, s1, acc, Y};
+    rs[t] = r;
+    if (pthread_create(&ts[t], NULL, gemm_range_run, &rs[t]) != 0)
+      rc = QOQ_ORACLE_EARG;
+    else
+      started[t] = 1;
+  }
+  for (int t = 0; t < threads && started; ++t)
+    if (started[t]) {
+      pthread_join(ts[t], NULL);
+      if (rs[t].rc == QOQ_ORACLE_EARG) rc = QOQ_ORACLE_EARG;
+      else if (rs[t].rc == QOQ_ORACLE_ERANGE && rc == QOQ_ORACLE_OK) rc = QOQ_ORACLE_ERANGE;
+    }
+  free(rs);
+  free(ts);
+  free(started);
   return rc;
 }
 

@@ -315,6 +315,31 @@ def check_gemm_library(o) -> None:
     assert acc.shape == (M, N)
 
 
+def check_gemm_threads(o) -> None:
+    """The multi-threaded product (output channels cut into ranges, one
+    dequantized weight row at a time) equals the single-threaded oracle and
+    numpy's int64 matmul of the dequantized weights, element for element, for
+    thread counts that divide N, do not divide it, and exceed it."""
+    M, N, K, g = 5, 44, 640, 64
+    W = synth.weights(N, K, 23)
+    X = synth.activations(M, K, 23)
+    r = o.weight_quant(synth.bits(W), g)
+    Xq, sx = o.act_quant(synth.bits(X))
+    acc1, Y1 = o.gemm(Xq, sx, r["q4"], r["s2"], r["z"], r["s1"], g)
+    w8 = o.dequant_weights(r["q4"], r["s2"], r["z"], g).astype(np.int64)
+    ref = Xq.astype(np.int64) @ w8.T
+    for threads in (2, 3, 4, 7, 44, 100):
+        acc, Y = o.gemm(Xq, sx, r["q4"], r["s2"], r["z"], r["s1"], g, threads=threads)
+        assert np.array_equal(acc, ref) and np.array_equal(acc, acc1), threads
+        assert np.array_equal(Y, Y1), threads
+    # worst-case magnitudes through the threaded path: 127 * 120 * K
+    Kw = 2048
+    r = o.weight_quant(synth.bits(np.full((3, Kw), np.float16(1.0))), 128)
+    Xq, sx = o.act_quant(synth.bits(np.full((2, Kw), np.float16(1.0))))
+    acc, _ = o.gemm(Xq, sx, r["q4"], r["s2"], r["z"], r["s1"], 128, threads=2)
+    assert (acc == 127 * 120 * Kw).all()
+
+
 def check_acc_range(o) -> None:
     """|acc| <= 127 * 127 * K stays below 2^31 for K <= 131072 (worst case)."""
     K = 1024
@@ -436,6 +461,6 @@ ALL_CHECKS = [
     check_half_to_double, check_double_to_half, check_appendix_a, check_appendix_a_g128,
     check_fig3_literal, check_level1_bruteforce, check_level2_bruteforce, check_invariants,
     check_error_bounds, check_lossless_grid, check_zero_and_underflow, check_gemm_library,
-    check_acc_range, check_norm_exact_stats, check_norm_layer_constant_row, check_norm_rms_unit_row,
+    check_gemm_threads, check_acc_range, check_norm_exact_stats, check_norm_layer_constant_row, check_norm_rms_unit_row,
     check_norm_error_bound, check_norm_quant_composition,
 ]

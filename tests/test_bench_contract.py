@@ -61,7 +61,40 @@ def test_reference_arm_json_line(bench):
     assert d["config"]["workload"] == "decode_qkv_7b"
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
+    # the reference arm times the same workload as the GPU arm, on all host cores
+    assert "full workload" in cb["sample"]
+    import oracle
+
+    assert cb["cores"] == oracle.host_cores()
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_oracle_sample_is_bounded(bench):
+    """The full workload where the product is small; otherwise a multiple of
+    128 output channels that keeps the oracle's work near the bound."""
+    from w4a8_quantized_serving_gb300 import synth
+
+    W = synth.WORKLOADS
+    assert bench.oracle_sample_channels(W[1], 2e10) == W[1]["N"]
+    n4 = bench.oracle_sample_channels(W[4], 2e10)
+    assert n4 % 128 == 0 and 128 <= n4 < W[4]["N"]
+    assert W[4]["M"] * n4 * W[4]["K"] <= 2e10
+    assert bench.oracle_sample_channels(W[4], 1.0) == 128
+
+
+def test_roofline_picks_the_binding_roof(bench):
+    """Below the ridge the GEMM is reported against HBM (algorithmic bytes per
+    launch / time), above it against the tensor peak (2MNK / time)."""
+    peaks = {"hbm_gbs": 6666.9, "bf16_tflops": 1967.3, "bf16_tflops_sustained": 1756.1}
+    r = bench.roofline_of(16, 12288, 4096, 128, 0.01, 20, peaks, "measured")
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+    assert r["achieved"] == pytest.approx(26435616 / 1e-5 / 1e9)
+    assert r["frac"] == pytest.approx(r["achieved"] / 6666.9)
+    r = bench.roofline_of(4096, 28672, 8192, 128, 1.4, 20, peaks, "measured")
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s" and r["peak"] == 1967.3
+    assert r["achieved"] == pytest.approx(2.0 * 4096 * 28672 * 8192 / 1.4e-3 / 1e12)
+    # a long timed region runs under the power cap: the sustained peak
+    assert bench.roofline_of(4096, 28672, 8192, 128, 1.4, 1000, peaks, "measured")["peak"] == 1756.1
 
 
 def _max_over_ranks_worker(rank, world, port, q):

@@ -161,10 +161,12 @@ def test_gemm_deterministic_and_workspace_reuse():
 # ------------------------------------------------------- full-size workloads --
 
 @pytest.mark.parametrize("cfg", [1, 2, 3, 4])
-def test_gemm_workload_sampled(cfg):
-    """Full-size workloads in the benchmark's launch configuration: bit-exact
-    quantization outputs, and the GEMM on sampled entries the oracle computes
-    one by one."""
+def test_gemm_workload_full(cfg):
+    """Full-size workloads in the benchmark's launch configuration, compared
+    element by element: the quantization outputs and every int32 accumulator
+    bit-exact, every fp16 Y within the tolerance.  The oracle's product runs
+    on all host threads (its threaded form is pinned to the single-threaded
+    one)."""
     c = synth.WORKLOADS[cfg]
     M, N, K = c["M"], c["N"], c["K"]
     W = synth.weights(N, K, c["seed"])
@@ -173,15 +175,93 @@ def test_gemm_workload_sampled(cfg):
     o = gc.oracle_layer(W, X, full_gemm=False)
     gc.check_weights(q(), g, o, N, K)
     gc.check_acts(g, o)
-    rng = np.random.default_rng(cfg)
-    ns = 3000
-    mi = np.concatenate([rng.integers(0, M, ns), np.full(N // 128, M - 1), np.zeros(64, np.int64)])
-    ni = np.concatenate([rng.integers(0, N, ns), np.arange(0, N, 128) + 127, np.arange(64)])
-    acc_ref, y_ref = gc.oracle.gemm_entries(mi, ni, o["Xq"], o["sx"], o["q4"], o["s2"], o["z"], o["s1"])
-    acc = g["acc"].cpu().numpy()[mi, ni]
-    Y = gc.f16_bits(g["Y"])[mi, ni]
-    assert np.array_equal(acc.astype(np.int64), acc_ref)
-    ok, rel, ab = gc.y_close(Y, y_ref)
+    del W, X
+    acc_ref, y_ref = gc.oracle.gemm(o["Xq"], o["sx"], o["q4"], o["s2"], o["z"], o["s1"], threads=0)
+    acc = g["acc"].cpu().numpy()
+    bad = acc.astype(np.int64) != acc_ref
+    assert not bad.any(), f"{int(bad.sum())} accumulators differ, first at {np.argwhere(bad)[:5].tolist()}"
+    ok, rel, ab = gc.y_close(gc.f16_bits(g["Y"]), y_ref)
+    assert ok, (rel, ab)
+
+
+# ------------------------------------------- fp32 accumulation, adversarial --
+
+def _accumulation_case(M: int, N: int, K: int, small_group):
+    """Weights and activations whose fp32 partial sums first climb into
+    [2^23, 2^24) with maximal products and then take +-1 products.
+
+    Group j of every weight row is "big" (Q8 = 119 on all 128 channels: s2 = 8,
+    z = 0, w8 = 120) unless small_group(j), where it is "small" (Q8 in {0, 1}
+    or {-1, 0}: s2 = 1, w8 = +-1).  The activations are given as codes: 127
+    on big channels (the sign alternates per token) and a fixed +-1 pattern on
+    small ones, so that a dropped +-1 changes the exact sum.  In the fp32
+    accumulator of one fold chunk (8 groups per accumulator), seven big groups
+    reach 7 * 128 * 127 * 120 = 13,655,040 units, where the fp32 spacing is 1,
+    and the small group's products then land one unit at a time."""
+    G = K // 128
+    s1 = 2.0 ** -10
+    W = np.empty((N, K), np.float64)
+    row_sign = np.where(np.arange(N) % 2 == 0, 1.0, -1.0)[:, None]
+    for j in range(G):
+        cols = slice(128 * j, 128 * j + 128)
+        if small_group(j):
+            pat = (np.arange(128) % 3 != 1).astype(np.float64)  # codes 0 / 1
+            W[:, cols] = row_sign * pat[None, :] * s1
+        else:
+            W[:, cols] = 119 * s1
+    Xq = np.empty((M, K), np.int8)
+    tok_sign = np.where(np.arange(M) % 2 == 0, 1, -1)[:, None]
+    for j in range(G):
+        cols = slice(128 * j, 128 * j + 128)
+        if small_group(j):
+            Xq[:, cols] = np.where(np.arange(128) % 4 == 1, -1, 1)[None, :]
+        else:
+            Xq[:, cols] = 127 * tok_sign
+    sx = np.full(M, 0x0400, np.uint16)  # 2^-14: Y stays well inside the fp16 range
+    return f16(W), Xq, sx
+
+
+@pytest.mark.parametrize("kernel", ["decode", "bulk"])
+def test_gemm_fp32_accumulation_large_then_unit_products(kernel):
+    """The exact-integer product runs on fp32 tensor-core accumulators, exact
+    while partial sums stay below 2^24.  Drive each accumulator's partial sums
+    to 13.7M units (past 2^23, where only integers are representable) with
+    maximal products, then add +-1 products: any truncation in the tensor
+    core's accumulation shows as a wrong int32 result.  Whole tiles only (N is
+    chosen so that every CTA takes one tile and no split-K applies), so the
+    fold chunks start at group 0: the decode kernel's four slots take groups
+    j, j + 4, ... of each 32-group chunk, the bulk kernel folds every 8
+    consecutive groups."""
+    import torch
+
+    mod = q()
+    sms = min(torch.cuda.get_device_properties(0).multi_processor_count, 160)
+    if kernel == "decode":
+        M, K = 16, 8192
+        N = 128 * sms
+        small = lambda j: j % 32 >= 28  # each slot: 7 big groups, then 1 small, per chunk
+    else:
+        M, K = 256, 4096
+        N = 128 * (sms // 2)
+        small = lambda j: j % 8 == 7    # 7 big groups, then 1 small, per chunk
+    W, Xq, sx = _accumulation_case(M, N, K, small)
+    o = gc.oracle.weight_quant(synth.bits(W), 128)
+    w8 = gc.oracle.dequant_weights(o["q4"], o["s2"], o["z"], 128)
+    assert set(np.unique(w8).tolist()) == {-1, 0, 1, 120}, "case construction"
+    acc_ref, y_ref = gc.oracle.gemm(Xq, sx, o["q4"], o["s2"], o["z"], o["s1"], threads=0)
+    packed, s1 = mod.qoq_pack_weights(gc.to_dev_f16(W))
+    t = gc.torch()
+    Xq_d = t.from_numpy(Xq).cuda()
+    sx_d = t.from_numpy(sx.view(np.float16)).cuda()
+    acc = t.empty((M, N), dtype=t.int32, device="cuda")
+    ws = t.zeros(mod.qoq_gemm_workspace_bytes(M, N, K), dtype=t.uint8, device="cuda")
+    Y = mod.qoq_w4a8_gemm(Xq_d, sx_d, packed, s1, N, acc_debug=acc, workspace=ws)
+    assert mod.qoq_last_device_status(ws) == 0
+    assert np.array_equal(gc.f16_bits(s1), o["s1"])
+    got = acc.cpu().numpy().astype(np.int64)
+    bad = got != acc_ref
+    assert not bad.any(), f"{int(bad.sum())} accumulators differ, e.g. {got[bad][:3]} vs {acc_ref[bad][:3]}"
+    ok, rel, ab = gc.y_close(gc.f16_bits(Y), y_ref)
     assert ok, (rel, ab)
 
 

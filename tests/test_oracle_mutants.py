@@ -35,6 +35,8 @@ MUTANTS = {
     "layer_no_centering": ("volatile float t = kind == 1 ? x - mu : x;", "volatile float t = x;"),
     "layer_variance_sign": ("(unsigned __int128)K * s2 - a1 * a1;", "(unsigned __int128)K * s2 + a1 * a1;"),
     "rms_mean_divisor": ("spread = s2f / (float)K;", "spread = s2f / (float)(K + 1);"),
+    "threads_range_gap": ("(int)((int64_t)N * (t + 1) / threads),", "(int)((int64_t)N * (t + 1) / threads) - (t & 1),"),
+    "threads_group_index": ("r->s2[(size_t)n * G + k / r->g]);", "r->s2[(size_t)n * G + k % G]);"),
 }
 
 

@@ -259,6 +259,21 @@ __device__ __forceinline__ void named_bar_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(NTHREADS) : "memory");
 }
 
+// Called once per CTA (one thread), after a CTA-wide barrier that follows
+// every read of the hand-off epoch in the CTA: counts the CTA out, and the
+// last CTA of the launch resets the counter and advances the epoch.  The
+// counter's acq_rel update orders each CTA's epoch reads before the last
+// CTA's advance; the next launch reads the epoch only after
+// griddepcontrol.wait, i.e. after this launch has completed.  A launch that
+// ran out of a wait limit still reaches this point in every CTA.
+__device__ __forceinline__ void advance_epoch_at_exit(const GemmParams& p) {
+  int32_t* const hdr = p.status;
+  if (atom_add_acq_rel(hdr + kWsExitWord, 1) == p.P - 1) {
+    hdr[kWsExitWord] = 0;
+    hdr[kWsEpochWord] = (int32_t)((uint32_t)hdr[kWsEpochWord] + 1u);
+  }
+}
+
 // ------------------------------------------------------------------ output --
 
 // Y[m, n] for the COLS tokens m = m0 .. m0+COLS-1 held by this thread.

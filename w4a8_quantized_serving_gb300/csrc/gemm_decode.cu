@@ -103,23 +103,30 @@ __device__ __forceinline__ int sk_cta_of(const GemmParams& p, uint32_t it) {
 // owner, the CTA holding the tile's first group: that part is the last unit
 // of its range, so it comes last in time.  Every other contributor holds a
 // later part of the tile as the first unit of its range, and stores it into
-// its own slot as {int32 partial sum, call id} pairs, which are single-copy
-// atomic: the owner reads the slots of the CTAs after it and retries only
-// while an entry does not carry this call's id yet.  No counter, fence or
-// clearing is involved.
+// its own slot as {int32 partial sum, tag} pairs, which are single-copy
+// atomic: the owner reads the slots of the CTAs after it, retries only while
+// an entry does not carry this launch's tag yet, and clears each entry it has
+// consumed.  The tag is 2 e + 1 for the epoch e in the workspace header,
+// which the last CTA of every launch advances (advance_epoch_at_exit), so a
+// launch replayed from a CUDA graph never accepts a partial sum that an
+// earlier replay left behind.  Tags are odd, so neither a cleared entry (0)
+// nor the fp16 operand copy of the bulk kernel (integer-valued halves, whose
+// lowest bit is 0) that may share the workspace can match one.
 template <int BN, int TOK>
-__device__ __forceinline__ void slot_store(const GemmParams& p, int tok0, int row, const int32_t (&run)[TOK]) {
+__device__ __forceinline__ void slot_store(const GemmParams& p, uint32_t tag, int tok0, int row,
+                                           const int32_t (&run)[TOK]) {
   unsigned long long* sl = p.sk_slot + (size_t)blockIdx.x * BN * kTileN;
-  const unsigned long long tag = (unsigned long long)p.call_id << 32;
+  const unsigned long long hi = (unsigned long long)tag << 32;
 #pragma unroll
-  for (int i = 0; i < TOK; ++i) st_relaxed_b64(sl + (tok0 + i) * kTileN + row, tag | (uint32_t)run[i]);
+  for (int i = 0; i < TOK; ++i) st_relaxed_b64(sl + (tok0 + i) * kTileN + row, hi | (uint32_t)run[i]);
 }
 
 // Pieces of 16 tokens: all 16 loads in flight at once, without holding more
 // registers than that beside the running sums.
 template <int BN, int TOK>
-__device__ __forceinline__ bool slot_gather(const GemmParams& p, int c, int tok0, int row, int32_t (&run)[TOK]) {
-  const unsigned long long* sl = p.sk_slot + (size_t)c * BN * kTileN;
+__device__ __forceinline__ bool slot_gather(const GemmParams& p, uint32_t tag, int c, int tok0, int row,
+                                            int32_t (&run)[TOK]) {
+  unsigned long long* sl = p.sk_slot + (size_t)c * BN * kTileN;
   uint64_t t0 = 0;
 #pragma unroll
   for (int piece = 0; piece < TOK; piece += 16) {
@@ -130,7 +137,7 @@ __device__ __forceinline__ bool slot_gather(const GemmParams& p, int c, int tok0
       for (int i = 0; i < 16; ++i) {
         const unsigned long long v = ld_relaxed_b64(sl + (tok0 + piece + i) * kTileN + row);
         part[i] = (int32_t)(uint32_t)v;
-        all &= (uint32_t)(v >> 32) == p.call_id;
+        all &= (uint32_t)(v >> 32) == tag;
       }
       if (all) break;
       if ((tries & 15) == 0 && !spin_ok(p, t0)) return false;
@@ -139,6 +146,19 @@ __device__ __forceinline__ bool slot_gather(const GemmParams& p, int c, int tok0
     for (int i = 0; i < 16; ++i) run[piece + i] += part[i];
   }
   return true;
+}
+
+// After the owner has written Y: clear the entries it consumed from the slots
+// of CTAs b1 .. blockIdx.x + 1, so that the workspace is left as a zero-filled
+// one for the next launch of any shape.  Done last, when the running sums are
+// dead, so that it costs no registers on the gather's path.
+template <int BN, int TOK>
+__device__ __forceinline__ void slot_clear(const GemmParams& p, int b1, int tok0, int row) {
+  for (int c = b1; c > (int)blockIdx.x; --c) {
+    unsigned long long* const z = p.sk_slot + (size_t)c * BN * kTileN + tok0 * kTileN + row;
+#pragma unroll 4
+    for (int i = 0; i < TOK; ++i) st_relaxed_b64(z + i * kTileN, 0ull);
+  }
 }
 
 template <int BN, int GPT>
@@ -342,7 +362,7 @@ __global__ void __launch_bounds__(DecCfg<BN, GPT>::THREADS, 1) gemm_decode_kerne
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue --
-    grid_dep_wait();
+    grid_dep_wait();  // also orders the epoch read after the previous launch's advance
     constexpr int TOK = BN / (C::NEPI / 4);
     static_assert(TOK % 16 == 0, "epilogue loads 16 columns at a time");
     const int e = warp - C::EPI_WARP0;
@@ -350,6 +370,7 @@ __global__ void __launch_bounds__(DecCfg<BN, GPT>::THREADS, 1) gemm_decode_kerne
     const int row = quad * 32 + lane;
     const int tok0 = (e >> 2) * TOK;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    const uint32_t tag = 2u * (uint32_t)ld_relaxed(p.status + kWsEpochWord) + 1u;  // hand-off tag
     UnitIter iter;
     iter.init(p);
     Unit u;
@@ -398,7 +419,7 @@ __global__ void __launch_bounds__(DecCfg<BN, GPT>::THREADS, 1) gemm_decode_kerne
       if (u.g0 == 0 && u.g1 == p.G) {  // whole tile
         if (ok) write_tile_out<TOK>(p, run, tok0, n);
       } else if (u.g0 > 0) {  // a later part of a split tile: its owner adds it
-        if (ok) slot_store<BN, TOK>(p, tok0, row, run);
+        if (ok) slot_store<BN, TOK>(p, tag, tok0, row, run);
       } else {  // the split tile's owner: add the parts of the CTAs after it, then write
         if (e == 0 && lane == 0) QOQ_TRACE_AT(p, 960 + 4 * (unit_no & 7) + 0, 0);
         // Last contributor first: its part is the first unit of its range and
@@ -411,12 +432,13 @@ __global__ void __launch_bounds__(DecCfg<BN, GPT>::THREADS, 1) gemm_decode_kerne
           // overlaps the gather's instead of following it (wider rows would
           // spill the prefetched scales)
           const RowScales<TOK> sc = load_row_scales<TOK>(p, tok0, n);
-          for (int c = b1; ok && c > (int)blockIdx.x; --c) ok = slot_gather<BN, TOK>(p, c, tok0, row, run);
+          for (int c = b1; ok && c > (int)blockIdx.x; --c) ok = slot_gather<BN, TOK>(p, tag, c, tok0, row, run);
           if (ok) write_tile_out<TOK>(p, run, tok0, n, sc);
         } else {
-          for (int c = b1; ok && c > (int)blockIdx.x; --c) ok = slot_gather<BN, TOK>(p, c, tok0, row, run);
+          for (int c = b1; ok && c > (int)blockIdx.x; --c) ok = slot_gather<BN, TOK>(p, tag, c, tok0, row, run);
           if (ok) write_tile_out<TOK>(p, run, tok0, n);
         }
+        if (ok) slot_clear<BN, TOK>(p, b1, tok0, row);
         if (e == 0 && lane == 0) QOQ_TRACE_AT(p, 960 + 4 * (unit_no & 7) + 2, 0);
       }
       if (e == 0 && lane == 0) QOQ_TRACE_AT(p, 640 + unit_no, 0);
@@ -429,7 +451,10 @@ __global__ void __launch_bounds__(DecCfg<BN, GPT>::THREADS, 1) gemm_decode_kerne
   if (lane == 0) QOQ_TRACE_AT(p, 700 + 2 * warp, 0);
   __syncthreads();
   if (lane == 0) QOQ_TRACE_AT(p, 701 + 2 * warp, 0);
-  if (threadIdx.x == 0) QOQ_TRACE_AT(p, 2, 0);
+  if (threadIdx.x == 0) {
+    QOQ_TRACE_AT(p, 2, 0);
+    advance_epoch_at_exit(p);  // every thread of the CTA is past its epoch read
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);

@@ -75,11 +75,19 @@ qoq_status scratch_address(void** out) {
 
 // Zeroes the first n16 16-byte words of the array: the part of the workspace
 // that the GEMM requires to start at zero (header, counters, partial sums).
+// The decode kernel's hand-off epoch and CTA exit counter (header words 2
+// and 3) are kept: every launch leaves the counter at zero and advances the
+// epoch, so partial sums that a call which ran out of its wait limit left
+// behind carry an older tag than any later call's.
 __global__ void __launch_bounds__(256) no_alloc_clear_kernel(size_t n16) {
   uint4* p = reinterpret_cast<uint4*>(g_no_alloc_scratch);
   const size_t stride = (size_t)gridDim.x * blockDim.x;
-  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride)
-    p[i] = make_uint4(0u, 0u, 0u, 0u);
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride) {
+    if (i == 0)
+      *reinterpret_cast<uint2*>(g_no_alloc_scratch) = make_uint2(0u, 0u);  // status and abort words
+    else
+      p[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -112,9 +120,16 @@ extern "C" qoq_status qoq_w4a8_gemm_no_alloc(int M, int N, int K, int g, const i
   const size_t n16 = zero_bytes / 16;
   size_t blocks = (n16 + 255) / 256;
   if (blocks > 1024) blocks = 1024;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  no_alloc_clear_kernel<<<(unsigned)blocks, 256, 0, s>>>(n16);
-  if (cudaGetLastError() != cudaSuccess) return QOQ_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(256);
+  cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+  // The launch's own return code: an error left pending by unrelated work is
+  // neither reported as this call's nor cleared here.
+  if (cudaLaunchKernelEx(&cfg, no_alloc_clear_kernel, n16) != cudaSuccess) {
+    cudaGetLastError();  // clear the launch's own (non-sticky) error, as qoq_w4a8_gemm does
+    return QOQ_ERR_CUDA;
+  }
 
   return qoq_w4a8_gemm(M, N, K, g, Xq, sx_f16, packed, s1_f16, Y_f16, acc_debug, scratch,
                        QOQ_NO_ALLOC_SCRATCH_BYTES, stream);

@@ -30,7 +30,12 @@ constexpr int kFoldGroups = 8;     // fp32 TMEM partials are folded to int32 eve
 constexpr int kMaxSkTiles = 512;   // upper bound of split-K tiles per call (workspace sizing)
 constexpr int kMaxGrid = 160;      // upper bound of persistent CTAs per call (GB300: 152 SMs)
 
-constexpr int kWsHeaderBytes = 256;  // [0] sticky status, [1] id of a call that aborted
+// Workspace header, 32-bit words: [0] sticky status, [1] id of a call that
+// aborted, [2] hand-off epoch of the decode kernel (advanced by the last CTA
+// of every decode launch), [3] that kernel's CTA exit counter.
+constexpr int kWsHeaderBytes = 256;
+constexpr int kWsEpochWord = 2;
+constexpr int kWsExitWord = 3;
 
 // Token-tile width (MMA N) used for a given M.
 inline int gemm_bn_for_m(int M) {
@@ -44,7 +49,7 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Workspace partition for (M, N, K); device independent.
 //   token tiles of <= 64 (one tile): header, then one split-K slot per CTA
-//     ([BN][128] entries of {int32 partial sum, uint32 call id});
+//     ([BN][128] entries of {int32 partial sum, uint32 epoch tag});
 //   128-token tiles: header, split-K tile counters, int32 partial tiles, and
 //     the fp16 B-operand copy of Xq.
 // zero_bytes: the prefix that must be zero before the first call.
@@ -80,7 +85,9 @@ inline WsLayout gemm_ws_layout(int M, int N, int K) {
 // Split-K state lives in the workspace.  128-token tiles: int32 sums and
 // counts that every completed call leaves zeroed (the last contributor clears
 // them).  Decode tiles: each CTA's slot holds its partial sums tagged with the
-// call id, so stale slots never need clearing.
+// launch's epoch, read from the workspace header on the device (so a launch
+// replayed from a CUDA graph gets a fresh tag too); the owner that consumes
+// a slot clears it.
 // Tiles [0, T_dp) are processed whole, round-robin over the P CTAs; the
 // remaining T_sk tiles are split along K: their T_sk * G group-iterations are
 // cut into P equal contiguous ranges (stream-K), and partial int32 sums meet
@@ -95,14 +102,14 @@ struct GemmParams {
   int32_t* acc_debug;
   int32_t* sk_acc;  // [T_sk][BN][128]  (128-token tiles)
   int32_t* sk_cnt;  // [T_sk]           (128-token tiles)
-  unsigned long long* sk_slot;  // [P][BN][128] {int32 partial, uint32 call id} (decode tiles)
+  unsigned long long* sk_slot;  // [P][BN][128] {int32 partial, uint32 epoch tag} (decode tiles)
   int* status;      // workspace header
   int M, N, K, G, MT, NT, T, T_dp, T_sk, P;  // G: k-tiles (K / 128)
   int gpt;                                    // scale sets per k-tile (the kernel's template argument)
   uint32_t I_sk;  // T_sk * G <= 511 * 1024, so 32-bit schedule arithmetic suffices
   unsigned long long timeout_ns;
   int fault;
-  unsigned call_id;           // non-zero, distinct per call: the abort word names the aborting call
+  unsigned call_id;           // non-zero: the abort word names the aborting call (not a hand-off tag)
   unsigned long long* trace;  // per-CTA event clock, only with -DQOQ_TRACE (else unused)
 };
 
