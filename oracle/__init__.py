@@ -93,6 +93,8 @@ class Oracle:
         lib.qoq_oracle_gemm.restype = i32
         lib.qoq_oracle_gemm_threads.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P, P, i32]
         lib.qoq_oracle_gemm_threads.restype = i32
+        lib.qoq_oracle_gemm_zero_folded.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P, P, P]
+        lib.qoq_oracle_gemm_zero_folded.restype = i32
         lib.qoq_oracle_gemm_entries.argtypes = [i32, P, P, i32, i32, P, P, P, P, P, P, P, P]
         lib.qoq_oracle_gemm_entries.restype = i32
         lib.qoq_oracle_norm_quant_act.argtypes = [i32, i32, i32, ctypes.c_float, P, P, P, P, P, P, P, P]
@@ -171,6 +173,24 @@ class Oracle:
             raise OracleError("gemm: |acc| reached 2^31")
         return acc, Y
 
+    def gemm_zero_folded(self, Xq, sx, q4, s2, z, s1, g: int = 128):
+        """The product in its zero-point-folded form: returns (acc [M][N] int64,
+        Y [M][N] fp16 bits, RS [M][K/g] int64 per-group row sums of Xq)."""
+        Xq = _c(Xq, np.int8)
+        q4 = _c(q4, np.uint8)
+        M, K = Xq.shape
+        N = q4.shape[0]
+        acc = np.empty((M, N), np.int64)
+        Y = np.empty((M, N), np.uint16)
+        RS = np.empty((M, K // g), np.int64)
+        rc = _check(self.lib.qoq_oracle_gemm_zero_folded(M, N, K, g, _p(Xq), _p(_c(sx, np.uint16)), _p(q4),
+                                                         _p(_c(s2, np.uint8)), _p(_c(z, np.uint8)),
+                                                         _p(_c(s1, np.uint16)), _p(RS), _p(acc), _p(Y)),
+                    "gemm_zero_folded")
+        if rc == 2:
+            raise OracleError("gemm_zero_folded: |acc| reached 2^31")
+        return acc, Y, RS
+
     def gemm_entries(self, m_idx, n_idx, Xq, sx, q4, s2, z, s1, g: int = 128):
         """acc and Y for the listed (m, n) entries only."""
         m_idx = _c(m_idx, np.int32)
@@ -225,6 +245,7 @@ def default() -> Oracle:
 def __getattr__(name):
     # module-level shortcuts: oracle.weight_quant(...) etc. use the default build
     if name in ("half_to_double", "double_to_half", "dequant_code", "dequant_real", "weight_quant",
-                "dequant_weights", "act_quant", "gemm", "gemm_entries", "norm_quant_act"):
+                "dequant_weights", "act_quant", "gemm", "gemm_entries", "norm_quant_act",
+                "gemm_zero_folded"):
         return getattr(default(), name)
     raise AttributeError(name)

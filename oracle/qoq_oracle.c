@@ -276,6 +276,51 @@ int qoq_oracle_gemm(int M, int N, int K, int g, const int8_t* Xq, const uint16_t
   return rc;
 }
 
+/* Zero-point folding (QFactory notes, papercache.org, section 4.3 "mapping
+ * function transformation", Table 2: a matmul whose operand carries an
+ * offset is rewritten as the plain product plus a product with the all-ones
+ * matrix J, whose rows are the reduction's sums).  The weights of group j of
+ * row n are w8 = s2 q4 - zs with zs = z s2, so
+ *   acc[m,n] = sum_k Xq[m,k] (q4[n,k] s2[n,k/g])  -  sum_j zs[n,j] RS[m,j],
+ *   RS[m,j]  = sum over the g channels k of group j of Xq[m,k]  (Xq times J),
+ * all in int64, then the same epilogue as qoq_oracle_gemm.  The steps are
+ * taken in that order: row sums, the scale-only product, the correction.
+ * rowsum (nullable) receives RS [M][K/g].  Equal to qoq_oracle_gemm's acc by
+ * distributivity; the tests check that and a hand-worked example. */
+int qoq_oracle_gemm_zero_folded(int M, int N, int K, int g, const int8_t* Xq, const uint16_t* sx,
+                                const uint8_t* q4, const uint8_t* s2, const uint8_t* z, const uint16_t* s1,
+                                int64_t* rowsum, int64_t* acc, uint16_t* Y) {
+  if (M <= 0 || N <= 0 || K <= 0 || g <= 0 || K % g != 0 || !Xq || !sx || !q4 || !s2 || !z || !s1)
+    return QOQ_ORACLE_EARG;
+  const int G = K / g;
+  int64_t* RS = (int64_t*)malloc((size_t)M * G * sizeof(int64_t));
+  if (!RS) return QOQ_ORACLE_EARG;
+  for (int m = 0; m < M; ++m)
+    for (int j = 0; j < G; ++j) {
+      int64_t t = 0;
+      for (int k = j * g; k < (j + 1) * g; ++k) t += Xq[(size_t)m * K + k];
+      RS[(size_t)m * G + j] = t;
+    }
+  int rc = QOQ_ORACLE_OK;
+  for (int m = 0; m < M; ++m)
+    for (int n = 0; n < N; ++n) {
+      const int8_t* xrow = Xq + (size_t)m * K;
+      const uint8_t* qrow = q4 + (size_t)n * K;
+      int64_t scaled = 0;
+      for (int k = 0; k < K; ++k) scaled += (int64_t)xrow[k] * ((int64_t)qrow[k] * s2[(size_t)n * G + k / g]);
+      int64_t corr = 0;
+      for (int j = 0; j < G; ++j)
+        corr += ((int64_t)z[(size_t)n * G + j] * s2[(size_t)n * G + j]) * RS[(size_t)m * G + j];
+      const int64_t a = scaled - corr;
+      if (a >= ((int64_t)1 << 31) || a < -((int64_t)1 << 31)) rc = QOQ_ORACLE_ERANGE;
+      if (acc) acc[(size_t)m * N + n] = a;
+      if (Y) Y[(size_t)m * N + n] = epilogue(a, sx[m], s1[n]);
+    }
+  if (rowsum) memcpy(rowsum, RS, (size_t)M * G * sizeof(int64_t));
+  free(RS);
+  return rc;
+}
+
 /* The same product on several host threads, for full-size checks.  The
  * output channels are cut into `threads` contiguous ranges, one per POSIX
  * thread.  Per output channel n the thread first dequantizes the weight row,

@@ -340,6 +340,57 @@ def check_gemm_threads(o) -> None:
     assert (acc == 127 * 120 * Kw).all()
 
 
+def check_zero_folded_appendix(o) -> None:
+    """The zero-point-folded product on the hand-worked example: the per-group
+    row sums and the total, as worked by hand in the golden file."""
+    gold = load_golden("appendix_a_g4.txt")
+    zf = load_golden("appendix_a_zero_folded_g4.txt")
+    g = gold["g"]
+    W, X = _appendix_inputs(gold)
+    r = o.weight_quant(synth.bits(W), g)
+    Xq, sx = o.act_quant(synth.bits(X))
+    acc, Y, RS = o.gemm_zero_folded(Xq, sx, r["q4"], r["s2"], r["z"], r["s1"], g)
+    assert RS[0].tolist() == zf["RS"]
+    assert (r["z"][0].astype(int) * r["s2"][0]).tolist() == zf["zs"]
+    assert int(acc[0, 0]) == zf["acc"] == sum(zf["scaled"]) - sum(zf["correction"])
+    assert int(Y[0, 0]) == gold["Y_bits"]
+    # embedded at g = 128: the same numbers
+    W1, X1 = _appendix_inputs(gold, K=256, embed=True)
+    r = o.weight_quant(synth.bits(np.repeat(W1, 128, axis=0)), 128)
+    Xq, sx = o.act_quant(synth.bits(X1))
+    acc, Y, RS = o.gemm_zero_folded(Xq, sx, r["q4"], r["s2"], r["z"], r["s1"], 128)
+    assert RS[0].tolist() == zf["RS"] and (acc == zf["acc"]).all() and (Y == gold["Y_bits"]).all()
+
+
+def check_zero_folded_equals_direct(o) -> None:
+    """Distributivity: the folded form equals the direct product of the
+    dequantized weights for every group size, including codes and zeros at
+    their extremes; row sums equal numpy's per-group sums."""
+    rng = np.random.default_rng(31)
+    for g in (32, 64, 128, 256):
+        M, N, K = 3, 20, 512
+        W = synth.weights(N, K, 40 + g)
+        X = synth.activations(M, K, 40 + g)
+        W[:8] = np.tile(_adversarial_weights()[:8], (1, K // 256))  # constant, zero, alternating, tiny rows
+        r = o.weight_quant(synth.bits(W), g)
+        Xq, sx = o.act_quant(synth.bits(X))
+        acc0, Y0 = o.gemm(Xq, sx, r["q4"], r["s2"], r["z"], r["s1"], g)
+        acc, Y, RS = o.gemm_zero_folded(Xq, sx, r["q4"], r["s2"], r["z"], r["s1"], g)
+        assert np.array_equal(acc, acc0) and np.array_equal(Y, Y0), g
+        assert np.array_equal(RS, Xq.astype(np.int64).reshape(M, K // g, g).sum(axis=2)), g
+    # raw codes and zero points at their extremes (not produced by the quantizer)
+    M, N, K, g = 2, 5, 256, 128
+    q4 = rng.integers(0, 16, (N, K)).astype(np.uint8)
+    s2 = rng.integers(1, 17, (N, K // g)).astype(np.uint8)
+    z = rng.integers(0, 16, (N, K // g)).astype(np.uint8)
+    Xq = rng.integers(-127, 128, (M, K)).astype(np.int8)
+    sx = np.full(M, 0x2000, np.uint16)
+    s1 = np.full(N, 0x1000, np.uint16)
+    acc0, _ = o.gemm(Xq, sx, q4, s2, z, s1, g)
+    acc, _, _ = o.gemm_zero_folded(Xq, sx, q4, s2, z, s1, g)
+    assert np.array_equal(acc, acc0)
+
+
 def check_acc_range(o) -> None:
     """|acc| <= 127 * 127 * K stays below 2^31 for K <= 131072 (worst case)."""
     K = 1024
@@ -461,6 +512,6 @@ ALL_CHECKS = [
     check_half_to_double, check_double_to_half, check_appendix_a, check_appendix_a_g128,
     check_fig3_literal, check_level1_bruteforce, check_level2_bruteforce, check_invariants,
     check_error_bounds, check_lossless_grid, check_zero_and_underflow, check_gemm_library,
-    check_gemm_threads, check_acc_range, check_norm_exact_stats, check_norm_layer_constant_row, check_norm_rms_unit_row,
+    check_gemm_threads, check_zero_folded_appendix, check_zero_folded_equals_direct, check_acc_range, check_norm_exact_stats, check_norm_layer_constant_row, check_norm_rms_unit_row,
     check_norm_error_bound, check_norm_quant_composition,
 ]

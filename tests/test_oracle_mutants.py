@@ -35,6 +35,11 @@ MUTANTS = {
     "layer_no_centering": ("volatile float t = kind == 1 ? x - mu : x;", "volatile float t = x;"),
     "layer_variance_sign": ("(unsigned __int128)K * s2 - a1 * a1;", "(unsigned __int128)K * s2 + a1 * a1;"),
     "rms_mean_divisor": ("spread = s2f / (float)K;", "spread = s2f / (float)(K + 1);"),
+    "folded_correction_sign": ("const int64_t a = scaled - corr;", "const int64_t a = scaled + corr;"),
+    "folded_zero_without_scale": ("corr += ((int64_t)z[(size_t)n * G + j] * s2[(size_t)n * G + j]) * RS[(size_t)m * G + j];",
+                                  "corr += (int64_t)z[(size_t)n * G + j] * RS[(size_t)m * G + j];"),
+    "folded_rowsum_range": ("for (int k = j * g; k < (j + 1) * g; ++k) t += Xq[(size_t)m * K + k];",
+                            "for (int k = j * g; k < (j + 1) * g - 1; ++k) t += Xq[(size_t)m * K + k];"),
     "threads_range_gap": ("(int)((int64_t)N * (t + 1) / threads),", "(int)((int64_t)N * (t + 1) / threads) - (t & 1),"),
     "threads_group_index": ("r->s2[(size_t)n * G + k / r->g]);", "r->s2[(size_t)n * G + k % G]);"),
 }
