@@ -350,9 +350,10 @@ def bench_workload(q, torch, c: dict, args, dev, stream, dist, rank: int) -> dic
         else:
             q.qoq_quant_act(src, Xq=s["Xq"], sx=s["sx"])
 
+    gemm_call = q.qoq_w4a8_gemm_zero_folded if args.variant == "zero_folded" else q.qoq_w4a8_gemm
+
     def gemm(s, Y=None):
-        q.qoq_w4a8_gemm(s["Xq"], s["sx"], s["packed"], s["s1"], N, g=G, Y=s["Y"] if Y is None else Y,
-                        workspace=s["ws"])
+        gemm_call(s["Xq"], s["sx"], s["packed"], s["s1"], N, g=G, Y=s["Y"] if Y is None else Y, workspace=s["ws"])
 
     def steps_full(n: int):
         for i in range(n):
@@ -589,7 +590,9 @@ def run_ours(args, c: dict) -> None:
             "timing": (f"{args.repeats} timed regions of exactly K steps each "
                        f"({'a CUDA graph of K steps, replayed' if r['use_graph'] else 'direct launches'}); "
                        "median region reported"),
-            "mma": "tcgen05 kind::f16, exact integer operands, fp32 TMEM folded to int32"}),
+            "mma": "tcgen05 kind::f16, exact integer operands, fp32 TMEM folded to int32",
+            "variant": ("qoq_w4a8_gemm_zero_folded (q4*s2 in the main loop, zero points' share subtracted in "
+                        "the epilogue)" if args.variant == "zero_folded" else "qoq_w4a8_gemm")}),
         "regions_ms_per_step": {k: [round(v, 6) for v in vs] for k, vs in r["regions"].items()},
         "hbm_gb_per_s_step": world * nbytes["step"] / (r["ms_per_step"] * 1e-3) / 1e9,
         "roofline": roof,
@@ -601,7 +604,7 @@ def run_ours(args, c: dict) -> None:
         "clocks": clocks,
         # inside one timed region of K steps: act-quant + GEMM per step, and
         # for M > 64 also the B-operand convert
-        "gpu_launches": (2 if M <= 64 else 3) * args.steps,
+        "gpu_launches": ((2 if M <= 64 else 3) + (1 if args.variant == "zero_folded" else 0)) * args.steps,
         "pack_ms": r["pack_ms"],
     }
 
@@ -652,6 +655,8 @@ def main() -> None:
                     help="level-2 group size: 32, 64 or a multiple of 128 dividing K (default 128, the pages' g128)")
     ap.add_argument("--step", choices=["quant", "norm"], default="quant",
                     help="activation quantizer of the step: qoq_quant_act (default) or qoq_norm_quant_act (RMSNorm fused)")
+    ap.add_argument("--variant", choices=["direct", "zero_folded"], default="direct",
+                    help="GEMM entry point: qoq_w4a8_gemm (default) or qoq_w4a8_gemm_zero_folded")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle CPU timing (headline)")
     ap.add_argument("--cpu-budget-per-config", type=float, default=3.0,
                     help="seconds of oracle CPU timing per workload in per_config")

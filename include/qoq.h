@@ -110,7 +110,8 @@ size_t qoq_packed_weight_bytes(int N, int K, int g);
  * tagged with an epoch that the kernel keeps in the header and advances at
  * the end of every launch (BN x 128 x 8 bytes, BN = 16, 32 or 64 as M needs,
  * 160 slots); for M > 64 tile counters and int32 partial sums, and an fp16
- * copy of Xq laid out for the tensor-core B operand.
+ * copy of Xq laid out for the tensor-core B operand; and, for
+ * qoq_w4a8_gemm_zero_folded, int32 row sums of Xq per 128-channel k-tile.
  * The caller zero-fills the workspace once after allocating it (e.g.
  * cudaMemsetAsync); every call that completes leaves it fit for the next
  * call of any shape that it is large enough for, so no per-call clearing is
@@ -214,6 +215,29 @@ qoq_status qoq_w4a8_gemm(int M, int N, int K, int g, const int8_t* Xq, const uin
                          const uint8_t* packed, const uint16_t* s1_f16, uint16_t* Y_f16,
                          int32_t* acc_debug, void* workspace, size_t ws_bytes,
                          qoq_stream_t stream);
+
+/*
+ * The same GEMM with the zero points folded out of the main loop (QFactory
+ * notes, papercache.org, section 4.3 "mapping function transformation",
+ * Table 2: a matmul whose operand carries an offset becomes the offset-free
+ * product plus a product with the all-ones matrix J, whose rows are sums
+ * over the reduction).  With zs = z * s2 per (row, group) and the per-group
+ * row sums RS[m, j] = sum of Xq[m, k] over the channels k of group j:
+ *   acc[m,n] = sum_k Xq[m,k] * (q4[n,k] * s2[n,k/g])  -  sum_j zs[n,j] * RS[m,j],
+ * which equals qoq_w4a8_gemm's acc exactly (integer distributivity); Y as
+ * there.  The tensor cores see q4 * s2 (no zero point per weight); a
+ * pre-pass kernel writes RS into the workspace, and the epilogue subtracts
+ * the zs * RS terms.
+ * Arguments, results, workspace (qoq_gemm_workspace_bytes covers it) and
+ * errors as qoq_w4a8_gemm, except that the group size must be a multiple of
+ * 128 (g = 32 or 64 return QOQ_ERR_UNSUPPORTED).  Launches: the row-sum
+ * pre-pass, then (M > 64) the B-operand copy, then the GEMM, all with
+ * programmatic dependent launch.
+ */
+qoq_status qoq_w4a8_gemm_zero_folded(int M, int N, int K, int g, const int8_t* Xq,
+                                     const uint16_t* sx_f16, const uint8_t* packed,
+                                     const uint16_t* s1_f16, uint16_t* Y_f16, int32_t* acc_debug,
+                                     void* workspace, size_t ws_bytes, qoq_stream_t stream);
 
 /*
  * qoq_w4a8_gemm without a caller-supplied workspace.  The paper has no

@@ -14,7 +14,7 @@ _EXPORTS = (
     "qoq_gemm_workspace_bytes", "qoq_last_device_status", "qoq_pack_weights",
     "qoq_norm_quant_act", "qoq_packed_weight_bytes", "qoq_quant_act", "qoq_set_debug", "qoq_status_str",
     "qoq_unpack_weights_debug", "qoq_version", "qoq_w4a8_gemm", "qoq_w4a8_gemm_no_alloc",
-    "workspace_for",
+    "qoq_w4a8_gemm_zero_folded", "workspace_for",
 )
 
 __all__ = list(_EXPORTS)

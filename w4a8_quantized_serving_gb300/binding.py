@@ -22,7 +22,7 @@ QOQ_ERRORS = {
 EXPORTED = (
     "qoq_status_str", "qoq_version", "qoq_packed_weight_bytes", "qoq_gemm_workspace_bytes",
     "qoq_pack_weights", "qoq_quant_act", "qoq_norm_quant_act", "qoq_w4a8_gemm", "qoq_unpack_weights_debug",
-    "qoq_last_device_status", "qoq_set_debug", "qoq_w4a8_gemm_no_alloc",
+    "qoq_last_device_status", "qoq_set_debug", "qoq_w4a8_gemm_no_alloc", "qoq_w4a8_gemm_zero_folded",
 )
 
 _LOCK = threading.Lock()
@@ -69,6 +69,8 @@ def lib() -> ctypes.CDLL:
             L.qoq_norm_quant_act.restype = i32
             L.qoq_w4a8_gemm.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P, sz, P]
             L.qoq_w4a8_gemm.restype = i32
+            L.qoq_w4a8_gemm_zero_folded.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P, sz, P]
+            L.qoq_w4a8_gemm_zero_folded.restype = i32
             L.qoq_w4a8_gemm_no_alloc.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P]
             L.qoq_w4a8_gemm_no_alloc.restype = i32
             L.qoq_unpack_weights_debug.argtypes = [i32, i32, i32, P, P, P, P, P]
@@ -205,6 +207,18 @@ def qoq_w4a8_gemm(Xq, sx, packed, s1, N: int | None = None, g: int = 128, Y=None
                   workspace=None, stream=None):
     """Y fp16 [M][N] = W4A8 GEMM of (Xq, sx) with the packed weights (and s1).
     Y may be a pinned host tensor: the kernel writes it in place."""
+    return _gemm("qoq_w4a8_gemm", Xq, sx, packed, s1, N, g, Y, acc_debug, workspace, stream)
+
+
+def qoq_w4a8_gemm_zero_folded(Xq, sx, packed, s1, N: int | None = None, g: int = 128, Y=None, acc_debug=None,
+                              workspace=None, stream=None):
+    """The same GEMM with the zero points folded into the epilogue (q4 * s2 in
+    the main loop, minus z * s2 times the per-group row sums of Xq); g must be
+    a multiple of 128."""
+    return _gemm("qoq_w4a8_gemm_zero_folded", Xq, sx, packed, s1, N, g, Y, acc_debug, workspace, stream)
+
+
+def _gemm(name, Xq, sx, packed, s1, N, g, Y, acc_debug, workspace, stream):
     torch = _torch()
     M, K = Xq.shape
     if N is None:
@@ -215,11 +229,11 @@ def qoq_w4a8_gemm(Xq, sx, packed, s1, N: int | None = None, g: int = 128, Y=None
     if workspace is None:  # zero-filled once; every completed call leaves it zeroed
         workspace = torch.zeros(max(ws_need, 16), dtype=torch.uint8, device=Xq.device)
     acc_ptr = None if acc_debug is None else _dev(acc_debug, torch.int32, "acc_debug", (M, N))
-    code = lib().qoq_w4a8_gemm(M, N, K, g, _dev(Xq, torch.int8, "Xq"), _dev(sx, torch.float16, "sx", (M,)),
-                               _dev(packed, torch.uint8, "packed"), _dev(s1, torch.float16, "s1", (N,)),
-                               _dev(Y, torch.float16, "Y", (M, N), host_ok=True), acc_ptr,
-                               _dev(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream))
-    _check(code, "qoq_w4a8_gemm")
+    code = getattr(lib(), name)(M, N, K, g, _dev(Xq, torch.int8, "Xq"), _dev(sx, torch.float16, "sx", (M,)),
+                                _dev(packed, torch.uint8, "packed"), _dev(s1, torch.float16, "s1", (N,)),
+                                _dev(Y, torch.float16, "Y", (M, N), host_ok=True), acc_ptr,
+                                _dev(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream))
+    _check(code, name)
     return Y
 
 

@@ -136,13 +136,17 @@ qoq_status qoq_norm_quant_act(int M, int K, int kind, float eps, const uint16_t*
                                           reinterpret_cast<cudaStream_t>(stream)));
 }
 
-qoq_status qoq_w4a8_gemm(int M, int N, int K, int g, const int8_t* Xq, const uint16_t* sx_f16,
-                         const uint8_t* packed, const uint16_t* s1_f16, uint16_t* Y_f16,
-                         int32_t* acc_debug, void* workspace, size_t ws_bytes,
-                         qoq_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The two GEMM entry points share their checks and launch path.
+qoq_status gemm_entry(int M, int N, int K, int g, const int8_t* Xq, const uint16_t* sx_f16,
+                      const uint8_t* packed, const uint16_t* s1_f16, uint16_t* Y_f16, int32_t* acc_debug,
+                      void* workspace, size_t ws_bytes, qoq_stream_t stream, bool zero_folded) {
   if (!Xq || !sx_f16 || !packed || !s1_f16 || !Y_f16) return QOQ_ERR_NULL;
   if (!shape_ok_mk(M, K) || !shape_ok_nk(N, K)) return QOQ_ERR_SHAPE;
-  if (!qoq::group_size_ok(K, g)) return QOQ_ERR_UNSUPPORTED;
+  if (!qoq::group_size_ok(K, g) || (zero_folded && g < kGroup)) return QOQ_ERR_UNSUPPORTED;
   if (!aligned16(Xq) || !aligned16(sx_f16) || !aligned16(packed) || !aligned16(s1_f16) ||
       !aligned16(Y_f16) || (acc_debug && !aligned16(acc_debug)))
     return QOQ_ERR_MISALIGNED;
@@ -156,8 +160,26 @@ qoq_status qoq_w4a8_gemm(int M, int N, int K, int g, const int8_t* Xq, const uin
   unsigned call_id = g_call_id.fetch_add(1) + 1;
   if (call_id == 0) call_id = g_call_id.fetch_add(1) + 1;  // skip 0 on wrap-around
   return from_cuda(qoq::launch_gemm(M, N, K, g, Xq, sx_f16, packed, s1_f16, Y_f16, acc_debug, workspace,
-                                    sms, tmo, g_fault.load(), call_id, g_trace.load(),
+                                    sms, tmo, g_fault.load(), call_id, g_trace.load(), zero_folded,
                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+qoq_status qoq_w4a8_gemm(int M, int N, int K, int g, const int8_t* Xq, const uint16_t* sx_f16,
+                         const uint8_t* packed, const uint16_t* s1_f16, uint16_t* Y_f16,
+                         int32_t* acc_debug, void* workspace, size_t ws_bytes,
+                         qoq_stream_t stream) {
+  return gemm_entry(M, N, K, g, Xq, sx_f16, packed, s1_f16, Y_f16, acc_debug, workspace, ws_bytes, stream, false);
+}
+
+qoq_status qoq_w4a8_gemm_zero_folded(int M, int N, int K, int g, const int8_t* Xq, const uint16_t* sx_f16,
+                                     const uint8_t* packed, const uint16_t* s1_f16, uint16_t* Y_f16,
+                                     int32_t* acc_debug, void* workspace, size_t ws_bytes,
+                                     qoq_stream_t stream) {
+  return gemm_entry(M, N, K, g, Xq, sx_f16, packed, s1_f16, Y_f16, acc_debug, workspace, ws_bytes, stream, true);
 }
 
 qoq_status qoq_unpack_weights_debug(int N, int K, int g, const uint8_t* packed, uint8_t* q4,

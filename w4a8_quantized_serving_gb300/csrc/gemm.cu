@@ -65,7 +65,8 @@ struct BulkCfg {
   static_assert(SMEM_BYTES <= kSmemBudget, "shared memory");
 };
 
-template <int GPT>
+// ZF: the zero-point-folded variant (see zero_point_share).
+template <int GPT, bool ZF>
 __global__ void __launch_bounds__(BulkCfg<GPT>::THREADS, 1) gemm_bulk_kernel(const __grid_constant__ GemmParams p) {
   using C = BulkCfg<GPT>;
   constexpr int BN = C::BN;
@@ -175,7 +176,7 @@ __global__ void __launch_bounds__(BulkCfg<GPT>::THREADS, 1) gemm_bulk_kernel(con
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer --
     grid_dep_wait();
-    mma_role<BN, C::NACC, C::NABUF, C::ACOL0>(
+    mma_role<BN, C::NACC, C::NABUF, C::ACOL0, ZF ? kFoldGroupsZf : kFoldGroups>(
         p, tmem, bar_afull, bar_aempty, bar_accfull, bar_accempty, bar_drain,
         [&](uint32_t gi, int) { return sbase + (uint32_t)((gi % C::STAGES) * C::B_BYTES); },
         [&](uint32_t gi) { return bar_empty + 8 * (gi % C::STAGES); });
@@ -206,12 +207,12 @@ __global__ void __launch_bounds__(BulkCfg<GPT>::THREADS, 1) gemm_bulk_kernel(con
         }
         tc_fence_after();  // the MMAs that read this A buffer are complete
         const uint8_t* wt = smem + C::W_OFF + s * C::TILE;
-        DequantConsts k = dequant_consts(wt[row], wt[128 + row]);
+        DequantConsts k = dequant_consts(wt[row], ZF ? 0u : wt[128 + row]);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           if (GPT > 1 && c > 0 && c % (4 / GPT) == 0) {  // scale set u covers chunks u * 4 / GPT ..
             const int u = c / (4 / GPT);
-            k = dequant_consts(wt[u * 256 + row], wt[u * 256 + 128 + row]);
+            k = dequant_consts(wt[u * 256 + row], ZF ? 0u : wt[u * 256 + 128 + row]);
           }
           uint32_t out[16];
           dequant_chunk(*reinterpret_cast<const uint4*>(wt + C::NIB + c * kWChunkBytes + row * 16), k, out);
@@ -229,8 +230,8 @@ __global__ void __launch_bounds__(BulkCfg<GPT>::THREADS, 1) gemm_bulk_kernel(con
   } else {
     // ------------------------------------------------------------ epilogue --
     grid_dep_wait();
-    epilogue_role<BN, C::NEPI, C::NACC>(p, tmem, C::EPI_WARP0, bar_accfull, bar_accempty,
-                                        reinterpret_cast<volatile int*>(smem + C::FLAG_OFF));
+    epilogue_role<BN, C::NEPI, C::NACC, ZF, C::TILE>(p, tmem, C::EPI_WARP0, bar_accfull, bar_accempty,
+                                                     reinterpret_cast<volatile int*>(smem + C::FLAG_OFF));
   }
 
   tc_fence_before();
@@ -263,7 +264,33 @@ __global__ void __launch_bounds__(256) convert_kernel(const ConvertParams c) {
   }
 }
 
-template <int GPT>
+// Row sums of Xq per 128-channel k-tile, RS[j][m] (0 for M <= m < rs_ld),
+// for the zero-point-folded variant.  One thread per (j, m): 128 bytes read,
+// summed four signed bytes at a time.
+__global__ void __launch_bounds__(256) rowsum_kernel(const RowSumParams r) {
+  grid_dep_launch_dependents();  // the GEMM may launch and start streaming weights
+  grid_dep_wait();               // Xq comes from the preceding kernel
+  const long long total = (long long)(r.K / kGroup) * r.rs_ld;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += stride) {
+    const int j = (int)(idx / r.rs_ld), m = (int)(idx % r.rs_ld);
+    int sum = 0;
+    if (m < r.M) {
+      const uint4* x = reinterpret_cast<const uint4*>(r.Xq + (size_t)m * r.K + (size_t)j * kGroup);
+#pragma unroll
+      for (int q = 0; q < kGroup / 16; ++q) {
+        const uint4 v = __ldcg(x + q);
+        sum = __dp4a((int)v.x, 0x01010101, sum);
+        sum = __dp4a((int)v.y, 0x01010101, sum);
+        sum = __dp4a((int)v.z, 0x01010101, sum);
+        sum = __dp4a((int)v.w, 0x01010101, sum);
+      }
+    }
+    r.rs[idx] = sum;
+  }
+}
+
+template <int GPT, bool ZF>
 cudaError_t launch_bulk_g(const GemmParams& p, cudaStream_t s) {
   using C = BulkCfg<GPT>;
   static std::mutex mu;
@@ -271,7 +298,7 @@ cudaError_t launch_bulk_g(const GemmParams& p, cudaStream_t s) {
   cudaError_t e;
   {
     std::lock_guard<std::mutex> lock(mu);
-    e = set_smem_attr_once(gemm_bulk_kernel<GPT>, C::SMEM_BYTES, done_mask);
+    e = set_smem_attr_once(gemm_bulk_kernel<GPT, ZF>, C::SMEM_BYTES, done_mask);
   }
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -282,14 +309,15 @@ cudaError_t launch_bulk_g(const GemmParams& p, cudaStream_t s) {
   cudaLaunchAttribute attr[1] = {pdl_attr()};
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_bulk_kernel<GPT>, p);
+  return cudaLaunchKernelEx(&cfg, gemm_bulk_kernel<GPT, ZF>, p);
 }
 
-cudaError_t launch_bulk(const GemmParams& p, cudaStream_t s) {
+cudaError_t launch_bulk(const GemmParams& p, bool zero_folded, cudaStream_t s) {
+  if (zero_folded) return p.gpt == 1 ? launch_bulk_g<1, true>(p, s) : cudaErrorInvalidValue;
   switch (p.gpt) {
-    case 1: return launch_bulk_g<1>(p, s);
-    case 2: return launch_bulk_g<2>(p, s);
-    case 4: return launch_bulk_g<4>(p, s);
+    case 1: return launch_bulk_g<1, false>(p, s);
+    case 2: return launch_bulk_g<2, false>(p, s);
+    case 4: return launch_bulk_g<4, false>(p, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -299,7 +327,7 @@ cudaError_t launch_bulk(const GemmParams& p, cudaStream_t s) {
 cudaError_t launch_gemm(int M, int N, int K, int g, const int8_t* Xq, const uint16_t* sx,
                         const uint8_t* packed, const uint16_t* s1, uint16_t* Y, int32_t* acc_debug,
                         void* ws, int num_sms, unsigned long long timeout_ns, int fault,
-                        unsigned call_id, unsigned long long* trace, cudaStream_t s) {
+                        unsigned call_id, unsigned long long* trace, bool zero_folded, cudaStream_t s) {
   const int BN = gemm_bn_for_m(M);
   const WsLayout L = gemm_ws_layout(M, N, K);
   GemmParams p = {};
@@ -314,17 +342,17 @@ cudaError_t launch_gemm(int M, int N, int K, int g, const int8_t* Xq, const uint
   // Whole tiles round-robin over the persistent CTAs; when the last wave
   // would be partial, it and one full wave are split along K instead
   // (stream-K), so every CTA gets the same number of groups.
-  const int P0 = std::max(1, std::min(num_sms, kMaxGrid));
-  if (p.T >= P0) {
-    const int rem = p.T % P0;
-    p.T_sk = rem == 0 ? 0 : std::min(p.T, rem + P0);
+  const int P0s = std::max(1, std::min(num_sms, kMaxGrid));
+  if (p.T >= P0s) {
+    const int rem = p.T % P0s;
+    p.T_sk = rem == 0 ? 0 : std::min(p.T, rem + P0s);
     p.T_dp = p.T - p.T_sk;
-    p.P = P0;
+    p.P = P0s;
   } else {
     p.T_dp = 0;
     p.T_sk = p.T;
     const long long want = ((long long)p.T * p.G + 3) / 4;  // at least ~4 groups per CTA
-    p.P = (int)std::max<long long>(1, std::min<long long>(P0, want));
+    p.P = (int)std::max<long long>(1, std::min<long long>(P0s, want));
   }
   p.I_sk = (uint32_t)p.T_sk * (uint32_t)p.G;  // T_sk <= 2 P0 - 1 <= 511, G <= 1024
   uint8_t* w = static_cast<uint8_t*>(ws);
@@ -343,10 +371,33 @@ cudaError_t launch_gemm(int M, int N, int K, int g, const int8_t* Xq, const uint
   p.fault = fault;
   p.call_id = call_id;
   p.trace = trace;
+  p.rs = reinterpret_cast<const int32_t*>(w + L.rs_off);
+  p.rs_ld = L.rs_ld;
+  const int P0 = std::max(1, std::min(num_sms, kMaxGrid));
+
+  if (zero_folded) {
+    if (p.gpt != 1) return cudaErrorInvalidValue;
+    RowSumParams r = {};
+    r.Xq = Xq;
+    r.rs = reinterpret_cast<int32_t*>(w + L.rs_off);
+    r.M = M;
+    r.K = K;
+    r.rs_ld = L.rs_ld;
+    const long long work = (long long)p.G * L.rs_ld;
+    cudaLaunchConfig_t rcfg = {};
+    rcfg.gridDim = dim3((unsigned)std::max<long long>(1, std::min<long long>((work + 255) / 256, (long long)P0 * 4)));
+    rcfg.blockDim = dim3(256);
+    rcfg.stream = s;
+    cudaLaunchAttribute rattr[1] = {pdl_attr()};
+    rcfg.attrs = rattr;
+    rcfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&rcfg, rowsum_kernel, r);
+    if (e != cudaSuccess) return e;
+  }
 
   if (BN <= 64) {
     if (p.MT != 1) return cudaErrorInvalidValue;  // the decode kernel holds all M tokens in one tile
-    return launch_gemm_decode(p, BN, s);
+    return launch_gemm_decode(p, BN, zero_folded, s);
   }
 
   ConvertParams c = {};
@@ -367,7 +418,7 @@ cudaError_t launch_gemm(int M, int N, int K, int g, const int8_t* Xq, const uint
   cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, convert_kernel, c);
   if (e != cudaSuccess) return e;
-  return launch_bulk(p, s);
+  return launch_bulk(p, zero_folded, s);
 }
 
 }  // namespace qoq

@@ -274,6 +274,38 @@ __device__ __forceinline__ void advance_epoch_at_exit(const GemmParams& p) {
   }
 }
 
+// -------------------------------------------------- zero-point folding --
+// The zero-point-folded variant (QFactory notes, section 4.3: a matmul whose
+// weight operand carries an offset splits into the offset-free product and a
+// product with the all-ones matrix, i.e. row sums): the tensor cores see
+// q4 * s2, and this subtracts the zero points' share of k-tiles g0 .. g1-1 of
+// weight tile nt for tokens m0 .. m0 + COLS - 1 of weight row `row`:
+//   run[i] -= (z * s2)[row, g] * RS[g][m0 + i]   for every k-tile g,
+// with s2 and z read from the packed tile (one scale set per k-tile, g >= 128)
+// and RS the row sums the pre-pass wrote.  Tokens past M (whose RS chunks may
+// lie past the array) are skipped; their outputs are never written.
+template <int COLS, int TILE>
+__device__ __forceinline__ void zero_point_share(const GemmParams& p, int nt, int g0, int g1, int m0, int row,
+                                                 int32_t (&run)[COLS]) {
+  static_assert(COLS % 4 == 0, "row sums are read four tokens at a time");
+  const uint8_t* t = p.packed + ((size_t)nt * p.G + g0) * TILE;
+  for (int g = g0; g < g1; ++g, t += TILE) {
+    const int zs = (int)__ldg(t + row) * (int)__ldg(t + 128 + row);  // s2 * z
+    const int4* r = reinterpret_cast<const int4*>(p.rs + (size_t)g * p.rs_ld + m0);
+#pragma unroll
+    for (int q = 0; q < COLS / 4; ++q) {
+      if (m0 + 4 * q < p.rs_ld) {
+        const int4 v = __ldcg(r + q);
+        run[4 * q + 0] -= zs * v.x;
+        run[4 * q + 1] -= zs * v.y;
+        run[4 * q + 2] -= zs * v.z;
+        run[4 * q + 3] -= zs * v.w;
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ output --
 // ------------------------------------------------------------------ output --
 
 // Y[m, n] for the COLS tokens m = m0 .. m0+COLS-1 held by this thread.
@@ -342,7 +374,7 @@ __device__ __forceinline__ void write_tile_out(const GemmParams& p, const int32_
 // address of group gi's B tile; the group's A-full barrier covers it too.
 // After each MMA group: commits to `bar_aempty[a]` and to `extra_commit(gi)`
 // (0 = none).
-template <int BN, int NACC, int NABUF, int ACOL0, typename BTile, typename ExtraCommit>
+template <int BN, int NACC, int NABUF, int ACOL0, int FOLD, typename BTile, typename ExtraCommit>
 __device__ __forceinline__ void mma_role(const GemmParams& p, uint32_t tmem, uint32_t bar_afull,
                                          uint32_t bar_aempty, uint32_t bar_accfull, uint32_t bar_accempty,
                                          uint32_t bar_drain, BTile b_tile, ExtraCommit extra_commit) {
@@ -353,8 +385,8 @@ __device__ __forceinline__ void mma_role(const GemmParams& p, uint32_t tmem, uin
   uint32_t gi = 0, chunk = 0;
   bool ok = true;
   while (ok && iter.next(p, u)) {
-    for (int c0 = u.g0; c0 < u.g1; c0 += kFoldGroups) {
-      const int c1 = min(u.g1, c0 + kFoldGroups);
+    for (int c0 = u.g0; c0 < u.g1; c0 += FOLD) {
+      const int c1 = min(u.g1, c0 + FOLD);
       const int b = chunk % NACC;
       if (!warp_wait_bar(bar_accempty + 8 * b, ((chunk / NACC) & 1) ^ 1, p)) {
         ok = false;
@@ -448,7 +480,8 @@ __device__ __forceinline__ void finish_unit(const GemmParams& p, const Unit& u, 
 // lane.  Per fold chunk: read the fp32 accumulator, convert to int32 (exact),
 // add.  At a unit's end: write Y (whole-K tile), or add the int32 partials
 // into the workspace and let the last contributor write Y and clear them.
-template <int BN, int NEPI, int NACC>
+template <int BN, int NEPI, int NACC, bool ZF = false, int TILE = kWTileBytes,
+          int FOLD = ZF ? kFoldGroupsZf : kFoldGroups>
 __device__ __forceinline__ void epilogue_role(const GemmParams& p, uint32_t tmem, int epi_warp0,
                                               uint32_t bar_accfull, uint32_t bar_accempty,
                                               volatile int* last_flag) {
@@ -473,8 +506,10 @@ __device__ __forceinline__ void epilogue_role(const GemmParams& p, uint32_t tmem
     int32_t run[TOK];
 #pragma unroll
     for (int i = 0; i < TOK; ++i) run[i] = 0;
-    for (int c0 = u.g0; c0 < u.g1; c0 += kFoldGroups, ++chunk) {
+    for (int c0 = u.g0; c0 < u.g1; c0 += FOLD, ++chunk) {
       const int b = chunk % NACC;
+      // zero points' share of the chunk, while its MMAs still run
+      if constexpr (ZF) zero_point_share<TOK, TILE>(p, nt, c0, min(u.g1, c0 + FOLD), mt * BN + tok0, row, run);
       if (ok) ok = conv_wait_bar(bar_accfull + 8 * b, (chunk / NACC) & 1, p);
       if (e == 0 && lane == 0) QOQ_TRACE_AT(p, 512 + (int)chunk, 0);
       if (ok) {

@@ -53,9 +53,9 @@ struct DecCfg {
   static constexpr int EPI_WARP0 = 2 + NDQ;
   static constexpr int THREADS = (2 + NDQ + NEPI) * 32;
   static constexpr int NACC = 2;
-  // Fold chunk: up to CH consecutive groups of a unit, so at most 8 groups of
-  // each slot go into one fp32 accumulator (exact below 2^24).
-  static constexpr int CH = kFoldGroups * NSLOT;
+  // Fold chunk: up to CH(fold) consecutive groups of a unit, so at most
+  // `fold` groups of each slot go into one fp32 accumulator (exact below 2^24).
+  __host__ __device__ static constexpr int chunk(int fold) { return fold * NSLOT; }
   // TMEM columns: accumulator b of slot j at (j * NACC + b) * BN; slot j's A
   // buffer (128 rows x 128 fp16 = 64 columns) at ACOL0 + 64 j.
   static constexpr int ACOL0 = (NSLOT * NACC * BN + 63) / 64 * 64;
@@ -161,9 +161,12 @@ __device__ __forceinline__ void slot_clear(const GemmParams& p, int b1, int tok0
   }
 }
 
-template <int BN, int GPT>
+// ZF: the zero-point-folded variant (A operand q4 * s2; the zero points'
+// share is subtracted in the epilogue, see zero_point_share).
+template <int BN, int GPT, bool ZF>
 __global__ void __launch_bounds__(DecCfg<BN, GPT>::THREADS, 1) gemm_decode_kernel(const __grid_constant__ GemmParams p) {
   using C = DecCfg<BN, GPT>;
+  constexpr int CH = C::chunk(ZF ? kFoldGroupsZf : kFoldGroups);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -269,8 +272,8 @@ __global__ void __launch_bounds__(DecCfg<BN, GPT>::THREADS, 1) gemm_decode_kerne
     // waits and work, and the kernel winds down.
     bool ok = true;
     while (iter.next(p, u)) {
-      for (int c0 = u.g0; c0 < u.g1; c0 += C::CH, ++ch) {
-        const int len = min(C::CH, u.g1 - c0);
+      for (int c0 = u.g0; c0 < u.g1; c0 += CH, ++ch) {
+        const int len = min(CH, u.g1 - c0);
         const uint32_t gc0 = gi_u + (uint32_t)(c0 - u.g0);
         const int b = ch % C::NACC;
         const uint32_t d_tmem = tmem + (uint32_t)((slot * C::NACC + b) * BN);
@@ -316,7 +319,7 @@ __global__ void __launch_bounds__(DecCfg<BN, GPT>::THREADS, 1) gemm_decode_kerne
               s2v[u] = wt[u * 256 + row];
               zv[u] = wt[u * 256 + 128 + row];
             }
-            DequantConsts kc = dequant_consts(s2v[0], zv[0]);
+            DequantConsts kc = dequant_consts(s2v[0], ZF ? 0u : zv[0]);
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_empty + 8 * s);  // the weight tile is in registers
 #pragma unroll
@@ -327,7 +330,8 @@ __global__ void __launch_bounds__(DecCfg<BN, GPT>::THREADS, 1) gemm_decode_kerne
             fence_proxy_async_smem();  // generic-proxy writes -> the MMA's async-proxy reads
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-              if (GPT > 1 && c > 0 && c % (4 / GPT) == 0) kc = dequant_consts(s2v[c / (4 / GPT)], zv[c / (4 / GPT)]);
+              if (GPT > 1 && c > 0 && c % (4 / GPT) == 0)
+                kc = dequant_consts(s2v[c / (4 / GPT)], ZF ? 0u : zv[c / (4 / GPT)]);
               uint32_t out[16];
               dequant_chunk(wv[c], kc, out);
               tmem_st16(tmem + lane_base + C::ACOL0 + 64 * slot + c * 16, out);
@@ -381,10 +385,12 @@ __global__ void __launch_bounds__(DecCfg<BN, GPT>::THREADS, 1) gemm_decode_kerne
       int32_t run[TOK];
 #pragma unroll
       for (int i = 0; i < TOK; ++i) run[i] = 0;
-      for (int c0 = u.g0; c0 < u.g1; c0 += C::CH, ++ch) {
-        const int len = min(C::CH, u.g1 - c0);
+      for (int c0 = u.g0; c0 < u.g1; c0 += CH, ++ch) {
+        const int len = min(CH, u.g1 - c0);
         const uint32_t gc0 = gi_u + (uint32_t)(c0 - u.g0);
         const int b = ch % C::NACC;
+        // zero points' share of the chunk's groups, while their MMAs still run
+        if constexpr (ZF) zero_point_share<TOK, C::TILE>(p, u.tile, c0, c0 + len, tok0, row, run);
         if (ok) ok = conv_wait_bar(bar_accfull + 8 * b, (ch / C::NACC) & 1, p);
         if (e == 0 && lane == 0) QOQ_TRACE_AT(p, 512 + (int)ch, 0);
         if (ok) {
@@ -461,7 +467,7 @@ __global__ void __launch_bounds__(DecCfg<BN, GPT>::THREADS, 1) gemm_decode_kerne
   }
 }
 
-template <int BN, int GPT>
+template <int BN, int GPT, bool ZF>
 cudaError_t launch_bn(const GemmParams& p, cudaStream_t s) {
   using C = DecCfg<BN, GPT>;
   static std::mutex mu;
@@ -469,7 +475,7 @@ cudaError_t launch_bn(const GemmParams& p, cudaStream_t s) {
   cudaError_t e;
   {
     std::lock_guard<std::mutex> lock(mu);
-    e = set_smem_attr_once(gemm_decode_kernel<BN, GPT>, C::SMEM_BYTES, done_mask);
+    e = set_smem_attr_once(gemm_decode_kernel<BN, GPT, ZF>, C::SMEM_BYTES, done_mask);
   }
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -480,26 +486,27 @@ cudaError_t launch_bn(const GemmParams& p, cudaStream_t s) {
   cudaLaunchAttribute attr[1] = {pdl_attr()};
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_decode_kernel<BN, GPT>, p);
+  return cudaLaunchKernelEx(&cfg, gemm_decode_kernel<BN, GPT, ZF>, p);
 }
 
-template <int GPT>
+template <int GPT, bool ZF>
 cudaError_t launch_gemm_decode_g(const GemmParams& p, int BN, cudaStream_t s) {
   switch (BN) {
-    case 16: return launch_bn<16, GPT>(p, s);
-    case 32: return launch_bn<32, GPT>(p, s);
-    case 64: return launch_bn<64, GPT>(p, s);
+    case 16: return launch_bn<16, GPT, ZF>(p, s);
+    case 32: return launch_bn<32, GPT, ZF>(p, s);
+    case 64: return launch_bn<64, GPT, ZF>(p, s);
     default: return cudaErrorInvalidValue;
   }
 }
 
 }  // namespace
 
-cudaError_t launch_gemm_decode(const GemmParams& p, int BN, cudaStream_t s) {
+cudaError_t launch_gemm_decode(const GemmParams& p, int BN, bool zero_folded, cudaStream_t s) {
+  if (zero_folded) return p.gpt == 1 ? launch_gemm_decode_g<1, true>(p, BN, s) : cudaErrorInvalidValue;
   switch (p.gpt) {
-    case 1: return launch_gemm_decode_g<1>(p, BN, s);
-    case 2: return launch_gemm_decode_g<2>(p, BN, s);
-    case 4: return launch_gemm_decode_g<4>(p, BN, s);
+    case 1: return launch_gemm_decode_g<1, false>(p, BN, s);
+    case 2: return launch_gemm_decode_g<2, false>(p, BN, s);
+    case 4: return launch_gemm_decode_g<4, false>(p, BN, s);
     default: return cudaErrorInvalidValue;
   }
 }

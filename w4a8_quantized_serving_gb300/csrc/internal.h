@@ -27,6 +27,8 @@ __host__ __device__ constexpr int w_tile_bytes(int gpt) { return w_nib_offset(gp
 constexpr int kWTileBytes = w_tile_bytes(1);  // g >= 128: 8448 bytes
 constexpr int kFoldGroups = 8;     // fp32 TMEM partials are folded to int32 every 8 groups
                                    // (1024 channels: 127*127*1024 < 2^24, exact in fp32)
+constexpr int kFoldGroupsZf = 4;   // the zero-point-folded variant's operand q4 * s2 reaches 240:
+                                   // every 4 groups (512 channels: 240*127*512 < 2^24)
 constexpr int kMaxSkTiles = 512;   // upper bound of split-K tiles per call (workspace sizing)
 constexpr int kMaxGrid = 160;      // upper bound of persistent CTAs per call (GB300: 152 SMs)
 
@@ -52,9 +54,13 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 //     ([BN][128] entries of {int32 partial sum, uint32 epoch tag});
 //   128-token tiles: header, split-K tile counters, int32 partial tiles, and
 //     the fp16 B-operand copy of Xq.
+// Both end with the per-k-tile row sums of Xq that the zero-point-folded
+// variant subtracts in its epilogue: int32 [K/128][rs_ld], rs_ld = M rounded
+// up to a multiple of 4 (rewritten by every call of that variant).
 // zero_bytes: the prefix that must be zero before the first call.
 struct WsLayout {
-  size_t cnt_off, acc_off, slot_off, xh_off, zero_bytes, total;
+  size_t cnt_off, acc_off, slot_off, xh_off, rs_off, zero_bytes, total;
+  int rs_ld;
 };
 
 inline WsLayout gemm_ws_layout(int M, int N, int K) {
@@ -63,20 +69,24 @@ inline WsLayout gemm_ws_layout(int M, int N, int K) {
   const long long T = MT * (N / kTileN);
   const long long skmax = T < kMaxSkTiles ? T : kMaxSkTiles;
   WsLayout L;
+  L.rs_ld = (M + 3) / 4 * 4;
+  const size_t rs_bytes = (size_t)(K / kGroup) * L.rs_ld * 4;
   if (BN <= 64) {
     L.cnt_off = L.acc_off = 0;  // unused
     L.slot_off = kWsHeaderBytes;
-    L.xh_off = align_up(L.slot_off + (size_t)kMaxGrid * BN * kTileN * 8, 1024);
+    L.xh_off = align_up(L.slot_off + (size_t)kMaxGrid * BN * kTileN * 8, 1024);  // no B copy: end of slots
+    L.rs_off = L.xh_off;
     L.zero_bytes = kWsHeaderBytes;
-    L.total = L.xh_off;
+    L.total = align_up(L.rs_off + rs_bytes, 256);
     return L;
   }
   L.slot_off = 0;  // unused
   L.cnt_off = kWsHeaderBytes;
   L.acc_off = align_up(L.cnt_off + (size_t)skmax * 4, 256);
   L.xh_off = align_up(L.acc_off + (size_t)skmax * BN * kTileN * 4, 1024);
+  L.rs_off = align_up(L.xh_off + (size_t)MT * K * BN * 2, 256);
   L.zero_bytes = L.xh_off;
-  L.total = align_up(L.xh_off + (size_t)MT * K * BN * 2, 256);
+  L.total = align_up(L.rs_off + rs_bytes, 256);
   return L;
 }
 
@@ -111,6 +121,8 @@ struct GemmParams {
   int fault;
   unsigned call_id;           // non-zero: the abort word names the aborting call (not a hand-off tag)
   unsigned long long* trace;  // per-CTA event clock, only with -DQOQ_TRACE (else unused)
+  const int32_t* rs;          // zero-point-folded variant: row sums of Xq per k-tile, [G][rs_ld]
+  int rs_ld;
 };
 
 // Event tracing for pipeline studies: compiled in only with -DQOQ_TRACE.
@@ -145,6 +157,13 @@ struct ConvertParams {
   int M, K, BN, MT;
 };
 
+// Row sums of Xq per 128-channel k-tile, for the zero-point-folded variant.
+struct RowSumParams {
+  const int8_t* Xq;
+  int32_t* rs;  // [K/128][rs_ld]
+  int M, K, rs_ld;
+};
+
 // Launch attribute for programmatic dependent launch: the kernel may start
 // before the preceding kernel on the stream has finished, once that kernel
 // has triggered (griddepcontrol.launch_dependents) or exited; it must execute
@@ -166,10 +185,13 @@ cudaError_t launch_pack(int N, int K, int g, const uint16_t* W, uint8_t* packed,
                         cudaStream_t s);
 cudaError_t launch_unpack(int N, int K, int g, const uint8_t* packed, uint8_t* q4, uint8_t* s2, uint8_t* z,
                           cudaStream_t s);
-cudaError_t launch_gemm_decode(const GemmParams& p, int BN, cudaStream_t s);
+cudaError_t launch_gemm_decode(const GemmParams& p, int BN, bool zero_folded, cudaStream_t s);
+// zero_folded: the variant that feeds q4 * s2 to the tensor cores and
+// subtracts the zero points' share, sum_j z s2 RS[m, j], in the epilogue
+// (g >= 128 only); it first launches the row-sum pre-pass.
 cudaError_t launch_gemm(int M, int N, int K, int g, const int8_t* Xq, const uint16_t* sx,
                         const uint8_t* packed, const uint16_t* s1, uint16_t* Y, int32_t* acc_debug,
                         void* ws, int num_sms, unsigned long long timeout_ns, int fault,
-                        unsigned call_id, unsigned long long* trace, cudaStream_t s);
+                        unsigned call_id, unsigned long long* trace, bool zero_folded, cudaStream_t s);
 
 }  // namespace qoq
