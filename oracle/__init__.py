@@ -95,6 +95,10 @@ class Oracle:
         lib.qoq_oracle_gemm_threads.restype = i32
         lib.qoq_oracle_gemm_zero_folded.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P, P, P]
         lib.qoq_oracle_gemm_zero_folded.restype = i32
+        lib.qoq_oracle_act_quant_w4ax.argtypes = [i32, i32, i32, P, P, P]
+        lib.qoq_oracle_act_quant_w4ax.restype = i32
+        lib.qoq_oracle_gemm_w4ax.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P, P, P]
+        lib.qoq_oracle_gemm_w4ax.restype = i32
         lib.qoq_oracle_gemm_entries.argtypes = [i32, P, P, i32, i32, P, P, P, P, P, P, P, P]
         lib.qoq_oracle_gemm_entries.restype = i32
         lib.qoq_oracle_norm_quant_act.argtypes = [i32, i32, i32, ctypes.c_float, P, P, P, P, P, P, P, P]
@@ -191,6 +195,32 @@ class Oracle:
             raise OracleError("gemm_zero_folded: |acc| reached 2^31")
         return acc, Y, RS
 
+    def act_quant_w4ax(self, X_bits: np.ndarray, n8: int):
+        """W4Ax activations of fp16 X [M][K]: the n8 leading 128-channel blocks
+        8-bit, the rest 4-bit, one symmetric scale per (token, block).
+        Returns (codes [M][K] int8, sxb [M][K/128] fp16 bits)."""
+        X = _c(X_bits, np.uint16)
+        M, K = X.shape
+        codes = np.empty((M, K), np.int8)
+        sxb = np.empty((M, K // 128), np.uint16)
+        _check(self.lib.qoq_oracle_act_quant_w4ax(M, K, int(n8), _p(X), _p(codes), _p(sxb)), "act_quant_w4ax")
+        return codes, sxb
+
+    def gemm_w4ax(self, codes, sxb, q4, s2, z, s1, g: int = 128, want_blocks: bool = False):
+        """W4Ax product: (acc_sum [M][N] int64, Y [M][N] fp16 bits, and
+        acc_blocks [M][N][K/128] int64 when want_blocks)."""
+        codes = _c(codes, np.int8)
+        q4 = _c(q4, np.uint8)
+        M, K = codes.shape
+        N = q4.shape[0]
+        acc = np.empty((M, N), np.int64)
+        Y = np.empty((M, N), np.uint16)
+        blocks = np.empty((M, N, K // 128), np.int64) if want_blocks else None
+        _check(self.lib.qoq_oracle_gemm_w4ax(M, N, K, g, _p(codes), _p(_c(sxb, np.uint16)), _p(q4),
+                                             _p(_c(s2, np.uint8)), _p(_c(z, np.uint8)), _p(_c(s1, np.uint16)),
+                                             _p(blocks), _p(acc), _p(Y)), "gemm_w4ax")
+        return (acc, Y, blocks) if want_blocks else (acc, Y)
+
     def gemm_entries(self, m_idx, n_idx, Xq, sx, q4, s2, z, s1, g: int = 128):
         """acc and Y for the listed (m, n) entries only."""
         m_idx = _c(m_idx, np.int32)
@@ -246,6 +276,6 @@ def __getattr__(name):
     # module-level shortcuts: oracle.weight_quant(...) etc. use the default build
     if name in ("half_to_double", "double_to_half", "dequant_code", "dequant_real", "weight_quant",
                 "dequant_weights", "act_quant", "gemm", "gemm_entries", "norm_quant_act",
-                "gemm_zero_folded"):
+                "gemm_zero_folded", "act_quant_w4ax", "gemm_w4ax"):
         return getattr(default(), name)
     raise AttributeError(name)

@@ -238,6 +238,31 @@ int qoq_oracle_act_quant(int M, int K, const uint16_t* X, int8_t* Xq, uint16_t* 
 }
 
 /* ------------------------------------------------------------------------ */
+/* W4Ax activations: 4-bit blocks with 8-bit outlier blocks                  */
+/* ------------------------------------------------------------------------ */
+
+/* COMET explainer (bookshelf), FMPQ: activations are quantized in blocks of
+ * 128 channels (the tensor-core tile's granularity); the outlier channels,
+ * clustered into a few blocks by a channel permutation, stay at 8 bits and
+ * every other block goes to 4 bits.  Readings taken (the pages fix neither
+ * the scale nor the rounding): the permutation puts the outlier blocks first,
+ * so the n8 leading blocks are 8-bit; each (token m, block b) has its own
+ * symmetric scale, the recipe of the per-token quantizer with qmax = 127
+ * (8-bit) or 7 (4-bit):
+ *   s[m,b] = fp16(amax_b / qmax) (IEEE fp32 divide), code = clamp(rint(x / s), +-qmax).
+ * Out: codes [M][K] int8 (one code per byte), sxb [M][K/128] fp16 bits. */
+int qoq_oracle_act_quant_w4ax(int M, int K, int n8, const uint16_t* X, int8_t* codes, uint16_t* sxb) {
+  if (M <= 0 || K <= 0 || K % 128 != 0 || n8 < 0 || n8 > K / 128 || !X || !codes || !sxb)
+    return QOQ_ORACLE_EARG;
+  const int G = K / 128;
+  for (int m = 0; m < M; ++m)
+    for (int b = 0; b < G; ++b)
+      symmetric_row(128, X + (size_t)m * K + (size_t)b * 128, b < n8 ? 127 : 7, &sxb[(size_t)m * G + b],
+                    codes + (size_t)m * K + (size_t)b * 128);
+  return QOQ_ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------ */
 /* GEMM: integer accumulation, per-channel scales in the epilogue            */
 /* ------------------------------------------------------------------------ */
 
@@ -274,6 +299,42 @@ int qoq_oracle_gemm(int M, int N, int K, int g, const int8_t* Xq, const uint16_t
       if (Y) Y[(size_t)m * N + n] = epilogue(a, sx[m], s1[n]);
     }
   return rc;
+}
+
+/* W4Ax product (COMET explainer, the W4Ax kernel: mixed 4-bit and 8-bit
+ * activation blocks times 4-bit weights, each block's partial sums scaled by
+ * the block's activation scale on the general-purpose cores).  With the
+ * dequantized weights w8 = (q4 - z) s2 of the progressive group format:
+ *   acc_b[m,n] = sum over the 128 channels k of block b of codes[m,k] w8[n,k]  (int64),
+ *   Y[m,n] = fp16_rn(s1[n] * sum_b sxb[m,b] * acc_b[m,n])
+ * the sum over blocks taken in double, in block order, then rounded once to
+ * fp16 (each term s * acc_b is exact in double).  acc_sum (nullable) gets
+ * sum_b acc_b, acc_blocks (nullable) every acc_b as [M][N][K/128]. */
+int qoq_oracle_gemm_w4ax(int M, int N, int K, int g, const int8_t* codes, const uint16_t* sxb,
+                         const uint8_t* q4, const uint8_t* s2, const uint8_t* z, const uint16_t* s1,
+                         int64_t* acc_blocks, int64_t* acc_sum, uint16_t* Y) {
+  if (M <= 0 || N <= 0 || K <= 0 || K % 128 != 0 || g <= 0 || K % g != 0 || !codes || !sxb || !q4 || !s2 ||
+      !z || !s1)
+    return QOQ_ORACLE_EARG;
+  const int G = K / g, B = K / 128;
+  for (int m = 0; m < M; ++m)
+    for (int n = 0; n < N; ++n) {
+      double y = 0.0;
+      int64_t total = 0;
+      for (int b = 0; b < B; ++b) {
+        int64_t a = 0;
+        for (int k = b * 128; k < (b + 1) * 128; ++k) {
+          const size_t gi = (size_t)n * G + k / g;
+          a += (int64_t)codes[(size_t)m * K + k] * qoq_oracle_dequant_code(q4[(size_t)n * K + k], z[gi], s2[gi]);
+        }
+        if (acc_blocks) acc_blocks[((size_t)m * N + n) * B + b] = a;
+        total += a;
+        y += qoq_oracle_half_to_double(sxb[(size_t)m * B + b]) * (double)a;
+      }
+      if (acc_sum) acc_sum[(size_t)m * N + n] = total;
+      if (Y) Y[(size_t)m * N + n] = qoq_oracle_double_to_half(qoq_oracle_half_to_double(s1[n]) * y);
+    }
+  return QOQ_ORACLE_OK;
 }
 
 /* Zero-point folding (QFactory notes, papercache.org, section 4.3 "mapping

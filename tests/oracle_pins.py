@@ -391,6 +391,110 @@ def check_zero_folded_equals_direct(o) -> None:
     assert np.array_equal(acc, acc0)
 
 
+# ----------------------------------------------------------------- W4Ax --
+# COMET explainer, FMPQ and the W4Ax kernel: 128-channel activation blocks,
+# the n8 leading (outlier) blocks at 8 bits, the rest at 4 bits, one scale per
+# (token, block); the product scales each block's integer partial sum.
+
+def _w4ax_golden_inputs(gold: dict, zf: dict):
+    """X [1][256] and W [128][256] of the hand-worked W4Ax example."""
+    appx = load_golden("appendix_a_g4.txt")
+    K = 256
+    Wl = np.zeros(K)
+    for j in range(2):
+        Wl[128 * j:128 * j + 4] = np.array(appx["Q8"][4 * j:4 * j + 4]) * 2.0 ** -7
+    Xl = np.zeros(K)
+    Xl[0:4] = np.array(gold["codes0"]) * 2.0 ** -6
+    Xl[128:132] = np.array(gold["codes1"]) * 2.0 ** -3
+    return f16(Xl).reshape(1, K), np.repeat(f16(Wl).reshape(1, K), 128, axis=0), appx
+
+
+def check_w4ax_golden(o) -> None:
+    gold = load_golden("w4ax_two_blocks.txt")
+    X, W, appx = _w4ax_golden_inputs(gold, None)
+    codes, sxb = o.act_quant_w4ax(synth.bits(X), gold["n8"])
+    assert codes[0, 0:4].tolist() == gold["codes0"] and codes[0, 128:132].tolist() == gold["codes1"]
+    assert not codes[0, 4:128].any() and not codes[0, 132:].any()
+    assert sxb[0].tolist() == gold["scale_bits"]
+    r = o.weight_quant(synth.bits(W), 128)
+    acc, Y, blocks = o.gemm_w4ax(codes, sxb, r["q4"], r["s2"], r["z"], r["s1"], 128, want_blocks=True)
+    assert (blocks[0] == np.array(gold["acc_blocks"])).all()
+    assert (acc == gold["acc_sum"]).all() and (Y == gold["Y_bits"]).all()
+
+
+def check_w4ax_8bit_blocks(o) -> None:
+    """An 8-bit block is the per-token quantizer applied to that block alone."""
+    M, K = 5, 512
+    X = synth.activations(M, K, 61)
+    codes, sxb = o.act_quant_w4ax(synth.bits(X), K // 128)
+    for b in range(K // 128):
+        cq, cs = o.act_quant(synth.bits(X[:, 128 * b:128 * b + 128]))
+        assert np.array_equal(codes[:, 128 * b:128 * b + 128], cq) and np.array_equal(sxb[:, b], cs)
+
+
+def check_w4ax_4bit_bruteforce(o) -> None:
+    """4-bit blocks: s = fp16(amax / 7) and each code the integer in [-7, 7]
+    nearest x / s (ties to even), from exact rationals; |s c - x| <= s / 2
+    wherever x / s lies within the range."""
+    rng = np.random.default_rng(62)
+    M, K, n8 = 4, 384, 1
+    X = f16(rng.standard_normal((M, K)) * np.array([1.0, 30.0, 0.01, 1.0])[:, None])
+    X[3, 128:256] = f16(((np.arange(128) % 15) - 7 + 0.5) * 2.0 ** -4)  # exact ties, amax = 7.5 * 2^-4
+    codes, sxb = o.act_quant_w4ax(synth.bits(X), n8)
+    for m in range(M):
+        for b in range(n8, K // 128):
+            blk = X[m, 128 * b:128 * b + 128].astype(np.float64)
+            amax = float(np.abs(blk).max())
+            s_bits = int(f16(np.float32(amax) / np.float32(7.0)).view(np.uint16)) if amax > 0 else 0
+            assert int(sxb[m, b]) == s_bits, (m, b)
+            s = float(np.uint16(s_bits).view(np.float16))
+            for k in range(128):
+                want = 0 if s == 0 else max(-7, min(7, nearest_int_half_even(Fraction(blk[k]) / Fraction(s))))
+                assert int(codes[m, 128 * b + k]) == want, (m, b, k)
+                if s and abs(blk[k] / s) <= 7.5:
+                    assert abs(s * want - blk[k]) <= s / 2 + 1e-12
+
+
+def check_w4ax_gemm_reduces_to_w4a8(o) -> None:
+    """With every block 8-bit and every block of a row sharing its max-abs,
+    the block scales all equal the per-token scale: the W4Ax product is the
+    W4A8 product, bit for bit."""
+    M, N, K = 3, 24, 512
+    X = f16(np.clip(synth.activations(M, K, 63).astype(np.float64), -1.0, 1.0))
+    X[:, ::128] = f16(np.array([5.0, -2.0, 9.0]))[:, None]  # the row max sits in every block
+    W = synth.weights(N, K, 63)
+    r = o.weight_quant(synth.bits(W), 128)
+    codes, sxb = o.act_quant_w4ax(synth.bits(X), K // 128)
+    Xq, sx = o.act_quant(synth.bits(X))
+    assert (sxb == sx[:, None]).all() and np.array_equal(codes, Xq)
+    acc_ref, Y_ref = o.gemm(Xq, sx, r["q4"], r["s2"], r["z"], r["s1"], 128)
+    acc, Y = o.gemm_w4ax(codes, sxb, r["q4"], r["s2"], r["z"], r["s1"], 128)
+    assert np.array_equal(acc, acc_ref) and np.array_equal(Y, Y_ref)
+
+
+def check_w4ax_gemm_float_reference(o) -> None:
+    """Y against float64 dequant-then-matmul (s_b c) (s1 w8) rounded to fp16:
+    equal, or one fp16 unit apart where the two summation orders straddle a
+    rounding boundary; the per-block sums against numpy's int64 matmul."""
+    M, N, K = 6, 40, 640
+    X = synth.activations(M, K, 64)
+    W = synth.weights(N, K, 64)
+    r = o.weight_quant(synth.bits(W), 64)
+    codes, sxb = o.act_quant_w4ax(synth.bits(X), 2)
+    acc, Y, blocks = o.gemm_w4ax(codes, sxb, r["q4"], r["s2"], r["z"], r["s1"], 64, want_blocks=True)
+    w8 = o.dequant_weights(r["q4"], r["s2"], r["z"], 64).astype(np.int64)
+    c = codes.astype(np.int64)
+    for b in range(K // 128):
+        sl = slice(128 * b, 128 * b + 128)
+        assert np.array_equal(blocks[:, :, b], c[:, sl] @ w8[:, sl].T)
+    assert np.array_equal(acc, c @ w8.T)
+    xd = c * np.repeat(half_val(sxb), 128, axis=1)
+    yd = (xd @ (w8 * half_val(r["s1"])[:, None]).T).astype(np.float16)
+    ulp = np.abs(Y.view(np.float16).astype(np.int32) - yd.view(np.int16).astype(np.int32))
+    got, ref = Y.view(np.int16).astype(np.int32), yd.view(np.int16).astype(np.int32)
+    assert (np.abs(got - ref) <= 1).all() and (got == ref).mean() > 0.99
+
+
 def check_acc_range(o) -> None:
     """|acc| <= 127 * 127 * K stays below 2^31 for K <= 131072 (worst case)."""
     K = 1024
@@ -512,6 +616,7 @@ ALL_CHECKS = [
     check_half_to_double, check_double_to_half, check_appendix_a, check_appendix_a_g128,
     check_fig3_literal, check_level1_bruteforce, check_level2_bruteforce, check_invariants,
     check_error_bounds, check_lossless_grid, check_zero_and_underflow, check_gemm_library,
-    check_gemm_threads, check_zero_folded_appendix, check_zero_folded_equals_direct, check_acc_range, check_norm_exact_stats, check_norm_layer_constant_row, check_norm_rms_unit_row,
+    check_gemm_threads, check_w4ax_golden, check_w4ax_8bit_blocks, check_w4ax_4bit_bruteforce,
+    check_w4ax_gemm_reduces_to_w4a8, check_w4ax_gemm_float_reference, check_zero_folded_appendix, check_zero_folded_equals_direct, check_acc_range, check_norm_exact_stats, check_norm_layer_constant_row, check_norm_rms_unit_row,
     check_norm_error_bound, check_norm_quant_composition,
 ]

@@ -40,6 +40,10 @@ MUTANTS = {
                                   "corr += (int64_t)z[(size_t)n * G + j] * RS[(size_t)m * G + j];"),
     "folded_rowsum_range": ("for (int k = j * g; k < (j + 1) * g; ++k) t += Xq[(size_t)m * K + k];",
                             "for (int k = j * g; k < (j + 1) * g - 1; ++k) t += Xq[(size_t)m * K + k];"),
+    "w4ax_four_bit_range": ("b < n8 ? 127 : 7, &sxb", "b < n8 ? 127 : 8, &sxb"),
+    "w4ax_leading_blocks": ("b < n8 ? 127 : 7, &sxb", "b <= n8 ? 127 : 7, &sxb"),
+    "w4ax_block_scale_index": ("y += qoq_oracle_half_to_double(sxb[(size_t)m * B + b]) * (double)a;",
+                               "y += qoq_oracle_half_to_double(sxb[(size_t)m * B]) * (double)a;"),
     "threads_range_gap": ("(int)((int64_t)N * (t + 1) / threads),", "(int)((int64_t)N * (t + 1) / threads) - (t & 1),"),
     "threads_group_index": ("r->s2[(size_t)n * G + k / r->g]);", "r->s2[(size_t)n * G + k % G]);"),
 }
