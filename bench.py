@@ -48,12 +48,29 @@ UNIT = "TOPS"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
-def algorithmic_bytes(M: int, N: int, K: int, g: int = 128) -> dict:
+def algorithmic_bytes(M: int, N: int, K: int, g: int = 128, n8: int | None = None) -> dict:
     """Bytes the GEMM call must move at least once: q4 nibbles, per-group s2 and
-    z, s1, Xq, s_x, and the fp16 output; plus the activation quantizer's."""
-    gemm = N * K // 2 + 2 * N * (K // g) + 2 * N + M * K + 2 * M + 2 * M * N
-    act = 2 * M * K + M * K + 2 * M
+    z, s1, Xq, s_x, and the fp16 output; plus the activation quantizer's.
+    With n8 (the W4Ax path): the activations are the n8 8-bit blocks (128 bytes
+    per token) and the 4-bit ones (64 bytes), with one fp16 scale per (token,
+    block)."""
+    weights = N * K // 2 + 2 * N * (K // g) + 2 * N
+    if n8 is None:
+        acts = M * K + 2 * M
+    else:
+        G = K // 128
+        acts = M * (128 * n8 + 64 * (G - n8)) + 2 * M * G
+    gemm = weights + acts + 2 * M * N
+    act = 2 * M * K + acts
     return {"gemm": gemm, "act": act, "step": gemm + act}
+
+
+def outlier_first_permutation(seed: int, K: int) -> np.ndarray:
+    """Channel order with the activation generator's outlier channels first
+    (the W4Ax path's channel permutation: they fall into the leading 8-bit
+    block), the other channels in their order."""
+    out = synth.outlier_channels(seed, synth.TAG_X, K, 4)
+    return np.concatenate([out, np.setdiff1d(np.arange(K), out)])
 
 
 def load_peaks() -> tuple[dict, str]:
@@ -277,11 +294,12 @@ def config_dict(c: dict, extra: dict | None = None) -> dict:
 
 # ------------------------------------------------------------------ GPU arm --
 
-def roofline_of(M: int, N: int, K: int, g: int, gemm_ms: float, steps: int, peaks: dict, peak_src: str) -> dict:
+def roofline_of(M: int, N: int, K: int, g: int, gemm_ms: float, steps: int, peaks: dict, peak_src: str,
+                n8: int | None = None) -> dict:
     """The GEMM call against the roofline that binds it: HBM below the ridge
     (algorithmic bytes / time), the tensor pipe above it (2MNK / time)."""
     ops = 2.0 * M * N * K
-    nbytes = algorithmic_bytes(M, N, K, g)["gemm"]
+    nbytes = algorithmic_bytes(M, N, K, g, n8)["gemm"]
     ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
     if ops / nbytes < ridge:
         achieved = nbytes / (gemm_ms * 1e-3) / 1e9
@@ -311,8 +329,16 @@ def bench_workload(q, torch, c: dict, args, dev, stream, dist, rank: int) -> dic
     K_steps, repeats = args.steps, args.repeats
 
     # weights: generated once, packed on the GPU (timed separately), cloned into a pool
-    W = torch.from_numpy(synth.weights(N, K, c["seed"])).to(dev)
-    X = torch.from_numpy(synth.activations(M, K, c["seed"] + rank)).to(dev)
+    w4ax = args.path == "w4ax"
+    n8 = args.n8
+    Wn = synth.weights(N, K, c["seed"])
+    Xn = synth.activations(M, K, c["seed"] + rank)
+    if w4ax:  # the channel permutation, applied upstream to both operands
+        perm = outlier_first_permutation(c["seed"] + rank, K)
+        Wn, Xn = np.ascontiguousarray(Wn[:, perm]), np.ascontiguousarray(Xn[:, perm])
+    W = torch.from_numpy(Wn).to(dev)
+    X = torch.from_numpy(Xn).to(dev)
+    del Wn, Xn
     packed, s1 = q.qoq_pack_weights(W, g=G)
     torch.cuda.synchronize()
     pk_ev0, pk_ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -325,17 +351,22 @@ def bench_workload(q, torch, c: dict, args, dev, stream, dist, rank: int) -> dic
     del W
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    ws_bytes = q.qoq_gemm_workspace_bytes(M, N, K, G)
-    set_bytes = packed.numel() + 2 * N + 2 * M * K + M * K + 2 * M + 2 * M * N + ws_bytes
+    ws_bytes = q.qoq_w4ax_workspace_bytes(M, N, K, G) if w4ax else q.qoq_gemm_workspace_bytes(M, N, K, G)
+    act_row = q.qoq_w4ax_act_bytes(1, K, n8) if w4ax else K
+    set_bytes = packed.numel() + 2 * N + 2 * M * K + M * act_row + 2 * M * (K // 128) + 2 * M * N + ws_bytes
     nsets = max(2, int(np.ceil(3 * l2 / set_bytes)))
     sets = []
     for _ in range(nsets):
-        sets.append(dict(
-            packed=packed.clone(), s1=s1.clone(), X=X.clone(),
-            Xq=torch.empty((M, K), dtype=torch.int8, device=dev),
-            sx=torch.empty(M, dtype=torch.float16, device=dev),
-            Y=torch.empty((M, N), dtype=torch.float16, device=dev),
-            ws=torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)))
+        st_ = dict(packed=packed.clone(), s1=s1.clone(), X=X.clone(),
+                   Y=torch.empty((M, N), dtype=torch.float16, device=dev),
+                   ws=torch.zeros(ws_bytes, dtype=torch.uint8, device=dev))
+        if w4ax:
+            st_["Xa"] = torch.empty((M, act_row), dtype=torch.uint8, device=dev)
+            st_["sxb"] = torch.empty((M, K // 128), dtype=torch.float16, device=dev)
+        else:
+            st_["Xq"] = torch.empty((M, K), dtype=torch.int8, device=dev)
+            st_["sx"] = torch.empty(M, dtype=torch.float16, device=dev)
+        sets.append(st_)
     del packed, s1
 
     # the step's activation quantizer: the per-token quantizer alone, or fused
@@ -345,7 +376,9 @@ def bench_workload(q, torch, c: dict, args, dev, stream, dist, rank: int) -> dic
 
     def quantize(s, X_src=None):
         src = s["X"] if X_src is None else X_src
-        if norm_step:
+        if w4ax:
+            q.qoq_quant_act_w4ax(src, n8, Xa=s["Xa"], sxb=s["sxb"])
+        elif norm_step:
             q.qoq_norm_quant_act(src, gamma, kind="rms", eps=1e-6, Xq=s["Xq"], sx=s["sx"])
         else:
             q.qoq_quant_act(src, Xq=s["Xq"], sx=s["sx"])
@@ -353,7 +386,12 @@ def bench_workload(q, torch, c: dict, args, dev, stream, dist, rank: int) -> dic
     gemm_call = q.qoq_w4a8_gemm_zero_folded if args.variant == "zero_folded" else q.qoq_w4a8_gemm
 
     def gemm(s, Y=None):
-        gemm_call(s["Xq"], s["sx"], s["packed"], s["s1"], N, g=G, Y=s["Y"] if Y is None else Y, workspace=s["ws"])
+        if w4ax:
+            q.qoq_w4ax_gemm(s["Xa"], s["sxb"], n8, s["packed"], s["s1"], K, N, g=G, Y=s["Y"] if Y is None else Y,
+                            workspace=s["ws"])
+        else:
+            gemm_call(s["Xq"], s["sx"], s["packed"], s["s1"], N, g=G, Y=s["Y"] if Y is None else Y,
+                      workspace=s["ws"])
 
     def steps_full(n: int):
         for i in range(n):
@@ -489,7 +527,7 @@ def bench_workload(q, torch, c: dict, args, dev, stream, dist, rank: int) -> dic
     ms_per_step, gemm_ms, act_ms, copy_ms, direct_ms = max_over_ranks(
         dist, [med(step_regions), med(gemm_regions), med(act_regions), med(copy_regions), med(direct_regions)],
         dev)
-    quant_name = "qoq_norm_quant_act" if norm_step else "qoq_quant_act"
+    quant_name = "qoq_quant_act_w4ax" if w4ax else ("qoq_norm_quant_act" if norm_step else "qoq_quant_act")
     if direct_ms <= copy_ms:
         e2e_ms, e2e_how = direct_ms, (
             f"public API per step with host buffers: {quant_name} reads X in place from pinned host memory and "
@@ -507,7 +545,7 @@ def bench_workload(q, torch, c: dict, args, dev, stream, dist, rank: int) -> dic
         regions={"step": step_regions, "gemm": gemm_regions, "quantizer": act_regions},
         l2_policy=f"rotating pool of {nsets} buffer sets, {nsets * set_bytes / 1e6:.0f} MB "
                   f"(>= 3x L2 {l2 / 1e6:.0f} MB)",
-        norm_step=norm_step, quant_name=quant_name)
+        norm_step=norm_step, quant_name=quant_name, n8=n8 if w4ax else None)
     del sets
     torch.cuda.empty_cache()
     return out
@@ -518,7 +556,7 @@ def config_summary(c: dict, r: dict, args, world: int, peaks: dict, peak_src: st
     M, N, K = c["M"], c["N"], c["K"]
     G = c.get("g", 128)
     ops = 2.0 * M * N * K
-    roof = roofline_of(M, N, K, G, r["gemm_ms"], args.steps, peaks, peak_src)
+    roof = roofline_of(M, N, K, G, r["gemm_ms"], args.steps, peaks, peak_src, r["n8"])
     return {
         "workload": c["name"], "M": M, "N": N, "K": K, "g": G,
         "value": job_tops(world, ops, r["ms_per_step"]), "unit": UNIT, "ms_per_step": r["ms_per_step"],
@@ -557,12 +595,14 @@ def run_ours(args, c: dict) -> None:
     clocks = sampler.stop()
 
     ops = 2.0 * M * N * K
-    nbytes = algorithmic_bytes(M, N, K, G)
+    nbytes = algorithmic_bytes(M, N, K, G, r["n8"])
     value = job_tops(world, ops, r["ms_per_step"])
-    roof = roofline_of(M, N, K, G, r["gemm_ms"], args.steps, peaks, peak_src)
+    roof = roofline_of(M, N, K, G, r["gemm_ms"], args.steps, peaks, peak_src, r["n8"])
     roof["traffic"] = args.traffic
     if roof["traffic"] is None:
-        if G == 128:
+        if r["n8"] is not None or args.variant != "direct":
+            roof["traffic_source"] = "no ncu record for this path"
+        elif G == 128:
             roof["traffic"], roof["traffic_source"] = recorded_traffic(c["name"])
         else:
             roof["traffic_source"] = f"no ncu record at g = {G}"
@@ -572,7 +612,7 @@ def run_ours(args, c: dict) -> None:
     # element, 2 per token for s_x, plus gamma (2K) when the norm is fused
     act_bytes = nbytes["act"] + (2 * K if r["norm_step"] else 0)
     act_gbs = act_bytes / (r["act_ms"] * 1e-3) / 1e9
-    act_roof = {"kernel": "qoq_norm_quant_act (RMSNorm)" if r["norm_step"] else "qoq_quant_act",
+    act_roof = {"kernel": r["quant_name"] + (" (RMSNorm)" if r["norm_step"] else ""),
                 "bound": "hbm", "achieved": act_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": act_gbs / peaks["hbm_gbs"], "algorithmic_bytes_per_launch": act_bytes,
                 "ms_per_launch": r["act_ms"],
@@ -591,7 +631,9 @@ def run_ours(args, c: dict) -> None:
                        f"({'a CUDA graph of K steps, replayed' if r['use_graph'] else 'direct launches'}); "
                        "median region reported"),
             "mma": "tcgen05 kind::f16, exact integer operands, fp32 TMEM folded to int32",
-            "variant": ("qoq_w4a8_gemm_zero_folded (q4*s2 in the main loop, zero points' share subtracted in "
+            "variant": ("qoq_w4ax_gemm (W4Ax: the outlier channels permuted into the first "
+                        f"{r['n8']} 8-bit 128-channel block(s), 4-bit blocks elsewhere)" if r["n8"] is not None else
+                        "qoq_w4a8_gemm_zero_folded (q4*s2 in the main loop, zero points' share subtracted in "
                         "the epilogue)" if args.variant == "zero_folded" else "qoq_w4a8_gemm")}),
         "regions_ms_per_step": {k: [round(v, 6) for v in vs] for k, vs in r["regions"].items()},
         "hbm_gb_per_s_step": world * nbytes["step"] / (r["ms_per_step"] * 1e-3) / 1e9,
@@ -604,7 +646,8 @@ def run_ours(args, c: dict) -> None:
         "clocks": clocks,
         # inside one timed region of K steps: act-quant + GEMM per step, and
         # for M > 64 also the B-operand convert
-        "gpu_launches": ((2 if M <= 64 else 3) + (1 if args.variant == "zero_folded" else 0)) * args.steps,
+        "gpu_launches": ((3 if r["n8"] is not None else (2 if M <= 64 else 3)) +
+                         (1 if args.variant == "zero_folded" else 0)) * args.steps,
         "pack_ms": r["pack_ms"],
     }
 
@@ -657,6 +700,9 @@ def main() -> None:
                     help="activation quantizer of the step: qoq_quant_act (default) or qoq_norm_quant_act (RMSNorm fused)")
     ap.add_argument("--variant", choices=["direct", "zero_folded"], default="direct",
                     help="GEMM entry point: qoq_w4a8_gemm (default) or qoq_w4a8_gemm_zero_folded")
+    ap.add_argument("--path", choices=["w4a8", "w4ax"], default="w4a8",
+                    help="w4a8 (default): QoQ W4A8; w4ax: 4-bit activation blocks with 8-bit outlier blocks")
+    ap.add_argument("--n8", type=int, default=1, help="W4Ax: leading 8-bit blocks (outlier channels permuted there)")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle CPU timing (headline)")
     ap.add_argument("--cpu-budget-per-config", type=float, default=3.0,
                     help="seconds of oracle CPU timing per workload in per_config")

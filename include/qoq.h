@@ -240,6 +240,64 @@ qoq_status qoq_w4a8_gemm_zero_folded(int M, int N, int K, int g, const int8_t* X
                                      void* workspace, size_t ws_bytes, qoq_stream_t stream);
 
 /*
+ * W4Ax: 4-bit activation blocks with 8-bit outlier blocks (COMET explainer,
+ * bookshelf: FMPQ quantizes activations in blocks of 128 channels, the size
+ * of the tensor-core tile, keeping the blocks that hold the outlier channels
+ * at 8 bits and the rest at 4 bits; a channel permutation clusters the
+ * outlier channels into few blocks, and the W4Ax kernel scales each block's
+ * partial sums on the general-purpose cores).  Here the permutation is
+ * applied upstream (to this layer's weight columns and to the producer of
+ * its activations) so that the outlier blocks come first: the n8 leading
+ * blocks are 8-bit.
+ *
+ * Activation row layout ("Xa"): per token row, blocks in order; an 8-bit
+ * block is 128 int8 codes; a 4-bit block is 64 bytes, byte i holding the code
+ * of channel 2i in its low nibble and that of channel 2i + 1 in its high
+ * nibble, two's complement.  Row stride 128 n8 + 64 (K/128 - n8) bytes;
+ * qoq_w4ax_act_bytes(M, K, n8) is M times that (0 for bad arguments).
+ */
+size_t qoq_w4ax_act_bytes(int M, int K, int n8);
+
+/*
+ * Per-(token, block) symmetric quantization for W4Ax:
+ *   q = 127 for blocks b < n8, 7 otherwise,
+ *   sxb[m][b] = fp16_rn(fp32(max over the block |X[m,k]|) / q) (IEEE fp32 divide),
+ *   code = clamp(rint(X[m,k] / sxb[m][b]), -q, q)  (fp32 divide, ties even);
+ *   an all-zero block gets scale 0 and codes 0.
+ * In:  X_f16 [M][K] fp16 bits; 0 <= n8 <= K/128 (else QOQ_ERR_UNSUPPORTED).
+ * Out: Xa (qoq_w4ax_act_bytes(M, K, n8) bytes, the layout above),
+ *      sxb_f16 [M][K/128] fp16 bits.
+ * Shape and pointer rules as qoq_quant_act; launched the same way
+ * (programmatic dependent launch).
+ */
+qoq_status qoq_quant_act_w4ax(int M, int K, int n8, const uint16_t* X_f16, uint8_t* Xa,
+                              uint16_t* sxb_f16, qoq_stream_t stream);
+
+/* Bytes of workspace qoq_w4ax_gemm needs (host-only; 0 for a bad shape);
+ * zero-filled once by the caller, like qoq_w4a8_gemm's. */
+size_t qoq_w4ax_workspace_bytes(int M, int N, int K, int g);
+
+/*
+ * The W4Ax GEMM with the progressively quantized 4-bit weights of
+ * qoq_pack_weights (w8 = (q4 - z) * s2):
+ *   acc_b[m,n] = sum over the channels k of block b of code[m,k] * w8[n,k]  (exact),
+ *   Y[m,n] = fp16_rn(s1[n] * sum_b sxb[m][b] * acc_b[m,n]),
+ * the sum over blocks in fp32 on the GPU (the oracle takes it in double; the
+ * two agree within the parity tolerance).  For a tile whose K range is split
+ * over two or more CTAs the fp32 partial sums meet through atomic additions,
+ * so Y may differ between calls by the rounding of the last fp32 bit.
+ * acc_debug (nullable): sum_b acc_b as int32, written by a second launch of
+ * the W4A8 kernel on the same operand copy.
+ * Every M runs on the 128-token-tile kernel (COMET's kernel targets the
+ * compute-bound, large-batch regime).  Errors as qoq_w4a8_gemm, plus
+ * QOQ_ERR_UNSUPPORTED for n8 outside [0, K/128]; workspace:
+ * qoq_w4ax_workspace_bytes.
+ */
+qoq_status qoq_w4ax_gemm(int M, int N, int K, int g, int n8, const uint8_t* Xa, const uint16_t* sxb_f16,
+                         const uint8_t* packed, const uint16_t* s1_f16, uint16_t* Y_f16, int32_t* acc_debug,
+                         void* workspace, size_t ws_bytes, qoq_stream_t stream);
+
+/*
  * qoq_w4a8_gemm without a caller-supplied workspace.  The paper has no
  * counterpart: this is a service for callers that cannot allocate device
  * memory.  Examples are a plugin given only its input and output buffers by a

@@ -174,3 +174,29 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(binding._build, "LIB", str(tmp_path / "missing.so"))
     with pytest.raises(binding.QoQError):
         binding.lib()
+
+
+def test_w4ax_sizes_and_validation():
+    """W4Ax activation bytes follow the documented row layout; argument errors
+    return before any device access (fake pointers)."""
+    L = _lib()
+    for M, K, n8 in [(1, 128, 0), (1, 128, 1), (16, 4096, 1), (4096, 8192, 5)]:
+        G = K // 128
+        assert q.qoq_w4ax_act_bytes(M, K, n8) == M * (128 * n8 + 64 * (G - n8))
+    assert q.qoq_w4ax_act_bytes(16, 4096, 33) == 0 and q.qoq_w4ax_act_bytes(16, 4096, -1) == 0
+    assert q.qoq_w4ax_workspace_bytes(16, 12288, 4096) > 0 and q.qoq_w4ax_workspace_bytes(16, 100, 4096) == 0
+    assert L.qoq_quant_act_w4ax(16, 512, 5, FAKE, FAKE, FAKE, None) == 3
+    assert L.qoq_quant_act_w4ax(16, 512, 1, None, FAKE, FAKE, None) == 1
+    assert L.qoq_quant_act_w4ax(16, 500, 1, FAKE, FAKE, FAKE, None) == 2
+    assert L.qoq_quant_act_w4ax(16, 512, 1, FAKE, MIS, FAKE, None) == 4
+    ws = q.qoq_w4ax_workspace_bytes(16, 256, 512)
+
+    def call(M=16, N=256, K=512, g=128, n8=1, Xa=FAKE, sx=FAKE, pk=FAKE, s1=FAKE, Y=FAKE, acc=None, w=FAKE, wb=ws):
+        return L.qoq_w4ax_gemm(M, N, K, g, n8, Xa, sx, pk, s1, Y, acc, w, wb, None)
+
+    assert call(Xa=None) == 1 and call(Y=None) == 1
+    assert call(n8=5) == 3 and call(n8=-1) == 3 and call(g=96) == 3
+    assert call(N=200) == 2 and call(M=0) == 2
+    assert call(pk=MIS) == 4 and call(acc=MIS) == 4
+    assert call(wb=ws - 1) == 5 and call(w=None) == 5
+

@@ -14,7 +14,8 @@ _EXPORTS = (
     "qoq_gemm_workspace_bytes", "qoq_last_device_status", "qoq_pack_weights",
     "qoq_norm_quant_act", "qoq_packed_weight_bytes", "qoq_quant_act", "qoq_set_debug", "qoq_status_str",
     "qoq_unpack_weights_debug", "qoq_version", "qoq_w4a8_gemm", "qoq_w4a8_gemm_no_alloc",
-    "qoq_w4a8_gemm_zero_folded", "workspace_for",
+    "qoq_w4a8_gemm_zero_folded", "qoq_w4ax_act_bytes", "qoq_quant_act_w4ax", "qoq_w4ax_workspace_bytes",
+    "qoq_w4ax_gemm", "workspace_for",
 )
 
 __all__ = list(_EXPORTS)

@@ -23,6 +23,7 @@ EXPORTED = (
     "qoq_status_str", "qoq_version", "qoq_packed_weight_bytes", "qoq_gemm_workspace_bytes",
     "qoq_pack_weights", "qoq_quant_act", "qoq_norm_quant_act", "qoq_w4a8_gemm", "qoq_unpack_weights_debug",
     "qoq_last_device_status", "qoq_set_debug", "qoq_w4a8_gemm_no_alloc", "qoq_w4a8_gemm_zero_folded",
+    "qoq_w4ax_act_bytes", "qoq_quant_act_w4ax", "qoq_w4ax_workspace_bytes", "qoq_w4ax_gemm",
 )
 
 _LOCK = threading.Lock()
@@ -69,6 +70,14 @@ def lib() -> ctypes.CDLL:
             L.qoq_norm_quant_act.restype = i32
             L.qoq_w4a8_gemm.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P, sz, P]
             L.qoq_w4a8_gemm.restype = i32
+            L.qoq_w4ax_act_bytes.argtypes = [i32, i32, i32]
+            L.qoq_w4ax_act_bytes.restype = sz
+            L.qoq_w4ax_workspace_bytes.argtypes = [i32, i32, i32, i32]
+            L.qoq_w4ax_workspace_bytes.restype = sz
+            L.qoq_quant_act_w4ax.argtypes = [i32, i32, i32, P, P, P, P]
+            L.qoq_quant_act_w4ax.restype = i32
+            L.qoq_w4ax_gemm.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P, P, P, sz, P]
+            L.qoq_w4ax_gemm.restype = i32
             L.qoq_w4a8_gemm_zero_folded.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P, sz, P]
             L.qoq_w4a8_gemm_zero_folded.restype = i32
             L.qoq_w4a8_gemm_no_alloc.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P]
@@ -256,6 +265,53 @@ def qoq_w4a8_gemm_no_alloc(Xq, sx, packed, s1, N: int | None = None, g: int = 12
                                         _dev(s1, torch.float16, "s1", (N,)),
                                         _dev(Y, torch.float16, "Y", (M, N), host_ok=True), acc_ptr, _stream(stream))
     _check(code, "qoq_w4a8_gemm_no_alloc")
+    return Y
+
+
+def qoq_w4ax_act_bytes(M: int, K: int, n8: int) -> int:
+    return int(lib().qoq_w4ax_act_bytes(M, K, n8))
+
+
+def qoq_w4ax_workspace_bytes(M: int, N: int, K: int, g: int = 128) -> int:
+    return int(lib().qoq_w4ax_workspace_bytes(M, N, K, g))
+
+
+def qoq_quant_act_w4ax(X, n8: int, Xa=None, sxb=None, stream=None):
+    """W4Ax activations of fp16 X [M][K]: the n8 leading 128-channel blocks
+    8-bit, the rest 4-bit (two codes per byte), one fp16 scale per (token,
+    block).  Returns (Xa uint8 [M][row bytes], sxb fp16 [M][K/128])."""
+    torch = _torch()
+    M, K = X.shape
+    dev = _out_device(X)
+    row = qoq_w4ax_act_bytes(1, K, n8)
+    if Xa is None:
+        Xa = torch.empty((M, row), dtype=torch.uint8, device=dev)
+    if sxb is None:
+        sxb = torch.empty((M, K // 128), dtype=torch.float16, device=dev)
+    _check(lib().qoq_quant_act_w4ax(M, K, n8, _dev(X, torch.float16, "X", (M, K), host_ok=True),
+                                    _dev(Xa, torch.uint8, "Xa"), _dev(sxb, torch.float16, "sxb", (M, K // 128)),
+                                    _stream(stream)), "qoq_quant_act_w4ax")
+    return Xa, sxb
+
+
+def qoq_w4ax_gemm(Xa, sxb, n8: int, packed, s1, K: int, N: int | None = None, g: int = 128, Y=None,
+                  acc_debug=None, workspace=None, stream=None):
+    """Y fp16 [M][N] = the W4Ax GEMM of (Xa, sxb) with the packed 4-bit weights."""
+    torch = _torch()
+    M = sxb.shape[0]
+    if N is None:
+        N = s1.shape[0]
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.float16, device=sxb.device)
+    if workspace is None:
+        workspace = torch.zeros(max(qoq_w4ax_workspace_bytes(M, N, K, g), 16), dtype=torch.uint8,
+                                device=sxb.device)
+    acc_ptr = None if acc_debug is None else _dev(acc_debug, torch.int32, "acc_debug", (M, N))
+    code = lib().qoq_w4ax_gemm(M, N, K, g, n8, _dev(Xa, torch.uint8, "Xa"),
+                               _dev(sxb, torch.float16, "sxb", (M, K // 128)), _dev(packed, torch.uint8, "packed"),
+                               _dev(s1, torch.float16, "s1", (N,)), _dev(Y, torch.float16, "Y", (M, N), host_ok=True),
+                               acc_ptr, _dev(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream))
+    _check(code, "qoq_w4ax_gemm")
     return Y
 
 

@@ -315,6 +315,65 @@ cudaError_t launch_norm_kind(const RowLayout& L, cudaLaunchConfig_t& cfg, int M,
   return cudaErrorInvalidValue;
 }
 
+// ----------------------------------------------------------------- W4Ax --
+// COMET explainer, FMPQ: activations in 128-channel blocks, the outlier
+// channels clustered (by a channel permutation) into the n8 leading blocks,
+// which stay at 8 bits, every other block at 4 bits; one symmetric scale per
+// (token, block):
+//   s = fp16_rn(fp32(max |x|) / q) (IEEE fp32 divide), code = clamp(rint(x / s), +-q),
+// q = 127 for 8-bit blocks, 7 for 4-bit blocks.  Storage per token row, blocks
+// in order: an 8-bit block is 128 int8 codes, a 4-bit block 64 bytes with the
+// code of channel 2i in the low nibble of byte i and that of 2i + 1 in the
+// high nibble (two's complement).  One warp per (row, pair of blocks): each
+// half-warp owns a block, 8 channels per lane, and reduces its max-abs with
+// shuffles inside the half.
+__global__ void __launch_bounds__(256) act_quant_w4ax_kernel(const uint16_t* __restrict__ X, uint8_t* __restrict__ Xa,
+                                                             uint16_t* __restrict__ sxb, int M, int K, int n8) {
+  grid_dep_launch_dependents();
+  grid_dep_wait();  // X may come from the preceding kernel; Xa and the scales may still be read by it
+  const int G = K / 128;
+  const int pairs = (G + 1) / 2;
+  const long long wid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (wid >= (long long)M * pairs) return;  // whole warps
+  const int lane = threadIdx.x & 31, l = lane & 15;
+  const int m = (int)(wid / pairs);
+  const int b = 2 * (int)(wid % pairs) + (lane >> 4);
+  const bool live = b < G;
+  uint4 v = make_uint4(0, 0, 0, 0);
+  if (live) v = __ldcg(reinterpret_cast<const uint4*>(X + (size_t)m * K + (size_t)b * 128) + l);
+  float amax = absmax8(v, 0.0f);
+#pragma unroll
+  for (int off = 8; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  if (!live) return;
+  const bool eight = b < n8;
+  const float q = eight ? 127.0f : 7.0f;
+  __half sh = __float2half_rn(0.0f);
+  if (amax > 0.0f) sh = __float2half_rn(__fdiv_rn(amax, q));
+  const float sf = __half2float(sh);
+  const float rf = sf != 0.0f ? __frcp_rn(sf) : 0.0f;
+  if (l == 0) sxb[(size_t)m * G + b] = __half_as_ushort(sh);
+  const __half* h = reinterpret_cast<const __half*>(&v);
+  int c[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    c[i] = sf != 0.0f ? (int)fminf(q, fmaxf(-q, rint_div_fp16(__half2float(h[i]), sf, rf))) : 0;
+  const size_t row_bytes = (size_t)128 * n8 + (size_t)64 * (G - n8);
+  uint8_t* row = Xa + (size_t)m * row_bytes;
+  if (eight) {
+    uint2 out;
+    out.x = (uint32_t)(c[0] & 0xff) | (uint32_t)(c[1] & 0xff) << 8 | (uint32_t)(c[2] & 0xff) << 16 |
+            (uint32_t)(c[3] & 0xff) << 24;
+    out.y = (uint32_t)(c[4] & 0xff) | (uint32_t)(c[5] & 0xff) << 8 | (uint32_t)(c[6] & 0xff) << 16 |
+            (uint32_t)(c[7] & 0xff) << 24;
+    *reinterpret_cast<uint2*>(row + (size_t)128 * b + 8 * l) = out;
+  } else {
+    uint32_t out = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) out |= (uint32_t)(c[i] & 0xf) << (4 * i);
+    *reinterpret_cast<uint32_t*>(row + (size_t)128 * n8 + (size_t)64 * (b - n8) + 4 * l) = out;
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_act_quant(int M, int K, const uint16_t* X, int8_t* Xq, uint16_t* sx,
@@ -335,6 +394,19 @@ cudaError_t launch_norm_quant(int M, int K, int kind, float eps, const uint16_t*
   cudaLaunchConfig_t cfg = row_config(L, s, attr);
   return kind == 1 ? launch_norm_kind<true>(L, cfg, M, K, eps, X, gamma, beta, Xq, sx)
                    : launch_norm_kind<false>(L, cfg, M, K, eps, X, gamma, beta, Xq, sx);
+}
+
+cudaError_t launch_act_quant_w4ax(int M, int K, int n8, const uint16_t* X, uint8_t* Xa, uint16_t* sxb,
+                                  cudaStream_t s) {
+  const long long warps = (long long)M * ((K / 128 + 1) / 2);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((warps + 7) / 8));
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1] = {pdl_attr()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, act_quant_w4ax_kernel, X, Xa, sxb, M, K, n8);
 }
 
 }  // namespace qoq

@@ -182,6 +182,49 @@ qoq_status qoq_w4a8_gemm_zero_folded(int M, int N, int K, int g, const int8_t* X
   return gemm_entry(M, N, K, g, Xq, sx_f16, packed, s1_f16, Y_f16, acc_debug, workspace, ws_bytes, stream, true);
 }
 
+size_t qoq_w4ax_act_bytes(int M, int K, int n8) {
+  if (!shape_ok_mk(M, K) || n8 < 0 || n8 > K / kGroup) return 0;
+  return (size_t)M * ((size_t)128 * n8 + (size_t)64 * (K / kGroup - n8));
+}
+
+size_t qoq_w4ax_workspace_bytes(int M, int N, int K, int g) {
+  if (!shape_ok_mk(M, K) || !shape_ok_nk(N, K) || !qoq::group_size_ok(K, g)) return 0;
+  return qoq::w4ax_ws_layout(M, N, K).total;
+}
+
+qoq_status qoq_quant_act_w4ax(int M, int K, int n8, const uint16_t* X_f16, uint8_t* Xa, uint16_t* sxb_f16,
+                              qoq_stream_t stream) {
+  if (!X_f16 || !Xa || !sxb_f16) return QOQ_ERR_NULL;
+  if (!shape_ok_mk(M, K)) return QOQ_ERR_SHAPE;
+  if (n8 < 0 || n8 > K / kGroup) return QOQ_ERR_UNSUPPORTED;
+  if (!aligned16(X_f16) || !aligned16(Xa) || !aligned16(sxb_f16)) return QOQ_ERR_MISALIGNED;
+  qoq_status st = device_info(nullptr);
+  if (st != QOQ_OK) return st;
+  return from_cuda(qoq::launch_act_quant_w4ax(M, K, n8, X_f16, Xa, sxb_f16, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+qoq_status qoq_w4ax_gemm(int M, int N, int K, int g, int n8, const uint8_t* Xa, const uint16_t* sxb_f16,
+                         const uint8_t* packed, const uint16_t* s1_f16, uint16_t* Y_f16, int32_t* acc_debug,
+                         void* workspace, size_t ws_bytes, qoq_stream_t stream) {
+  if (!Xa || !sxb_f16 || !packed || !s1_f16 || !Y_f16) return QOQ_ERR_NULL;
+  if (!shape_ok_mk(M, K) || !shape_ok_nk(N, K)) return QOQ_ERR_SHAPE;
+  if (!qoq::group_size_ok(K, g) || n8 < 0 || n8 > K / kGroup) return QOQ_ERR_UNSUPPORTED;
+  if (!aligned16(Xa) || !aligned16(sxb_f16) || !aligned16(packed) || !aligned16(s1_f16) || !aligned16(Y_f16) ||
+      (acc_debug && !aligned16(acc_debug)))
+    return QOQ_ERR_MISALIGNED;
+  if (!workspace || ws_bytes < qoq_w4ax_workspace_bytes(M, N, K, g)) return QOQ_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return QOQ_ERR_MISALIGNED;
+  int sms = 0;
+  qoq_status st = device_info(&sms);
+  if (st != QOQ_OK) return st;
+  unsigned long long tmo = g_timeout_ns.load();
+  if (tmo == 0) tmo = kDefaultTimeoutNs;
+  unsigned call_id = g_call_id.fetch_add(2) + 1;  // two ids: the W4Ax launch and the integer-sum launch
+  if (call_id == 0 || call_id + 1 == 0) call_id = g_call_id.fetch_add(2) + 1;
+  return from_cuda(qoq::launch_w4ax(M, N, K, g, n8, Xa, sxb_f16, packed, s1_f16, Y_f16, acc_debug, workspace, sms,
+                                    tmo, call_id, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 qoq_status qoq_unpack_weights_debug(int N, int K, int g, const uint8_t* packed, uint8_t* q4,
                                     uint8_t* s2, uint8_t* z, qoq_stream_t stream) {
   if (!packed || !q4 || !s2 || !z) return QOQ_ERR_NULL;

@@ -65,8 +65,10 @@ struct BulkCfg {
   static_assert(SMEM_BYTES <= kSmemBudget, "shared memory");
 };
 
-// ZF: the zero-point-folded variant (see zero_point_share).
-template <int GPT, bool ZF>
+// ZF: the zero-point-folded variant (see zero_point_share).  AX: the W4Ax
+// product (one accumulator per group, scaled per activation block; see
+// epilogue_role_ax).
+template <int GPT, bool ZF, bool AX = false>
 __global__ void __launch_bounds__(BulkCfg<GPT>::THREADS, 1) gemm_bulk_kernel(const __grid_constant__ GemmParams p) {
   using C = BulkCfg<GPT>;
   constexpr int BN = C::BN;
@@ -176,7 +178,7 @@ __global__ void __launch_bounds__(BulkCfg<GPT>::THREADS, 1) gemm_bulk_kernel(con
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer --
     grid_dep_wait();
-    mma_role<BN, C::NACC, C::NABUF, C::ACOL0, ZF ? kFoldGroupsZf : kFoldGroups>(
+    mma_role<BN, C::NACC, C::NABUF, C::ACOL0, AX ? 1 : (ZF ? kFoldGroupsZf : kFoldGroups)>(
         p, tmem, bar_afull, bar_aempty, bar_accfull, bar_accempty, bar_drain,
         [&](uint32_t gi, int) { return sbase + (uint32_t)((gi % C::STAGES) * C::B_BYTES); },
         [&](uint32_t gi) { return bar_empty + 8 * (gi % C::STAGES); });
@@ -230,8 +232,12 @@ __global__ void __launch_bounds__(BulkCfg<GPT>::THREADS, 1) gemm_bulk_kernel(con
   } else {
     // ------------------------------------------------------------ epilogue --
     grid_dep_wait();
-    epilogue_role<BN, C::NEPI, C::NACC, ZF, C::TILE>(p, tmem, C::EPI_WARP0, bar_accfull, bar_accempty,
-                                                     reinterpret_cast<volatile int*>(smem + C::FLAG_OFF));
+    if constexpr (AX)
+      epilogue_role_ax<BN, C::NEPI, C::NACC>(p, tmem, C::EPI_WARP0, bar_accfull, bar_accempty,
+                                            reinterpret_cast<volatile int*>(smem + C::FLAG_OFF));
+    else
+      epilogue_role<BN, C::NEPI, C::NACC, ZF, C::TILE>(p, tmem, C::EPI_WARP0, bar_accfull, bar_accempty,
+                                                       reinterpret_cast<volatile int*>(smem + C::FLAG_OFF));
   }
 
   tc_fence_before();
@@ -264,6 +270,62 @@ __global__ void __launch_bounds__(256) convert_kernel(const ConvertParams c) {
   }
 }
 
+// Sixteen 4-bit two's-complement codes (8 bytes, channel 2i in the low nibble
+// of byte i) -> sixteen int8 lanes in channel order: flip each code's sign bit
+// (offset binary t = code + 8 in [0, 15]), split even and odd channels into
+// bytes, interleave them, and sign-extend with ((t | 0x80) - 8) ^ 0x80 = t - 8
+// per byte, which borrows across no byte boundary.
+__device__ __forceinline__ uint4 expand_nibbles16(uint2 h) {
+  uint32_t out[4];
+  const uint32_t w2[2] = {h.x, h.y};
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const uint32_t t = w2[i] ^ 0x88888888u;  // offset binary: code + 8
+    const uint32_t ev = t & 0x0F0F0F0Fu, od = (t >> 4) & 0x0F0F0F0Fu;
+    uint32_t a, b;
+    asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(a) : "r"(ev), "r"(od));  // channels 0..3 of the word
+    asm("prmt.b32 %0, %1, %2, 0x7362;" : "=r"(b) : "r"(ev), "r"(od));  // channels 4..7
+    out[2 * i] = ((a | 0x80808080u) - 0x08080808u) ^ 0x80808080u;
+    out[2 * i + 1] = ((b | 0x80808080u) - 0x08080808u) ^ 0x80808080u;
+  }
+  return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+// W4Ax: the fp16 B-operand copy ([MT][G][2][128][64], as convert_kernel
+// writes it) from the mixed activation rows (n8 leading 8-bit blocks of 128
+// bytes, then 4-bit blocks of 64 bytes), and the block scales transposed to
+// [G][MT * 128] (0 for tokens past M) for the epilogue's per-group loads.
+__global__ void __launch_bounds__(256) convert_w4ax_kernel(const ConvertAxParams c) {
+  grid_dep_launch_dependents();  // the GEMM may launch and start streaming weights
+  grid_dep_wait();               // the activations come from the preceding kernel
+  const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  const int G = c.K / kGroup;
+  const size_t row_bytes = (size_t)128 * c.n8 + (size_t)64 * (G - c.n8);
+  const long long total = (long long)c.MT * 128 * (c.K / 16);
+  for (long long idx = tid; idx < total; idx += stride) {
+    const int m = (int)(idx / (c.K / 16));
+    const int k0 = (int)(idx % (c.K / 16)) * 16;
+    const int b = k0 / kGroup, kc = (k0 % kGroup) / 16;
+    uint4 raw = make_uint4(0, 0, 0, 0);
+    if (m < c.M) {
+      const uint8_t* rowp = c.Xa + (size_t)m * row_bytes;
+      if (b < c.n8)
+        raw = __ldcg(reinterpret_cast<const uint4*>(rowp + (size_t)128 * b + 16 * kc));
+      else
+        raw = expand_nibbles16(__ldcg(reinterpret_cast<const uint2*>(rowp + (size_t)128 * c.n8 +
+                                                                   (size_t)64 * (b - c.n8) + 8 * kc)));
+    }
+    const int mt = m / 128, r = m % 128;
+    store_b_chunk(reinterpret_cast<uint8_t*>(c.xh + (size_t)(mt * G + b) * 128 * kGroup), 128, r, kc, raw);
+  }
+  const long long nsc = (long long)G * c.sxT_ld;
+  for (long long idx = tid; idx < nsc; idx += stride) {
+    const int b = (int)(idx / c.sxT_ld), m = (int)(idx % c.sxT_ld);
+    c.sxT[idx] = m < c.M ? c.sxb[(size_t)m * G + b] : (uint16_t)0;
+  }
+}
+
 // Row sums of Xq per 128-channel k-tile, RS[j][m] (0 for M <= m < rs_ld),
 // for the zero-point-folded variant.  One thread per (j, m): 128 bytes read,
 // summed four signed bytes at a time.
@@ -290,7 +352,7 @@ __global__ void __launch_bounds__(256) rowsum_kernel(const RowSumParams r) {
   }
 }
 
-template <int GPT, bool ZF>
+template <int GPT, bool ZF, bool AX = false>
 cudaError_t launch_bulk_g(const GemmParams& p, cudaStream_t s) {
   using C = BulkCfg<GPT>;
   static std::mutex mu;
@@ -298,7 +360,7 @@ cudaError_t launch_bulk_g(const GemmParams& p, cudaStream_t s) {
   cudaError_t e;
   {
     std::lock_guard<std::mutex> lock(mu);
-    e = set_smem_attr_once(gemm_bulk_kernel<GPT, ZF>, C::SMEM_BYTES, done_mask);
+    e = set_smem_attr_once(gemm_bulk_kernel<GPT, ZF, AX>, C::SMEM_BYTES, done_mask);
   }
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -309,7 +371,16 @@ cudaError_t launch_bulk_g(const GemmParams& p, cudaStream_t s) {
   cudaLaunchAttribute attr[1] = {pdl_attr()};
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_bulk_kernel<GPT, ZF>, p);
+  return cudaLaunchKernelEx(&cfg, gemm_bulk_kernel<GPT, ZF, AX>, p);
+}
+
+cudaError_t launch_bulk_ax(const GemmParams& p, cudaStream_t s) {
+  switch (p.gpt) {
+    case 1: return launch_bulk_g<1, false, true>(p, s);
+    case 2: return launch_bulk_g<2, false, true>(p, s);
+    case 4: return launch_bulk_g<4, false, true>(p, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_bulk(const GemmParams& p, bool zero_folded, cudaStream_t s) {
@@ -419,6 +490,77 @@ cudaError_t launch_gemm(int M, int N, int K, int g, const int8_t* Xq, const uint
   cudaError_t e = cudaLaunchKernelEx(&cfg, convert_kernel, c);
   if (e != cudaSuccess) return e;
   return launch_bulk(p, zero_folded, s);
+}
+
+cudaError_t launch_w4ax(int M, int N, int K, int g, int n8, const uint8_t* Xa, const uint16_t* sxb,
+                        const uint8_t* packed, const uint16_t* s1, uint16_t* Y, int32_t* acc_debug, void* ws,
+                        int num_sms, unsigned long long timeout_ns, unsigned call_id, cudaStream_t s) {
+  constexpr int BN = 128;
+  const WsLayout L = w4ax_ws_layout(M, N, K);
+  GemmParams p = {};
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.G = K / kGroup;
+  p.gpt = gpt_for_group(g);
+  p.MT = (M + BN - 1) / BN;
+  p.NT = N / kTileN;
+  p.T = p.MT * p.NT;
+  const int P0 = std::max(1, std::min(num_sms, kMaxGrid));
+  if (p.T >= P0) {  // the schedule of launch_gemm
+    const int rem = p.T % P0;
+    p.T_sk = rem == 0 ? 0 : std::min(p.T, rem + P0);
+    p.T_dp = p.T - p.T_sk;
+    p.P = P0;
+  } else {
+    p.T_dp = 0;
+    p.T_sk = p.T;
+    const long long want = ((long long)p.T * p.G + 3) / 4;
+    p.P = (int)std::max<long long>(1, std::min<long long>(P0, want));
+  }
+  p.I_sk = (uint32_t)p.T_sk * (uint32_t)p.G;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  p.status = reinterpret_cast<int*>(w);
+  p.sk_cnt = reinterpret_cast<int32_t*>(w + L.cnt_off);
+  p.sk_acc = reinterpret_cast<int32_t*>(w + L.acc_off);
+  p.xh = reinterpret_cast<const uint16_t*>(w + L.xh_off);
+  p.sxT = reinterpret_cast<const uint16_t*>(w + L.rs_off);
+  p.sxT_ld = L.rs_ld;
+  p.packed = packed;
+  p.s1 = s1;
+  p.Y = Y;
+  p.timeout_ns = timeout_ns;
+  p.call_id = call_id;
+
+  ConvertAxParams c = {};
+  c.Xa = Xa;
+  c.sxb = sxb;
+  c.xh = reinterpret_cast<uint16_t*>(w + L.xh_off);
+  c.sxT = reinterpret_cast<uint16_t*>(w + L.rs_off);
+  c.M = M;
+  c.K = K;
+  c.n8 = n8;
+  c.MT = p.MT;
+  c.sxT_ld = L.rs_ld;
+  const long long work = (long long)p.MT * BN * (K / 16);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)std::max<long long>(1, std::min<long long>((work + 255) / 256, (long long)P0 * 4)));
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1] = {pdl_attr()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, convert_w4ax_kernel, c);
+  if (e != cudaSuccess) return e;
+  e = launch_bulk_ax(p, s);
+  if (e != cudaSuccess || !acc_debug) return e;
+  // sum_b acc_b for checking: the plain kernel on the same operand copy,
+  // integer folds every 8 groups, acc_debug written, no Y
+  GemmParams d = p;
+  d.Y = nullptr;
+  d.acc_debug = acc_debug;
+  d.call_id = call_id + 1 ? call_id + 1 : 1;
+  return launch_bulk(d, false, s);
 }
 
 }  // namespace qoq

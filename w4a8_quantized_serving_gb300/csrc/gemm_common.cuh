@@ -312,14 +312,16 @@ __device__ __forceinline__ void zero_point_share(const GemmParams& p, int nt, in
 template <int COLS>
 __device__ __forceinline__ void write_tile_out(const GemmParams& p, const int32_t (&run)[COLS], int m0,
                                                int n) {
-  const float s1f = __half2float(__ushort_as_half(p.s1[n]));
+  const float s1f = p.Y ? __half2float(__ushort_as_half(p.s1[n])) : 0.0f;
 #pragma unroll
   for (int i = 0; i < COLS; ++i) {
     const int m = m0 + i;
     if (m < p.M) {
-      const float sxf = __half2float(__ushort_as_half(p.sx[m]));
-      const float y = (float)run[i] * (sxf * s1f);
-      p.Y[(size_t)m * p.N + n] = __half_as_ushort(__float2half_rn(y));
+      if (p.Y) {  // (the W4Ax kernels' integer-sum launch writes acc_debug alone)
+        const float sxf = __half2float(__ushort_as_half(p.sx[m]));
+        const float y = (float)run[i] * (sxf * s1f);
+        p.Y[(size_t)m * p.N + n] = __half_as_ushort(__float2half_rn(y));
+      }
       if (p.acc_debug) p.acc_debug[(size_t)m * p.N + n] = run[i];
     }
   }
@@ -531,6 +533,110 @@ __device__ __forceinline__ void epilogue_role(const GemmParams& p, uint32_t tmem
                                 unit_no);
     if (e == 0 && lane == 0) QOQ_TRACE_AT(p, 640 + unit_no, 0);
     ++unit_no;
+  }
+}
+
+// ------------------------------------------------------------- W4Ax epilogue --
+// COMET explainer, the W4Ax kernel: each activation block's integer partial
+// sums are scaled by that block's scale on the general-purpose cores.  The
+// MMA warp commits one accumulator per 128-channel group (fold chunk of one
+// group); per group this thread adds, for its weight row and its TOK tokens,
+//   run[i] += D[i] * s[m_i, g]        (D = acc_g * 2^-13, exact in fp32),
+// and at a unit's end writes Y = fp16_rn(run * 2^13 * s1[n]), or adds its
+// float partial sums into the workspace for a split tile, where the last
+// contributor writes Y (the order of those additions is not fixed, so a split
+// tile's Y may differ between calls in the last fp32 bit before rounding).
+template <int COLS>
+__device__ __forceinline__ void write_tile_out_ax(const GemmParams& p, const float (&run)[COLS], int m0, int n) {
+  const float sc = kAccScale * __half2float(__ushort_as_half(p.s1[n]));  // exact: s1 times 2^13
+#pragma unroll
+  for (int i = 0; i < COLS; ++i) {
+    const int m = m0 + i;
+    if (m < p.M) p.Y[(size_t)m * p.N + n] = __half_as_ushort(__float2half_rn(run[i] * sc));
+  }
+}
+
+template <int BN, int NEPI, int NACC>
+__device__ __forceinline__ void epilogue_role_ax(const GemmParams& p, uint32_t tmem, int epi_warp0,
+                                                 uint32_t bar_accfull, uint32_t bar_accempty,
+                                                 volatile int* last_flag) {
+  constexpr int TOK = BN / (NEPI / 4);
+  static_assert(TOK % 16 == 0, "epilogue loads 16 columns at a time");
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = warp - epi_warp0;
+  const int quad = warp & 3;
+  const int row = quad * 32 + lane;
+  const int tok0 = (e >> 2) * TOK;
+  const int etid = threadIdx.x - epi_warp0 * 32;
+  const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+  UnitIter iter;
+  iter.init(p);
+  Unit u;
+  uint32_t chunk = 0;
+  bool ok = true;  // once false, keep the control flow (named barriers) but do no work
+  while (iter.next(p, u)) {
+    const int nt = u.tile / p.MT, mt = u.tile % p.MT;
+    const int n = nt * kTileN + row;
+    float run[TOK];
+#pragma unroll
+    for (int i = 0; i < TOK; ++i) run[i] = 0.0f;
+    for (int g = u.g0; g < u.g1; ++g, ++chunk) {
+      const int b = chunk % NACC;
+#pragma unroll
+      for (int piece = 0; piece < TOK / 16; ++piece) {
+        // the block's scales of these 16 tokens (issued before the wait on the first piece)
+        const uint4* sp = reinterpret_cast<const uint4*>(p.sxT + (size_t)g * p.sxT_ld + mt * BN + tok0 + piece * 16);
+        const uint4 s0 = __ldcg(sp), s1v = __ldcg(sp + 1);
+        if (piece == 0 && ok) ok = conv_wait_bar(bar_accfull + 8 * b, (chunk / NACC) & 1, p);
+        if (ok) {
+          if (piece == 0) tc_fence_after();
+          uint32_t v[16];
+          tmem_ld16_wait(tmem + lane_base + b * BN + tok0 + piece * 16, v);
+          const uint32_t sw[8] = {s0.x, s0.y, s0.z, s0.w, s1v.x, s1v.y, s1v.z, s1v.w};
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float2 sc = __half22float2(*reinterpret_cast<const __half2*>(&sw[i]));
+            run[piece * 16 + 2 * i] = fmaf(__uint_as_float(v[2 * i]), sc.x, run[piece * 16 + 2 * i]);
+            run[piece * 16 + 2 * i + 1] = fmaf(__uint_as_float(v[2 * i + 1]), sc.y, run[piece * 16 + 2 * i + 1]);
+          }
+        }
+      }
+      if (ok) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_accempty + 8 * b);
+      }
+    }
+    const int m0 = mt * BN + tok0;
+    if (u.g0 == 0 && u.g1 == p.G) {
+      if (ok) write_tile_out_ax<TOK>(p, run, m0, n);
+      continue;
+    }
+    // split tile: float partial sums meet in the workspace (see finish_unit)
+    const int sk = u.tile - p.T_dp;
+    float* part = reinterpret_cast<float*>(p.sk_acc) + (size_t)sk * BN * kTileN + (size_t)tok0 * kTileN;
+    if (ok) {
+#pragma unroll
+      for (int i = 0; i < TOK; ++i) red_add_relaxed_f32(part + i * kTileN + row, run[i]);
+    }
+    named_bar_sync<NEPI * 32>();
+    if (etid == 0) {
+      int last = 0;
+      if (ok) {
+        const int add = u.g1 - u.g0;
+        last = (atom_add_acq_rel(p.sk_cnt + sk, add) + add == p.G) ? 1 : 0;
+        if (last) p.sk_cnt[sk] = 0;  // every contributor has counted: reset for the next call
+      }
+      *last_flag = last;
+    }
+    named_bar_sync<NEPI * 32>();
+    if (ok && *last_flag) {
+#pragma unroll
+      for (int i = 0; i < TOK; ++i) run[i] = __ldcg(part + i * kTileN + row);
+#pragma unroll
+      for (int i = 0; i < TOK; ++i) __stcg(part + i * kTileN + row, 0.0f);  // leave it zeroed
+      write_tile_out_ax<TOK>(p, run, m0, n);
+    }
   }
 }
 

@@ -123,6 +123,8 @@ struct GemmParams {
   unsigned long long* trace;  // per-CTA event clock, only with -DQOQ_TRACE (else unused)
   const int32_t* rs;          // zero-point-folded variant: row sums of Xq per k-tile, [G][rs_ld]
   int rs_ld;
+  const uint16_t* sxT;        // W4Ax: activation block scales by block, [G][sxT_ld] fp16 (0 past M)
+  int sxT_ld;
 };
 
 // Event tracing for pipeline studies: compiled in only with -DQOQ_TRACE.
@@ -157,6 +159,34 @@ struct ConvertParams {
   int M, K, BN, MT;
 };
 
+// W4Ax activations (mixed 8-bit / 4-bit 128-channel blocks, n8 leading 8-bit
+// blocks) -> the fp16 B-operand copy and the transposed block scales.
+struct ConvertAxParams {
+  const uint8_t* Xa;
+  const uint16_t* sxb;  // [M][G]
+  uint16_t* xh;
+  uint16_t* sxT;        // [G][sxT_ld]
+  int M, K, n8, MT, sxT_ld;
+};
+
+// Workspace of qoq_w4ax_gemm: the 128-token-tile layout for any M, then the
+// transposed block scales, fp16 [K/128][MT * 128].
+inline WsLayout w4ax_ws_layout(int M, int N, int K) {
+  const int MT = (M + 127) / 128;
+  const long long T = (long long)MT * (N / kTileN);
+  const long long skmax = T < kMaxSkTiles ? T : kMaxSkTiles;
+  WsLayout L;
+  L.slot_off = 0;  // unused
+  L.cnt_off = kWsHeaderBytes;
+  L.acc_off = align_up(L.cnt_off + (size_t)skmax * 4, 256);
+  L.xh_off = align_up(L.acc_off + (size_t)skmax * 128 * kTileN * 4, 1024);
+  L.rs_off = align_up(L.xh_off + (size_t)MT * K * 128 * 2, 256);  // here: the block scales
+  L.rs_ld = MT * 128;
+  L.zero_bytes = L.xh_off;
+  L.total = align_up(L.rs_off + (size_t)(K / kGroup) * L.rs_ld * 2, 256);
+  return L;
+}
+
 // Row sums of Xq per 128-channel k-tile, for the zero-point-folded variant.
 struct RowSumParams {
   const int8_t* Xq;
@@ -183,9 +213,17 @@ cudaError_t launch_norm_quant(int M, int K, int kind, float eps, const uint16_t*
                               const uint16_t* beta, int8_t* Xq, uint16_t* sx, cudaStream_t s);
 cudaError_t launch_pack(int N, int K, int g, const uint16_t* W, uint8_t* packed, uint16_t* s1,
                         cudaStream_t s);
+cudaError_t launch_act_quant_w4ax(int M, int K, int n8, const uint16_t* X, uint8_t* Xa, uint16_t* sxb,
+                                  cudaStream_t s);
 cudaError_t launch_unpack(int N, int K, int g, const uint8_t* packed, uint8_t* q4, uint8_t* s2, uint8_t* z,
                           cudaStream_t s);
 cudaError_t launch_gemm_decode(const GemmParams& p, int BN, bool zero_folded, cudaStream_t s);
+// The W4Ax GEMM (mixed 4/8-bit activation blocks, per-block scales): always
+// the 128-token-tile kernel; with acc_debug a second launch of the plain
+// kernel on the same operand copy writes sum_b acc_b.
+cudaError_t launch_w4ax(int M, int N, int K, int g, int n8, const uint8_t* Xa, const uint16_t* sxb,
+                        const uint8_t* packed, const uint16_t* s1, uint16_t* Y, int32_t* acc_debug, void* ws,
+                        int num_sms, unsigned long long timeout_ns, unsigned call_id, cudaStream_t s);
 // zero_folded: the variant that feeds q4 * s2 to the tensor cores and
 // subtracts the zero points' share, sum_j z s2 RS[m, j], in the epilogue
 // (g >= 128 only); it first launches the row-sum pre-pass.

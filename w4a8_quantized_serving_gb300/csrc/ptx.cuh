@@ -237,6 +237,10 @@ __device__ __forceinline__ void red_add_relaxed(int32_t* addr, int32_t v) {
   asm volatile("red.relaxed.gpu.global.add.s32 [%0], %1;" ::"l"(addr), "r"(v) : "memory");
 }
 
+__device__ __forceinline__ void red_add_relaxed_f32(float* addr, float v) {
+  asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
+}
+
 __device__ __forceinline__ int32_t atom_add_acq_rel(int32_t* addr, int32_t v) {
   int32_t old;
   asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
