@@ -59,7 +59,13 @@ struct BulkCfg {
   static constexpr int SEQ_OFF = BAR_OFF + NBARS * 8;  // one 32-bit sequence word per stage
   static constexpr int TMEM_SLOT_OFF = SEQ_OFF + ((STAGES * 4 + 7) / 8) * 8;
   static constexpr int FLAG_OFF = TMEM_SLOT_OFF + 8;
-  static constexpr int SMEM_BYTES = FLAG_OFF + 8 + 1024;  // + slack for 1024-B alignment
+  // W4Ax: ring of SCR slots of one group's block scales for the tile's 128
+  // tokens (fp16, 256 B), filled by the producer's bulk copies, released by
+  // the epilogue; its full / empty barriers follow.
+  static constexpr int SCR = 8;
+  static constexpr int SC_OFF = (FLAG_OFF + 8 + 255) / 256 * 256;
+  static constexpr int SC_BAR_OFF = SC_OFF + SCR * 256;
+  static constexpr int SMEM_BYTES = SC_BAR_OFF + 2 * SCR * 8 + 1024;  // + slack for 1024-B alignment
   static_assert(NABUF >= NSLOT + 1, "A buffers");
   static_assert(STAGES >= 3, "pipeline depth");
   static_assert(SMEM_BYTES <= kSmemBudget, "shared memory");
@@ -102,6 +108,11 @@ __global__ void __launch_bounds__(BulkCfg<GPT>::THREADS, 1) gemm_bulk_kernel(con
       mbar_init(bar_accempty + 8 * b, C::NEPI);
     }
     mbar_init(bar_drain, 1);
+    if (AX)
+      for (int j = 0; j < C::SCR; ++j) {
+        mbar_init(sbase + C::SC_BAR_OFF + 8 * j, 1);                   // scales landed
+        mbar_init(sbase + C::SC_BAR_OFF + 8 * (C::SCR + j), C::NEPI);  // epilogue done with them
+      }
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(sbase + C::TMEM_SLOT_OFF, kTmemCols);
@@ -129,6 +140,21 @@ __global__ void __launch_bounds__(BulkCfg<GPT>::THREADS, 1) gemm_bulk_kernel(con
         const uint16_t* src = p.xh + ((size_t)(tile % p.MT) * p.G + gg) * (C::B_BYTES / 2);
         bulk_g2s(sbase + s * C::B_BYTES, src, C::B_BYTES, bar_full + 8 * s, pol);
       };
+      // W4Ax: group number q's block scales into ring slot q % SCR
+      uint32_t sc_mask = 0, sc_par = 0;  // per slot: a copy in its latest lap; its parity
+      auto issue_sc = [&](uint32_t qn, int tile, int gg) -> bool {
+        if (!AX) return true;
+        const int j = (int)(qn % C::SCR);
+        const uint32_t ph = (qn / C::SCR) & 1;
+        if (qn >= (uint32_t)C::SCR && !wait_bar(sbase + C::SC_BAR_OFF + 8 * (C::SCR + j), ph ^ 1, p)) return false;
+        const uint32_t full = sbase + C::SC_BAR_OFF + 8 * j;
+        mbar_arrive_expect_tx(full, 256);
+        bulk_g2s(sbase + C::SC_OFF + 256 * j, p.sxT + (size_t)gg * p.sxT_ld + (size_t)(tile % p.MT) * BN, 256, full,
+                 pol);
+        sc_mask |= 1u << j;
+        sc_par = (sc_par & ~(1u << j)) | (ph << j);
+        return true;
+      };
       // Weights do not depend on the preceding kernels: issue a few stages
       // before waiting on them.
       int npre = 0;
@@ -148,12 +174,17 @@ __global__ void __launch_bounds__(BulkCfg<GPT>::THREADS, 1) gemm_bulk_kernel(con
         }
       }
       grid_dep_wait();
-      for (int i = 0; i < npre; ++i) issue_x(i, pre_tile[i], pre_g[i]);
+      bool sc_ok = true;
+      for (int i = 0; i < npre; ++i) {
+        issue_x(i, pre_tile[i], pre_g[i]);
+        if (sc_ok) sc_ok = issue_sc((uint32_t)i, pre_tile[i], pre_g[i]);
+      }
       uint32_t gi = npre;
-      while (have) {
+      while (have && sc_ok) {
         const int s = gi % C::STAGES;
         const uint32_t ph = (gi / C::STAGES) & 1;
         if (!wait_bar(bar_empty + 8 * s, ph ^ 1, p)) break;
+        if (!issue_sc(gi, u.tile, g)) break;
         if (!(p.fault == 1 && gi == (uint32_t)C::STAGES + 1)) {  // test hook: skip one stage
           mbar_arrive_expect_tx(bar_full + 8 * s, kStageTx);
           issue_w(s, u.tile, g);
@@ -173,6 +204,8 @@ __global__ void __launch_bounds__(BulkCfg<GPT>::THREADS, 1) gemm_bulk_kernel(con
       // Let every copy still in flight land before the CTA may exit.
       for (int s = 0; s < C::STAGES; ++s)
         if (issued_mask & (1u << s)) wait_bar(bar_full + 8 * s, (issued_par >> s) & 1, p, false);
+      for (int j = 0; j < C::SCR; ++j)
+        if (sc_mask & (1u << j)) wait_bar(sbase + C::SC_BAR_OFF + 8 * j, (sc_par >> j) & 1, p, false);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -233,8 +266,9 @@ __global__ void __launch_bounds__(BulkCfg<GPT>::THREADS, 1) gemm_bulk_kernel(con
     // ------------------------------------------------------------ epilogue --
     grid_dep_wait();
     if constexpr (AX)
-      epilogue_role_ax<BN, C::NEPI, C::NACC>(p, tmem, C::EPI_WARP0, bar_accfull, bar_accempty,
-                                            reinterpret_cast<volatile int*>(smem + C::FLAG_OFF));
+      epilogue_role_ax<BN, C::NEPI, C::NACC, C::SCR>(p, tmem, C::EPI_WARP0, bar_accfull, bar_accempty,
+                                                    reinterpret_cast<volatile int*>(smem + C::FLAG_OFF),
+                                                    sbase + C::SC_OFF, sbase + C::SC_BAR_OFF);
     else
       epilogue_role<BN, C::NEPI, C::NACC, ZF, C::TILE>(p, tmem, C::EPI_WARP0, bar_accfull, bar_accempty,
                                                        reinterpret_cast<volatile int*>(smem + C::FLAG_OFF));

@@ -556,10 +556,14 @@ __device__ __forceinline__ void write_tile_out_ax(const GemmParams& p, const flo
   }
 }
 
-template <int BN, int NEPI, int NACC>
+// The block scales of group number q arrive in shared-memory slot q % SCR
+// (sc_smem + 256 slot: 128 fp16, one per token of the tile), announced on
+// barrier sc_bars + 8 slot; every epilogue warp arrives on sc_bars + 8 (SCR +
+// slot) when it is done with them.
+template <int BN, int NEPI, int NACC, int SCR>
 __device__ __forceinline__ void epilogue_role_ax(const GemmParams& p, uint32_t tmem, int epi_warp0,
                                                  uint32_t bar_accfull, uint32_t bar_accempty,
-                                                 volatile int* last_flag) {
+                                                 volatile int* last_flag, uint32_t sc_smem, uint32_t sc_bars) {
   constexpr int TOK = BN / (NEPI / 4);
   static_assert(TOK % 16 == 0, "epilogue loads 16 columns at a time");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -582,14 +586,20 @@ __device__ __forceinline__ void epilogue_role_ax(const GemmParams& p, uint32_t t
     for (int i = 0; i < TOK; ++i) run[i] = 0.0f;
     for (int g = u.g0; g < u.g1; ++g, ++chunk) {
       const int b = chunk % NACC;
+      const int slot = (int)(chunk % SCR);
+      if (ok) ok = conv_wait_bar(sc_bars + 8 * slot, (chunk / SCR) & 1, p);
+      if (ok) ok = conv_wait_bar(bar_accfull + 8 * b, (chunk / NACC) & 1, p);
+      if (ok) tc_fence_after();
 #pragma unroll
       for (int piece = 0; piece < TOK / 16; ++piece) {
-        // the block's scales of these 16 tokens (issued before the wait on the first piece)
-        const uint4* sp = reinterpret_cast<const uint4*>(p.sxT + (size_t)g * p.sxT_ld + mt * BN + tok0 + piece * 16);
-        const uint4 s0 = __ldcg(sp), s1v = __ldcg(sp + 1);
-        if (piece == 0 && ok) ok = conv_wait_bar(bar_accfull + 8 * b, (chunk / NACC) & 1, p);
         if (ok) {
-          if (piece == 0) tc_fence_after();
+          // this group's scales of these 16 tokens, from the ring
+          const uint32_t sa = sc_smem + 256 * slot + 2 * (tok0 + piece * 16);
+          uint4 s0, s1v;
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(s0.x), "=r"(s0.y), "=r"(s0.z), "=r"(s0.w) : "r"(sa));
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(s1v.x), "=r"(s1v.y), "=r"(s1v.z), "=r"(s1v.w) : "r"(sa + 16));
           uint32_t v[16];
           tmem_ld16_wait(tmem + lane_base + b * BN + tok0 + piece * 16, v);
           const uint32_t sw[8] = {s0.x, s0.y, s0.z, s0.w, s1v.x, s1v.y, s1v.z, s1v.w};
@@ -604,7 +614,10 @@ __device__ __forceinline__ void epilogue_role_ax(const GemmParams& p, uint32_t t
       if (ok) {
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar_accempty + 8 * b);
+        if (lane == 0) {
+          mbar_arrive(bar_accempty + 8 * b);
+          mbar_arrive(sc_bars + 8 * (SCR + slot));
+        }
       }
     }
     const int m0 = mt * BN + tok0;
