@@ -132,25 +132,26 @@ __global__ void __launch_bounds__(BulkCfg<GPT>::THREADS, 1) gemm_bulk_kernel(con
       int g = have ? u.g0 : 0;
       uint32_t issued_mask = 0, issued_par = 0;  // per stage: last issue and its parity
       constexpr uint32_t kStageTx = C::TILE + C::B_BYTES;
-      auto issue_w = [&](int s, int tile, int gg) {
-        const uint8_t* src = p.packed + ((size_t)(tile / p.MT) * p.G + gg) * C::TILE;
+      // the current unit's tile coordinates (computed once per unit)
+      TileXY xy = have ? tile_xy(p, u.tile) : TileXY{0, 0};
+      auto issue_w = [&](int s, int nt, int gg) {
+        const uint8_t* src = p.packed + ((size_t)nt * p.G + gg) * C::TILE;
         bulk_g2s(sbase + C::W_OFF + s * C::TILE, src, C::TILE, bar_full + 8 * s, pol);
       };
-      auto issue_x = [&](int s, int tile, int gg) {
-        const uint16_t* src = p.xh + ((size_t)(tile % p.MT) * p.G + gg) * (C::B_BYTES / 2);
+      auto issue_x = [&](int s, int mt, int gg) {
+        const uint16_t* src = p.xh + ((size_t)mt * p.G + gg) * (C::B_BYTES / 2);
         bulk_g2s(sbase + s * C::B_BYTES, src, C::B_BYTES, bar_full + 8 * s, pol);
       };
       // W4Ax: group number q's block scales into ring slot q % SCR
       uint32_t sc_mask = 0, sc_par = 0;  // per slot: a copy in its latest lap; its parity
-      auto issue_sc = [&](uint32_t qn, int tile, int gg) -> bool {
+      auto issue_sc = [&](uint32_t qn, int mt, int gg) -> bool {
         if (!AX) return true;
         const int j = (int)(qn % C::SCR);
         const uint32_t ph = (qn / C::SCR) & 1;
         if (qn >= (uint32_t)C::SCR && !wait_bar(sbase + C::SC_BAR_OFF + 8 * (C::SCR + j), ph ^ 1, p)) return false;
         const uint32_t full = sbase + C::SC_BAR_OFF + 8 * j;
         mbar_arrive_expect_tx(full, 256);
-        bulk_g2s(sbase + C::SC_OFF + 256 * j, p.sxT + (size_t)gg * p.sxT_ld + (size_t)(tile % p.MT) * BN, 256, full,
-                 pol);
+        bulk_g2s(sbase + C::SC_OFF + 256 * j, p.sxT + (size_t)gg * p.sxT_ld + (size_t)mt * BN, 256, full, pol);
         sc_mask |= 1u << j;
         sc_par = (sc_par & ~(1u << j)) | (ph << j);
         return true;
@@ -158,37 +159,40 @@ __global__ void __launch_bounds__(BulkCfg<GPT>::THREADS, 1) gemm_bulk_kernel(con
       // Weights do not depend on the preceding kernels: issue a few stages
       // before waiting on them.
       int npre = 0;
-      int pre_tile[kPrefetchStages], pre_g[kPrefetchStages];
+      int pre_mt[kPrefetchStages], pre_g[kPrefetchStages];
       while (have && npre < kPrefetchStages) {
         const int s = npre;
         mbar_arrive_expect_tx(bar_full + 8 * s, kStageTx);
-        issue_w(s, u.tile, g);
+        issue_w(s, xy.nt, g);
         st_release_shared(seq + 4 * s, (uint32_t)npre + 1);
-        pre_tile[npre] = u.tile;
+        pre_mt[npre] = xy.mt;
         pre_g[npre] = g;
         issued_mask |= 1u << s;
         ++npre;
         if (++g >= u.g1) {
           have = iter.next(p, u);
-          if (have) g = u.g0;
+          if (have) {
+            g = u.g0;
+            xy = tile_xy(p, u.tile);
+          }
         }
       }
       grid_dep_wait();
       bool sc_ok = true;
       for (int i = 0; i < npre; ++i) {
-        issue_x(i, pre_tile[i], pre_g[i]);
-        if (sc_ok) sc_ok = issue_sc((uint32_t)i, pre_tile[i], pre_g[i]);
+        issue_x(i, pre_mt[i], pre_g[i]);
+        if (sc_ok) sc_ok = issue_sc((uint32_t)i, pre_mt[i], pre_g[i]);
       }
       uint32_t gi = npre;
       while (have && sc_ok) {
         const int s = gi % C::STAGES;
         const uint32_t ph = (gi / C::STAGES) & 1;
         if (!wait_bar(bar_empty + 8 * s, ph ^ 1, p)) break;
-        if (!issue_sc(gi, u.tile, g)) break;
+        if (!issue_sc(gi, xy.mt, g)) break;
         if (!(p.fault == 1 && gi == (uint32_t)C::STAGES + 1)) {  // test hook: skip one stage
           mbar_arrive_expect_tx(bar_full + 8 * s, kStageTx);
-          issue_w(s, u.tile, g);
-          issue_x(s, u.tile, g);
+          issue_w(s, xy.nt, g);
+          issue_x(s, xy.mt, g);
           st_release_shared(seq + 4 * s, gi + 1);
           issued_mask |= 1u << s;
           issued_par = (issued_par & ~(1u << s)) | (ph << s);
@@ -198,7 +202,10 @@ __global__ void __launch_bounds__(BulkCfg<GPT>::THREADS, 1) gemm_bulk_kernel(con
         ++gi;
         if (++g >= u.g1) {
           have = iter.next(p, u);
-          if (have) g = u.g0;
+          if (have) {
+            g = u.g0;
+            xy = tile_xy(p, u.tile);
+          }
         }
       }
       // Let every copy still in flight land before the CTA may exit.

@@ -151,6 +151,26 @@ struct UnitIter {
   }
 };
 
+// Tile t -> (weight tile nt, token tile mt) for 128-token tiles.  Tiles go in
+// bands of kTileBand token tiles: inside a band the token tile changes
+// fastest, so the CTAs running at one time share ~P / kTileBand weight tiles
+// and kTileBand token tiles, and their operands stay in L2 (all token tiles of
+// a large prefill at once would not).  A band narrower than kTileBand (the
+// last one, or MT < kTileBand) keeps the same order.
+constexpr int kTileBand = 16;
+struct TileXY {
+  int nt, mt;
+};
+__device__ __forceinline__ TileXY tile_xy(const GemmParams& p, int t) {
+  const int band_tiles = kTileBand * p.NT;
+  const int band = t / band_tiles, r = t - band * band_tiles;
+  const int width = min(kTileBand, p.MT - band * kTileBand);
+  TileXY c;
+  c.nt = r / width;
+  c.mt = band * kTileBand + (r - c.nt * width);
+  return c;
+}
+
 // ------------------------------------------------------------------- waits --
 
 // Bounded wait on an mbarrier phase.  Returns false if the wait ran out (the
@@ -503,7 +523,8 @@ __device__ __forceinline__ void epilogue_role(const GemmParams& p, uint32_t tmem
   int unit_no = 0;
   bool ok = true;  // once false, keep the control flow (named barriers) but do no work
   while (iter.next(p, u)) {
-    const int nt = u.tile / p.MT, mt = u.tile % p.MT;
+    const TileXY xy = tile_xy(p, u.tile);
+    const int nt = xy.nt, mt = xy.mt;
     const int n = nt * kTileN + row;
     int32_t run[TOK];
 #pragma unroll
@@ -579,7 +600,8 @@ __device__ __forceinline__ void epilogue_role_ax(const GemmParams& p, uint32_t t
   uint32_t chunk = 0;
   bool ok = true;  // once false, keep the control flow (named barriers) but do no work
   while (iter.next(p, u)) {
-    const int nt = u.tile / p.MT, mt = u.tile % p.MT;
+    const TileXY xy = tile_xy(p, u.tile);
+    const int nt = xy.nt, mt = xy.mt;
     const int n = nt * kTileN + row;
     float run[TOK];
 #pragma unroll

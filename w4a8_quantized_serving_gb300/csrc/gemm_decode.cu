@@ -104,14 +104,14 @@ __device__ __forceinline__ int sk_cta_of(const GemmParams& p, uint32_t it) {
 // of its range, so it comes last in time.  Every other contributor holds a
 // later part of the tile as the first unit of its range, and stores it into
 // its own slot as {int32 partial sum, tag} pairs, which are single-copy
-// atomic: the owner reads the slots of the CTAs after it, retries only while
-// an entry does not carry this launch's tag yet, and clears each entry it has
-// consumed.  The tag is 2 e + 1 for the epoch e in the workspace header,
-// which the last CTA of every launch advances (advance_epoch_at_exit), so a
-// launch replayed from a CUDA graph never accepts a partial sum that an
-// earlier replay left behind.  Tags are odd, so neither a cleared entry (0)
-// nor the fp16 operand copy of the bulk kernel (integer-valued halves, whose
-// lowest bit is 0) that may share the workspace can match one.
+// atomic: the owner reads the slots of the CTAs after it and retries only
+// while an entry does not carry this launch's tag yet.  The tag is 2 e + 1 for
+// the epoch e in the workspace header, which the last CTA of every launch
+// advances (advance_epoch_at_exit), so a launch replayed from a CUDA graph
+// never accepts a partial sum that an earlier replay left behind, and nothing
+// needs clearing.  Tags are odd, so a zero-filled entry never matches one;
+// the state of 128-token-tile calls sharing the workspace lies above the
+// decode area (kDecodeArea) and never overlaps the slots.
 template <int BN, int TOK>
 __device__ __forceinline__ void slot_store(const GemmParams& p, uint32_t tag, int tok0, int row,
                                            const int32_t (&run)[TOK]) {
@@ -148,21 +148,6 @@ __device__ __forceinline__ bool slot_gather(const GemmParams& p, uint32_t tag, i
   return true;
 }
 
-// After the owner has written Y: clear the entries it consumed from the slots
-// of CTAs b1 .. blockIdx.x + 1, so that the workspace is left as a zero-filled
-// one for the next launch of any shape.  Done last, when the running sums are
-// dead, so that it costs no registers on the gather's path.
-template <int BN, int TOK>
-__device__ __forceinline__ void slot_clear(const GemmParams& p, int b1, int tok0, int row) {
-  for (int c = b1; c > (int)blockIdx.x; --c) {
-    unsigned long long* const z = p.sk_slot + (size_t)c * BN * kTileN + tok0 * kTileN + row;
-#pragma unroll 4
-    for (int i = 0; i < TOK; ++i) st_relaxed_b64(z + i * kTileN, 0ull);
-  }
-}
-
-// ZF: the zero-point-folded variant (A operand q4 * s2; the zero points'
-// share is subtracted in the epilogue, see zero_point_share).
 template <int BN, int GPT, bool ZF>
 __global__ void __launch_bounds__(DecCfg<BN, GPT>::THREADS, 1) gemm_decode_kernel(const __grid_constant__ GemmParams p) {
   using C = DecCfg<BN, GPT>;
@@ -444,7 +429,6 @@ __global__ void __launch_bounds__(DecCfg<BN, GPT>::THREADS, 1) gemm_decode_kerne
           for (int c = b1; ok && c > (int)blockIdx.x; --c) ok = slot_gather<BN, TOK>(p, tag, c, tok0, row, run);
           if (ok) write_tile_out<TOK>(p, run, tok0, n);
         }
-        if (ok) slot_clear<BN, TOK>(p, b1, tok0, row);
         if (e == 0 && lane == 0) QOQ_TRACE_AT(p, 960 + 4 * (unit_no & 7) + 2, 0);
       }
       if (e == 0 && lane == 0) QOQ_TRACE_AT(p, 640 + unit_no, 0);

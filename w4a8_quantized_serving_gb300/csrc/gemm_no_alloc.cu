@@ -73,21 +73,19 @@ qoq_status scratch_address(void** out) {
   return s.status;
 }
 
-// Zeroes the first n16 16-byte words of the array: the part of the workspace
-// that the GEMM requires to start at zero (header, counters, partial sums).
-// The decode kernel's hand-off epoch and CTA exit counter (header words 2
-// and 3) are kept: every launch leaves the counter at zero and advances the
-// epoch, so partial sums that a call which ran out of its wait limit left
-// behind carry an older tag than any later call's.
-__global__ void __launch_bounds__(256) no_alloc_clear_kernel(size_t n16) {
+// Zeroes the part of the workspace that the GEMM requires to start at zero:
+// the header's status and abort words, and the 16-byte words [lo16, hi16)
+// (split-K counters and partial sums of 128-token tiles).  The decode
+// kernel's hand-off epoch and CTA exit counter (header words 2 and 3) are
+// kept: every launch leaves the counter at zero and advances the epoch, so
+// partial sums that a call which ran out of its wait limit left behind carry
+// an older tag than any later call's.
+__global__ void __launch_bounds__(256) no_alloc_clear_kernel(size_t lo16, size_t hi16) {
   uint4* p = reinterpret_cast<uint4*>(g_no_alloc_scratch);
   const size_t stride = (size_t)gridDim.x * blockDim.x;
-  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride) {
-    if (i == 0)
-      *reinterpret_cast<uint2*>(g_no_alloc_scratch) = make_uint2(0u, 0u);  // status and abort words
-    else
-      p[i] = make_uint4(0u, 0u, 0u, 0u);
-  }
+  const size_t tid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (tid == 0) *reinterpret_cast<uint2*>(g_no_alloc_scratch) = make_uint2(0u, 0u);  // status and abort words
+  for (size_t i = lo16 + tid; i < hi16; i += stride) p[i] = make_uint4(0u, 0u, 0u, 0u);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -116,9 +114,10 @@ extern "C" qoq_status qoq_w4a8_gemm_no_alloc(int M, int N, int K, int g, const i
   // The array keeps whatever the previous call left (normally zeros, but not
   // after a call that ran out of its wait limit), so clear the zero-start part
   // on the stream before every GEMM.
-  const size_t zero_bytes = qoq::gemm_ws_layout(M, N, K).zero_bytes;
-  const size_t n16 = zero_bytes / 16;
-  size_t blocks = (n16 + 255) / 256;
+  const qoq::WsLayout L = qoq::gemm_ws_layout(M, N, K);
+  const size_t lo16 = L.cnt_off / 16, hi16 = L.zero_bytes / 16;
+  size_t blocks = (hi16 - lo16 + 255) / 256;
+  if (blocks < 1) blocks = 1;
   if (blocks > 1024) blocks = 1024;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)blocks);
@@ -126,7 +125,7 @@ extern "C" qoq_status qoq_w4a8_gemm_no_alloc(int M, int N, int K, int g, const i
   cfg.stream = reinterpret_cast<cudaStream_t>(stream);
   // The launch's own return code: an error left pending by unrelated work is
   // neither reported as this call's nor cleared here.
-  if (cudaLaunchKernelEx(&cfg, no_alloc_clear_kernel, n16) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&cfg, no_alloc_clear_kernel, lo16, hi16) != cudaSuccess) {
     cudaGetLastError();  // clear the launch's own (non-sticky) error, as qoq_w4a8_gemm does
     return QOQ_ERR_CUDA;
   }

@@ -57,11 +57,19 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 // Both end with the per-k-tile row sums of Xq that the zero-point-folded
 // variant subtracts in its epilogue: int32 [K/128][rs_ld], rs_ld = M rounded
 // up to a multiple of 4 (rewritten by every call of that variant).
-// zero_bytes: the prefix that must be zero before the first call.
+// Zero-start state: the header's status words and [cnt_off, zero_bytes)
+// (empty for decode-sized calls, whose split-K entries carry epoch tags).
 struct WsLayout {
   size_t cnt_off, acc_off, slot_off, xh_off, rs_off, zero_bytes, total;
   int rs_ld;
 };
+
+// Every region a decode-sized call (M <= 64) can touch lies below
+// kDecodeArea: the header, its split-K slots (at most kMaxGrid x 64 x 128
+// entries of 8 bytes) and its row sums (at most 1024 k-tiles x 64 tokens of 4
+// bytes).  The 128-token-tile layout starts its zero-start state above it, so
+// calls of both kinds can share a workspace without clearing anything.
+constexpr size_t kDecodeArea = kWsHeaderBytes + (size_t)kMaxGrid * 64 * kTileN * 8 + (size_t)1024 * 64 * 4;
 
 inline WsLayout gemm_ws_layout(int M, int N, int K) {
   const int BN = gemm_bn_for_m(M);
@@ -72,16 +80,16 @@ inline WsLayout gemm_ws_layout(int M, int N, int K) {
   L.rs_ld = (M + 3) / 4 * 4;
   const size_t rs_bytes = (size_t)(K / kGroup) * L.rs_ld * 4;
   if (BN <= 64) {
-    L.cnt_off = L.acc_off = 0;  // unused
+    L.acc_off = 0;  // unused
     L.slot_off = kWsHeaderBytes;
     L.xh_off = align_up(L.slot_off + (size_t)kMaxGrid * BN * kTileN * 8, 1024);  // no B copy: end of slots
     L.rs_off = L.xh_off;
-    L.zero_bytes = kWsHeaderBytes;
+    L.cnt_off = L.zero_bytes = kWsHeaderBytes;
     L.total = align_up(L.rs_off + rs_bytes, 256);
     return L;
   }
   L.slot_off = 0;  // unused
-  L.cnt_off = kWsHeaderBytes;
+  L.cnt_off = align_up(kDecodeArea, 1024);
   L.acc_off = align_up(L.cnt_off + (size_t)skmax * 4, 256);
   L.xh_off = align_up(L.acc_off + (size_t)skmax * BN * kTileN * 4, 1024);
   L.rs_off = align_up(L.xh_off + (size_t)MT * K * BN * 2, 256);
@@ -95,9 +103,9 @@ inline WsLayout gemm_ws_layout(int M, int N, int K) {
 // Split-K state lives in the workspace.  128-token tiles: int32 sums and
 // counts that every completed call leaves zeroed (the last contributor clears
 // them).  Decode tiles: each CTA's slot holds its partial sums tagged with the
-// launch's epoch, read from the workspace header on the device (so a launch
-// replayed from a CUDA graph gets a fresh tag too); the owner that consumes
-// a slot clears it.
+// launch's epoch, read from the workspace header on the device, so a launch
+// replayed from a CUDA graph gets a fresh tag too and stale entries never
+// need clearing.
 // Tiles [0, T_dp) are processed whole, round-robin over the P CTAs; the
 // remaining T_sk tiles are split along K: their T_sk * G group-iterations are
 // cut into P equal contiguous ranges (stream-K), and partial int32 sums meet
