@@ -599,6 +599,68 @@ def check_norm_error_bound(o) -> None:
                 assert abs(y[m, k] - ystar) <= bound, (kind, m, k, y[m, k], ystar)
 
 
+def _round_f32(q: Fraction) -> np.float32:
+    """The float32 nearest to the rational q, ties to even (no double rounding
+    through float64)."""
+    c = np.float32(float(q))
+    cands = [np.nextafter(c, np.float32(-np.inf)), c, np.nextafter(c, np.float32(np.inf))]
+    best = min(cands, key=lambda v: (abs(Fraction(float(v)) - q), int(np.float32(v).view(np.uint32)) & 1))
+    return np.float32(best)
+
+
+def _norm_chain(X, gamma, beta, kind, eps, dtype):
+    """The fused norm's arithmetic written out step by step: exact integer row
+    statistics, each rounded once to `dtype`, then every operation in `dtype`
+    (numpy float32 / float64 operations are IEEE, rounded to nearest), y
+    rounded to fp16."""
+    f = dtype
+    K = X.shape[1]
+    Y = np.empty(X.shape, np.float16)
+    for m in range(X.shape[0]):
+        a = [int(Fraction(float(v)) * 2 ** 24) for v in X[m].astype(np.float64)]
+        S1, S2 = sum(a), sum(v * v for v in a)
+        rnd = _round_f32 if f is np.float32 else (lambda q: np.float64(float(q)))
+        if kind == "rms":
+            spread = f(rnd(Fraction(S2)) * f(2.0 ** -48)) / f(K)
+            mu = f(0.0)
+        else:
+            v = K * S2 - S1 * S1
+            spread = f(rnd(Fraction(v)) * f(2.0 ** -48)) / (f(K) * f(K))
+            mu = f(rnd(Fraction(S1)) * f(2.0 ** -24)) / f(K)
+        r = f(1.0) / np.sqrt(f(spread + f(eps)))
+        for k in range(K):
+            x = f(X[m, k])
+            t = f(x - mu) if kind == "layer" else x
+            w = f(f(t * r) * f(gamma[k]))
+            if kind == "layer":
+                w = f(w + f(beta[k]))
+            Y[m, k] = np.float16(w)
+    return Y
+
+
+def check_norm_fp32_chain(o) -> None:
+    """The norm's reading (every step after the exact row sums in fp32) against
+    that chain written out with numpy float32 on exact rationals, bit for bit;
+    and, on the same rows, a float64 chain gives other fp16 values, so the pin
+    tells the two readings apart."""
+    rng = np.random.default_rng(16)
+    K = 4096
+    X = (rng.standard_normal((6, K)) * np.array([[1.0], [0.07], [3.0], [0.5], [20.0], [0.01]])).astype(np.float16)
+    X[2] += np.float16(0.75)
+    gamma = rng.uniform(0.5, 1.5, K).astype(np.float16)
+    beta = rng.uniform(-0.3, 0.3, K).astype(np.float16)
+    eps = 1e-5
+    for kind in ("rms", "layer"):
+        r = o.norm_quant_act(_bits16(X), _bits16(gamma), _bits16(beta) if kind == "layer" else None,
+                             kind=kind, eps=eps)
+        y32 = _norm_chain(X, gamma, beta, kind, np.float32(eps), np.float32)
+        assert np.array_equal(r["Y"], y32.view(np.uint16)), kind
+        y64 = _norm_chain(X, gamma, beta, kind, eps, np.float64)
+        assert (y64.view(np.uint16) != r["Y"]).any(), f"{kind}: the rows do not separate the two chains"
+        Xq, sx = o.act_quant(y32.view(np.uint16))
+        assert np.array_equal(Xq, r["Xq"]) and np.array_equal(sx, r["sx"])
+
+
 def check_norm_quant_composition(o) -> None:
     """The fused quantization equals the per-token quantizer applied to the
     normalized fp16 rows."""
@@ -618,5 +680,5 @@ ALL_CHECKS = [
     check_error_bounds, check_lossless_grid, check_zero_and_underflow, check_gemm_library,
     check_gemm_threads, check_w4ax_golden, check_w4ax_8bit_blocks, check_w4ax_4bit_bruteforce,
     check_w4ax_gemm_reduces_to_w4a8, check_w4ax_gemm_float_reference, check_zero_folded_appendix, check_zero_folded_equals_direct, check_acc_range, check_norm_exact_stats, check_norm_layer_constant_row, check_norm_rms_unit_row,
-    check_norm_error_bound, check_norm_quant_composition,
+    check_norm_error_bound, check_norm_fp32_chain, check_norm_quant_composition,
 ]

@@ -44,6 +44,8 @@ MUTANTS = {
     "w4ax_leading_blocks": ("b < n8 ? 127 : 7, &sxb", "b <= n8 ? 127 : 7, &sxb"),
     "w4ax_block_scale_index": ("y += qoq_oracle_half_to_double(sxb[(size_t)m * B + b]) * (double)a;",
                                "y += qoq_oracle_half_to_double(sxb[(size_t)m * B]) * (double)a;"),
+    "norm_unrounded_product": ("volatile float w = u * (float)qoq_oracle_half_to_double(gamma[k]);",
+                               "volatile float w = (float)((double)t * (double)r * qoq_oracle_half_to_double(gamma[k]));"),
     "threads_range_gap": ("(int)((int64_t)N * (t + 1) / threads),", "(int)((int64_t)N * (t + 1) / threads) - (t & 1),"),
     "threads_group_index": ("r->s2[(size_t)n * G + k / r->g]);", "r->s2[(size_t)n * G + k % G]);"),
 }
