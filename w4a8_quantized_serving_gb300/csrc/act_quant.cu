@@ -5,7 +5,7 @@
 // quantizer into the preceding LayerNorm; here it is a standalone kernel).
 //   s_x[m]  = fp16_rn(fp32(max_k |X[m,k]|) / 127)        (IEEE fp32 divide)
 //   Xq[m,k] = clamp(rint(X[m,k] / s_x[m]), -127, 127)      (fp32 divide, ties even;
-//             computed without a divide by rint_div_fp16, which gives the same codes)
+//             computed without a divide by quant_bits, which gives the same codes)
 // An all-zero row gets s_x = 0 and Xq = 0.
 //
 // Each token row is owned by T threads (T a power of two, 32..1024), each
@@ -27,24 +27,33 @@
 namespace qoq {
 namespace {
 
-__device__ __forceinline__ float absmax8(uint4 v, float m) {
+// Running max-abs of fp16 values, kept in fp16 (exact) two lanes at a time.
+__device__ __forceinline__ __half2 absmax8(uint4 v, __half2 m) {
   const __half2* h = reinterpret_cast<const __half2*>(&v);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    float2 f = __half22float2(__habs2(h[i]));
-    m = fmaxf(m, fmaxf(f.x, f.y));
-  }
+  for (int i = 0; i < 4; ++i) m = __hmax2(m, __habs2(h[i]));
   return m;
 }
+__device__ __forceinline__ float hmax_float(__half2 m) {
+  const float2 f = __half22float2(m);
+  return fmaxf(f.x, f.y);
+}
 
-__device__ __forceinline__ uint32_t quant4(const __half* h, float sf, float rf) {
-  uint32_t r = 0;
+// int8 codes of 8 fp16 values (one 16-byte vector), packed little-endian.
+template <bool CLAMP>
+__device__ __forceinline__ uint2 quant8(uint4 v, float sf, float rf) {
+  const __half2* h = reinterpret_cast<const __half2*>(&v);
+  uint32_t b[8];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float q = fminf(127.0f, fmaxf(-127.0f, rint_div_fp16(__half2float(h[i]), sf, rf)));
-    r |= (uint32_t)((int)q & 0xff) << (8 * i);
+    const float2 f = __half22float2(h[i]);
+    b[2 * i] = quant_bits<CLAMP>(f.x, sf, rf, 127.0f);
+    b[2 * i + 1] = quant_bits<CLAMP>(f.y, sf, rf, 127.0f);
   }
-  return r;
+  // low byte of each biased pattern is the code byte
+  const uint32_t lo = __byte_perm(__byte_perm(b[0], b[1], 0x0040), __byte_perm(b[2], b[3], 0x0040), 0x5410);
+  const uint32_t hi = __byte_perm(__byte_perm(b[4], b[5], 0x0040), __byte_perm(b[6], b[7], 0x0040), 0x5410);
+  return make_uint2(lo, hi);
 }
 
 // Max-abs of a token row held by T threads (thread t has `amax` of its
@@ -75,16 +84,17 @@ __device__ __forceinline__ void quant_row(const uint4 (&v)[MAXV], float amax, in
   const float rf = sf != 0.0f ? __frcp_rn(sf) : 0.0f;
   if (t == 0) sx[row] = __half_as_ushort(s);
   uint2* qr = reinterpret_cast<uint2*>(Xq + (size_t)row * K);
+  if (sf >= kFp16MinNormal) {  // |x / s| <= 127 (1 + 2^-11): no clamp
 #pragma unroll
-  for (int i = 0; i < MAXV; ++i) {
-    const int idx = t + i * T;
-    if (idx < nvec) {
-      uint2 out = make_uint2(0, 0);
-      if (sf != 0.0f) {
-        const __half* h = reinterpret_cast<const __half*>(&v[i]);
-        out = make_uint2(quant4(h, sf, rf), quant4(h + 4, sf, rf));
-      }
-      qr[idx] = out;
+    for (int i = 0; i < MAXV; ++i) {
+      const int idx = t + i * T;
+      if (idx < nvec) qr[idx] = quant8<false>(v[i], sf, rf);
+    }
+  } else {  // subnormal or zero scale (zero gives zero codes)
+#pragma unroll
+    for (int i = 0; i < MAXV; ++i) {
+      const int idx = t + i * T;
+      if (idx < nvec) qr[idx] = quant8<true>(v[i], sf, rf);
     }
   }
 }
@@ -104,16 +114,16 @@ __global__ void __launch_bounds__(1024) act_quant_kernel(const uint16_t* __restr
   const bool live = row < M;
   const uint4* xr = reinterpret_cast<const uint4*>(X + (size_t)(live ? row : 0) * K);
   uint4 v[MAXV];
-  float amax = 0.0f;
+  __half2 m2 = __float2half2_rn(0.0f);
 #pragma unroll
   for (int i = 0; i < MAXV; ++i) {
     const int idx = t + i * T;
     if (live && idx < nvec) {
       v[i] = __ldcg(xr + idx);  // L2: X may have been written by the preceding kernel
-      amax = absmax8(v[i], amax);
+      m2 = absmax8(v[i], m2);
     }
   }
-  amax = row_absmax(amax, T, warp_max);
+  const float amax = row_absmax(hmax_float(m2), T, warp_max);
   if (!live) return;
   quant_row<MAXV>(v, amax, row, t, T, nvec, K, Xq, sx);
 }
@@ -341,7 +351,7 @@ __global__ void __launch_bounds__(256) act_quant_w4ax_kernel(const uint16_t* __r
   const bool live = b < G;
   uint4 v = make_uint4(0, 0, 0, 0);
   if (live) v = __ldcg(reinterpret_cast<const uint4*>(X + (size_t)m * K + (size_t)b * 128) + l);
-  float amax = absmax8(v, 0.0f);
+  float amax = hmax_float(absmax8(v, __float2half2_rn(0.0f)));
 #pragma unroll
   for (int off = 8; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
   if (!live) return;
@@ -353,23 +363,25 @@ __global__ void __launch_bounds__(256) act_quant_w4ax_kernel(const uint16_t* __r
   const float rf = sf != 0.0f ? __frcp_rn(sf) : 0.0f;
   if (l == 0) sxb[(size_t)m * G + b] = __half_as_ushort(sh);
   const __half* h = reinterpret_cast<const __half*>(&v);
-  int c[8];
+  uint32_t c[8];  // biased patterns: the low byte (nibble) is the code's 8-bit (4-bit) two's complement
+  if (sf >= kFp16MinNormal) {  // |x / s| <= q (1 + 2^-11): no clamp
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
-    c[i] = sf != 0.0f ? (int)fminf(q, fmaxf(-q, rint_div_fp16(__half2float(h[i]), sf, rf))) : 0;
+    for (int i = 0; i < 8; ++i) c[i] = quant_bits<false>(__half2float(h[i]), sf, rf, q);
+  } else {  // subnormal or zero scale (zero gives zero codes)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) c[i] = quant_bits<true>(__half2float(h[i]), sf, rf, q);
+  }
   const size_t row_bytes = (size_t)128 * n8 + (size_t)64 * (G - n8);
   uint8_t* row = Xa + (size_t)m * row_bytes;
   if (eight) {
     uint2 out;
-    out.x = (uint32_t)(c[0] & 0xff) | (uint32_t)(c[1] & 0xff) << 8 | (uint32_t)(c[2] & 0xff) << 16 |
-            (uint32_t)(c[3] & 0xff) << 24;
-    out.y = (uint32_t)(c[4] & 0xff) | (uint32_t)(c[5] & 0xff) << 8 | (uint32_t)(c[6] & 0xff) << 16 |
-            (uint32_t)(c[7] & 0xff) << 24;
+    out.x = __byte_perm(__byte_perm(c[0], c[1], 0x0040), __byte_perm(c[2], c[3], 0x0040), 0x5410);
+    out.y = __byte_perm(__byte_perm(c[4], c[5], 0x0040), __byte_perm(c[6], c[7], 0x0040), 0x5410);
     *reinterpret_cast<uint2*>(row + (size_t)128 * b + 8 * l) = out;
   } else {
     uint32_t out = 0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) out |= (uint32_t)(c[i] & 0xf) << (4 * i);
+    for (int i = 0; i < 8; ++i) out |= (c[i] & 0xfu) << (4 * i);
     *reinterpret_cast<uint32_t*>(row + (size_t)128 * n8 + (size_t)64 * (b - n8) + 4 * l) = out;
   }
 }

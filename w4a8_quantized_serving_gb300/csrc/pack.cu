@@ -59,9 +59,7 @@ __device__ __forceinline__ void level1_codes(const uint16_t* wr, int t, int lane
   const __half* h = reinterpret_cast<const __half*>(&raw);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    int q = 0;
-    if (s1f != 0.0f) q = (int)fminf(119.0f, fmaxf(-119.0f, rint_div_fp16(__half2float(h[i]), s1f, r1f)));
-    q8[i] = q;
+    q8[i] = quant_code(__half2float(h[i]), s1f, r1f, 119.0f);  // 0 where s1 = 0
   }
 }
 

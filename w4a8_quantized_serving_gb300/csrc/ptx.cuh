@@ -217,19 +217,35 @@ __device__ __forceinline__ unsigned long long ld_relaxed_b64(const unsigned long
 
 // --------------------------------------------------------- exact rounding --
 
-// rint(x / s) with ties to even, for fp16-valued x and s > 0, without a divide.
-// The exact quotient of two fp16 values is either a half-integer or at least
-// 2^-13 away from every half-integer while |x / s| < 256; y = x * rcp_rn(s) is
-// within 2^-23 |x / s| of it, so rint(y) is right except at exact ties, which
-// one FMA detects exactly ((f + 1/2) * s has at most 20 significant bits).
-// This equals rint(fl32(x / s)) with an IEEE divide, the rule the quantizers
-// follow, because fl32(x / s) cannot cross or land on a half-integer either.
-__device__ __forceinline__ float rint_div_fp16(float x, float s, float rcp_s) {
-  const float y = x * rcp_s;
-  const float f = floorf(y);
-  if (fmaf(f + 0.5f, s, -x) == 0.0f) return (((int)f) & 1) ? f + 1.0f : f;
-  return rintf(y);
+// rint(x / s) with ties to even, for fp16-valued x and s >= 0 (s = 0 with
+// rcp_s = 0 gives 0), without a divide and on the FP32 pipe alone.
+//   y1 = x rcp_rn(s);  e = fma(-y1, s, x);  y = fma(e, rcp_rn(s), y1)
+// e is the exact remainder x - y1 s (about 12 significant bits), so y is the
+// quotient to within an ulp and exactly n + 1/2 wherever x / s is: y rounds
+// like the exact quotient, which is either a half-integer or at least 2^-13
+// away from every half-integer while |x / s| < 256.  Adding 1.5 * 2^23
+// rounds to nearest, ties to even, and leaves the bit pattern
+// 0x4B400000 + code (the low byte is the code's two's-complement byte).
+// This equals clamp(rint(fl32(x / s)), -q, q) with an IEEE divide, the rule
+// the quantizers follow, because fl32(x / s) cannot cross or land on a
+// half-integer either.  CLAMP clamps y to [-q, q] first; callers may leave
+// it out when s = fp16_rn(amax / q) is a normal fp16 number and |x| <= amax,
+// since then |x / s| <= q (1 + 2^-11) never rounds past q.
+constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23
+constexpr uint32_t kRoundMagicBits = 0x4B400000u;
+template <bool CLAMP>
+__device__ __forceinline__ uint32_t quant_bits(float x, float s, float rcp_s, float q) {
+  const float y1 = __fmul_rn(x, rcp_s);
+  const float e = __fmaf_rn(-y1, s, x);
+  float y = __fmaf_rn(e, rcp_s, y1);
+  if (CLAMP) y = fminf(q, fmaxf(-q, y));
+  return __float_as_uint(__fadd_rn(y, kRoundMagic));
 }
+__device__ __forceinline__ int quant_code(float x, float s, float rcp_s, float q) {
+  return (int)(quant_bits<true>(x, s, rcp_s, q) - kRoundMagicBits);
+}
+// The smallest normal fp16 value: scales at or above it need no clamp.
+constexpr float kFp16MinNormal = 6.103515625e-05f;  // 2^-14
 
 // ------------------------------------------------------ global atomics --
 
