@@ -113,6 +113,15 @@ def test_gemm_token_counts(M):
     _run_full(M, 384, 1152, 300 + M)
 
 
+@pytest.mark.parametrize("M", [65, 128, 129, 200, 256, 300])
+def test_gemm_pair_token_counts(M):
+    """N a multiple of 256: 128-token tiles run on CTA pairs (two weight tiles
+    per pair tile, M=256 MMAs, each CTA staging half of every token tile); 9
+    groups cross the fold boundary, and two pair tiles per token tile are
+    split along K over the pairs."""
+    _run_full(M, 512, 1152, 500 + M)
+
+
 @pytest.mark.parametrize("M,N,K", [(16, 128, 4096), (64, 1024, 2048), (128, 2048, 1024), (5, 128, 16384)])
 def test_gemm_split_k_shapes(M, N, K):
     _run_full(M, N, K, 400 + M)
@@ -313,13 +322,15 @@ def test_gemm_exact_across_alternating_inputs(M, N, K):
     assert not bad, f"calls {bad} differ from their input set's first result"
 
 
-def test_device_wait_timeout_is_reported_and_context_survives():
+@pytest.mark.parametrize("M,N,K", [(16, 128 * 152, 8192), (200, 4096, 8192)])
+def test_device_wait_timeout_is_reported_and_context_survives(M, N, K):
     """A producer that skips one pipeline stage (test hook) makes the waits
     downstream run out after a short limit; the kernel returns, the status
-    reads QOQ_ERR_DEVICE_TIMEOUT, and the next call is correct."""
+    reads QOQ_ERR_DEVICE_TIMEOUT, and the next call is correct.  M=16: the
+    decode kernel; M=200, N=4096: the CTA-pair kernel, where the other CTA of
+    the pair and the leading CTA's MMA issuer run out as well."""
     mod = q()
     t = gc.torch()
-    M, N, K = 16, 128 * 152, 8192
     W = synth.weights(N, K, 61)
     X = synth.activations(M, K, 61)
     Wd, Xd = gc.to_dev_f16(W), gc.to_dev_f16(X)

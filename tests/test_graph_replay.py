@@ -95,6 +95,57 @@ def test_graph_replays_with_new_inputs_are_exact():
         assert ok, (j, rel, ab)
 
 
+def test_graph_replays_pair_kernel_with_new_inputs_are_exact():
+    """128-token tiles on CTA pairs (M=200, N=4096, K=4096: two token tiles,
+    sixteen pair tiles, every one split along K over the pairs): three calls
+    in one graph over two workspaces, 20 replays with new activations in the
+    captured buffers; every replay's accumulators bit-exact against the
+    oracle."""
+    mod = q()
+    t = gc.torch()
+    M, N, K = 200, 4096, 4096
+    W = synth.weights(N, K, 95)
+    packed, s1 = mod.qoq_pack_weights(gc.to_dev_f16(W))
+    o = gc.oracle.weight_quant(synth.bits(W), 128)
+    n_sets, n_calls, n_replays = 4, 3, 20
+    sets = _input_sets(o, M, K, n_sets, 970)
+    xq = [t.empty((M, K), dtype=t.int8, device="cuda") for _ in range(n_calls)]
+    sx = [t.empty(M, dtype=t.float16, device="cuda") for _ in range(n_calls)]
+    acc = [t.empty((M, N), dtype=t.int32, device="cuda") for _ in range(n_calls)]
+    ws_bytes = mod.qoq_gemm_workspace_bytes(M, N, K)
+    ws = [t.zeros(ws_bytes, dtype=t.uint8, device="cuda") for _ in range(2)]
+
+    def load(r: int):
+        for j in range(n_calls):
+            s = sets[(r + j) % n_sets]
+            xq[j].copy_(s["Xq"])
+            sx[j].copy_(s["sx"])
+            acc[j].fill_(-1)
+
+    def calls():
+        for j in range(n_calls):
+            mod.qoq_w4a8_gemm(xq[j], sx[j], packed, s1, N, acc_debug=acc[j], workspace=ws[j % 2])
+
+    load(0)
+    calls()
+    t.cuda.synchronize()
+    graph = t.cuda.CUDAGraph()
+    with t.cuda.graph(graph):
+        calls()
+    t.cuda.synchronize()
+    bad = []
+    for r in range(n_replays):
+        load(r)
+        graph.replay()
+        for j in range(n_calls):
+            if not t.equal(acc[j], sets[(r + j) % n_sets]["acc"]):
+                bad.append((r, j))
+    t.cuda.synchronize()
+    for w in ws:
+        assert mod.qoq_last_device_status(w) == 0
+    assert not bad, f"(replay, call) pairs with wrong accumulators: {bad[:10]} ({len(bad)} in all)"
+
+
 def test_workspace_shared_across_token_counts():
     """One workspace, sized for the largest call, serves a sequence of calls
     whose token counts switch between the decode kernel (M <= 64) and the

@@ -38,10 +38,11 @@ def test_pack_bit_exact_and_layout_other_g(g):
 
 
 @pytest.mark.parametrize("g", [32, 64, 256, "K"])
-@pytest.mark.parametrize("M,N,K", [(16, 384, 1024), (40, 640, 1152), (200, 384, 1024), (1, 128, 768)])
+@pytest.mark.parametrize("M,N,K", [(16, 384, 1024), (40, 640, 1152), (200, 384, 1024), (200, 512, 1152), (1, 128, 768)])
 def test_gemm_other_g(g, M, N, K):
     """Decode token tiles (M <= 64) and 128-token tiles (M > 64), with split-K
-    tiles, at each group size."""
+    tiles, at each group size; N = 512 runs the 128-token tiles on CTA pairs,
+    N = 384 on single CTAs."""
     gg = K if g == "K" else g
     if K % gg:
         pytest.skip("g must divide K")

@@ -36,12 +36,14 @@ namespace {
 constexpr int kPrefetchStages = 4;  // weight stages issued before waiting on the preceding kernel
 
 // GPT: level-2 scale sets per packed k-tile (g = 128 / GPT, or a multiple of
-// 128 with GPT = 1).
-template <int GPT>
+// 128 with GPT = 1).  PAIR: the CTA-pair form (each CTA stages its own weight
+// tile and half of the token tile).
+template <int GPT, bool PAIR = false>
 struct BulkCfg {
   static constexpr int TILE = w_tile_bytes(GPT);  // packed k-tile bytes
   static constexpr int NIB = w_nib_offset(GPT);   // offset of its code chunks
   static constexpr int BN = 128;
+  static constexpr int BROWS = PAIR ? BN / 2 : BN;  // token rows of B staged by this CTA
   static constexpr int NSLOT = 2;   // groups dequantized concurrently
   static constexpr int NDQ = 4 * NSLOT;
   static constexpr int NEPI = 16;   // 4 per TMEM lane quadrant, 32 tokens each
@@ -50,9 +52,9 @@ struct BulkCfg {
   static constexpr int NACC = 2;
   static constexpr int ACOL0 = NACC * BN;
   static constexpr int NABUF = (kTmemCols - ACOL0) / 64;
-  static constexpr int B_BYTES = BN * kGroup * 2;
+  static constexpr int B_BYTES = BROWS * kGroup * 2;
   static constexpr int STAGE_BYTES = B_BYTES + TILE;
-  static constexpr int STAGES = (kSmemBudget - 2048) / STAGE_BYTES;  // 2 KB: barriers + alignment
+  static constexpr int STAGES = (kSmemBudget - 4096) / STAGE_BYTES;  // 4 KB: barriers, scale ring, alignment
   static constexpr int W_OFF = STAGES * B_BYTES;
   static constexpr int BAR_OFF = W_OFF + STAGES * TILE;
   static constexpr int NBARS = 2 * STAGES + 2 * NABUF + 2 * NACC + 1;
@@ -74,10 +76,23 @@ struct BulkCfg {
 // ZF: the zero-point-folded variant (see zero_point_share).  AX: the W4Ax
 // product (one accumulator per group, scaled per activation block; see
 // epilogue_role_ax).
-template <int GPT, bool ZF, bool AX = false>
-__global__ void __launch_bounds__(BulkCfg<GPT>::THREADS, 1) gemm_bulk_kernel(const __grid_constant__ GemmParams p) {
-  using C = BulkCfg<GPT>;
+// PAIR: launched in clusters of two CTAs (cluster rank = blockIdx.x % 2).  A
+// unit's tile is a pair tile (256 weight rows x 128 tokens): CTA r stages
+// weight tile 2 nt + r and tokens 64 r .. 64 r + 63 of every k-tile, dequantizes
+// its weight tile into its own TMEM, and holds that tile's accumulators; the
+// leading CTA (r = 0) issues the pair's M=256 MMAs, which read both CTAs'
+// operands, once both CTAs' dequant slots have arrived on its A-full barrier.
+// Each CTA's epilogue folds and writes its own 128 rows.  Half of every token
+// tile per SM halves the activation bytes each SM stages per group (24.3 KB
+// instead of 40.4 KB), so the same shared memory holds nine stages, not five.
+template <int GPT, bool ZF, bool AX = false, bool PAIR = false>
+__global__ void __launch_bounds__(BulkCfg<GPT, PAIR>::THREADS, 1)
+    gemm_bulk_kernel(const __grid_constant__ GemmParams p) {
+  static_assert(!(PAIR && (ZF || AX)), "the pair form covers the direct W4A8 product");
+  using C = BulkCfg<GPT, PAIR>;
   constexpr int BN = C::BN;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0;
+  const uint32_t widx = PAIR ? blockIdx.x >> 1 : blockIdx.x;  // worker index of the schedule
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -100,12 +115,12 @@ __global__ void __launch_bounds__(BulkCfg<GPT>::THREADS, 1) gemm_bulk_kernel(con
       mbar_init(bar_empty + 8 * s, 1 + 4);  // MMA commit + the 4 warps of one dequant slot
     }
     for (int a = 0; a < C::NABUF; ++a) {
-      mbar_init(bar_afull + 8 * a, 4);
+      mbar_init(bar_afull + 8 * a, PAIR ? 8 : 4);  // one dequant slot's warps (of both CTAs)
       mbar_init(bar_aempty + 8 * a, 1);
     }
     for (int b = 0; b < C::NACC; ++b) {
       mbar_init(bar_accfull + 8 * b, 1);
-      mbar_init(bar_accempty + 8 * b, C::NEPI);
+      mbar_init(bar_accempty + 8 * b, PAIR ? 2 * C::NEPI : C::NEPI);
     }
     mbar_init(bar_drain, 1);
     if (AX)
@@ -115,9 +130,15 @@ __global__ void __launch_bounds__(BulkCfg<GPT>::THREADS, 1) gemm_bulk_kernel(con
       }
     fence_mbar_init();
   }
-  if (warp == 1) tmem_alloc(sbase + C::TMEM_SLOT_OFF, kTmemCols);
+  if (warp == 1) {
+    if constexpr (PAIR)
+      tmem_alloc_pair(sbase + C::TMEM_SLOT_OFF, kTmemCols);
+    else
+      tmem_alloc(sbase + C::TMEM_SLOT_OFF, kTmemCols);
+  }
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync_all();  // both CTAs' barriers exist before either arrives remotely
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + C::TMEM_SLOT_OFF);
 
@@ -126,7 +147,7 @@ __global__ void __launch_bounds__(BulkCfg<GPT>::THREADS, 1) gemm_bulk_kernel(con
     if (lane == 0) {
       const uint64_t pol = policy_evict_last();  // weights and activations are both re-read
       UnitIter iter;
-      iter.init(p);
+      iter.init(p, widx);
       Unit u;
       bool have = iter.next(p, u);
       int g = have ? u.g0 : 0;
@@ -135,11 +156,13 @@ __global__ void __launch_bounds__(BulkCfg<GPT>::THREADS, 1) gemm_bulk_kernel(con
       // the current unit's tile coordinates (computed once per unit)
       TileXY xy = have ? tile_xy(p, u.tile) : TileXY{0, 0};
       auto issue_w = [&](int s, int nt, int gg) {
-        const uint8_t* src = p.packed + ((size_t)nt * p.G + gg) * C::TILE;
+        const int wt = PAIR ? 2 * nt + (int)rank : nt;  // this CTA's weight tile
+        const uint8_t* src = p.packed + ((size_t)wt * p.G + gg) * C::TILE;
         bulk_g2s(sbase + C::W_OFF + s * C::TILE, src, C::TILE, bar_full + 8 * s, pol);
       };
       auto issue_x = [&](int s, int mt, int gg) {
-        const uint16_t* src = p.xh + ((size_t)mt * p.G + gg) * (C::B_BYTES / 2);
+        // PAIR: this CTA's token half of the block, [2][64][64] fp16 in one piece
+        const uint16_t* src = p.xh + ((size_t)mt * p.G + gg) * (BN * kGroup) + (size_t)rank * (C::BROWS * kGroup);
         bulk_g2s(sbase + s * C::B_BYTES, src, C::B_BYTES, bar_full + 8 * s, pol);
       };
       // W4Ax: group number q's block scales into ring slot q % SCR
@@ -187,7 +210,7 @@ __global__ void __launch_bounds__(BulkCfg<GPT>::THREADS, 1) gemm_bulk_kernel(con
       while (have && sc_ok) {
         const int s = gi % C::STAGES;
         const uint32_t ph = (gi / C::STAGES) & 1;
-        if (!wait_bar(bar_empty + 8 * s, ph ^ 1, p)) break;
+        if (!wait_bar<PAIR>(bar_empty + 8 * s, ph ^ 1, p)) break;  // released by the pair's MMA too
         if (!issue_sc(gi, xy.mt, g)) break;
         if (!(p.fault == 1 && gi == (uint32_t)C::STAGES + 1)) {  // test hook: skip one stage
           mbar_arrive_expect_tx(bar_full + 8 * s, kStageTx);
@@ -218,10 +241,11 @@ __global__ void __launch_bounds__(BulkCfg<GPT>::THREADS, 1) gemm_bulk_kernel(con
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer --
     grid_dep_wait();
-    mma_role<BN, C::NACC, C::NABUF, C::ACOL0, AX ? 1 : (ZF ? kFoldGroupsZf : kFoldGroups)>(
-        p, tmem, bar_afull, bar_aempty, bar_accfull, bar_accempty, bar_drain,
-        [&](uint32_t gi, int) { return sbase + (uint32_t)((gi % C::STAGES) * C::B_BYTES); },
-        [&](uint32_t gi) { return bar_empty + 8 * (gi % C::STAGES); });
+    if (rank == 0)  // of a pair, the leading CTA issues
+      mma_role<BN, C::NACC, C::NABUF, C::ACOL0, AX ? 1 : (ZF ? kFoldGroupsZf : kFoldGroups), PAIR>(
+          p, tmem, bar_afull, bar_aempty, bar_accfull, bar_accempty, bar_drain,
+          [&](uint32_t gi, int) { return sbase + (uint32_t)((gi % C::STAGES) * C::B_BYTES); },
+          [&](uint32_t gi) { return bar_empty + 8 * (gi % C::STAGES); });
   } else if (warp < C::EPI_WARP0) {
     // ------------------------------------------------------------- dequant --
     grid_dep_wait();
@@ -230,7 +254,7 @@ __global__ void __launch_bounds__(BulkCfg<GPT>::THREADS, 1) gemm_bulk_kernel(con
     const int row = quad * 32 + lane;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     UnitIter iter;
-    iter.init(p);
+    iter.init(p, widx);
     Unit u;
     uint32_t gi = 0;
     bool ok = true;
@@ -242,7 +266,7 @@ __global__ void __launch_bounds__(BulkCfg<GPT>::THREADS, 1) gemm_bulk_kernel(con
         // every lane waits, then the warp votes: it reaches the tensor memory
         // stores below converged (see conv_wait_bar)
         const bool got = wait_seq(seq + 4 * s, gi + 1, p) && wait_bar(bar_full + 8 * s, (gi / C::STAGES) & 1, p) &&
-                         wait_bar(bar_aempty + 8 * a, ((gi / C::NABUF) & 1) ^ 1, p);
+                         wait_bar<PAIR>(bar_aempty + 8 * a, ((gi / C::NABUF) & 1) ^ 1, p);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
@@ -264,7 +288,10 @@ __global__ void __launch_bounds__(BulkCfg<GPT>::THREADS, 1) gemm_bulk_kernel(con
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(bar_afull + 8 * a);
+          if (PAIR && rank != 0)
+            mbar_arrive_remote(bar_afull + 8 * a, 0);  // the pair's MMAs are issued by the leading CTA
+          else
+            mbar_arrive(bar_afull + 8 * a);
           mbar_arrive(bar_empty + 8 * s);
         }
       }
@@ -277,21 +304,28 @@ __global__ void __launch_bounds__(BulkCfg<GPT>::THREADS, 1) gemm_bulk_kernel(con
                                                     reinterpret_cast<volatile int*>(smem + C::FLAG_OFF),
                                                     sbase + C::SC_OFF, sbase + C::SC_BAR_OFF);
     else
-      epilogue_role<BN, C::NEPI, C::NACC, ZF, C::TILE>(p, tmem, C::EPI_WARP0, bar_accfull, bar_accempty,
-                                                       reinterpret_cast<volatile int*>(smem + C::FLAG_OFF));
+      epilogue_role<BN, C::NEPI, C::NACC, ZF, C::TILE, ZF ? kFoldGroupsZf : kFoldGroups, PAIR>(
+          p, tmem, C::EPI_WARP0, bar_accfull, bar_accempty, reinterpret_cast<volatile int*>(smem + C::FLAG_OFF));
   }
 
   tc_fence_before();
   __syncthreads();
+  // A pair's MMAs read both CTAs' shared and tensor memory: neither CTA frees
+  // or leaves before the leading CTA's issuer has drained them.
+  if constexpr (PAIR) cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    if constexpr (PAIR)
+      tmem_dealloc_pair(tmem, kTmemCols);
+    else
+      tmem_dealloc(tmem, kTmemCols);
   }
 }
 
 // fp16 copy of Xq in the B-operand layout for 128-token tiles: [MT][G][2][128][64]
 // fp16, each [128][64] block 128B-swizzled (16-byte chunk c of row r stored at
-// chunk c ^ (r & 7)), rows m >= M zero.
+// chunk c ^ (r & 7)), rows m >= M zero; with c.split, [MT][G][2][2][64][64]
+// (token half, then channel half) for the CTA-pair kernel.
 __global__ void __launch_bounds__(256) convert_kernel(const ConvertParams c) {
   grid_dep_launch_dependents();  // the GEMM may launch and start streaming weights
   grid_dep_wait();               // Xq comes from the preceding kernel
@@ -307,7 +341,11 @@ __global__ void __launch_bounds__(256) convert_kernel(const ConvertParams c) {
     if (m < c.M) raw = __ldcg(reinterpret_cast<const uint4*>(c.Xq + (size_t)m * c.K + k0));  // L2: from the preceding kernel
     const int g = k0 / kGroup, kc = (k0 % kGroup) / 16;
     const int mt = m / c.BN, r = m % c.BN;
-    store_b_chunk(reinterpret_cast<uint8_t*>(c.xh + (size_t)(mt * G + g) * c.BN * kGroup), c.BN, r, kc, raw);
+    uint8_t* blk = reinterpret_cast<uint8_t*>(c.xh + (size_t)(mt * G + g) * c.BN * kGroup);
+    if (c.split)  // half r / 64 of the block, rows in the same 128B-swizzle phase (r % 64 = r mod 8 too)
+      store_b_chunk(blk + (r / 64) * (64 * kGroup * 2), 64, r % 64, kc, raw);
+    else
+      store_b_chunk(blk, c.BN, r, kc, raw);
   }
 }
 
@@ -434,6 +472,99 @@ cudaError_t launch_bulk(const GemmParams& p, bool zero_folded, cudaStream_t s) {
   }
 }
 
+
+// The CTA-pair kernel: clusters of two CTAs, p.P pairs.
+template <int GPT>
+cudaError_t launch_pair_g(const GemmParams& p, cudaStream_t s) {
+  using C = BulkCfg<GPT, true>;
+  static std::mutex mu;
+  static uint64_t done_mask = 0;
+  cudaError_t e;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    e = set_smem_attr_once(gemm_bulk_kernel<GPT, false, false, true>, C::SMEM_BYTES, done_mask);
+  }
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * p.P);
+  cfg.blockDim = dim3(C::THREADS);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0] = pdl_attr();
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, gemm_bulk_kernel<GPT, false, false, true>, p);
+}
+
+cudaError_t launch_pair(const GemmParams& p, cudaStream_t s) {
+  switch (p.gpt) {
+    case 1: return launch_pair_g<1>(p, s);
+    case 2: return launch_pair_g<2>(p, s);
+    case 4: return launch_pair_g<4>(p, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+// CTA pairs of the pair kernel that fit on the current device at once (one
+// CTA per SM; a GPC with an odd number of free SMs leaves one out), cached per
+// device.  0 if the query fails.
+int pair_capacity() {
+  static std::mutex mu;
+  static int cached[64];
+  static bool have[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev < 64 && have[dev]) return cached[dev];
+  using C = BulkCfg<1, true>;
+  uint64_t done_mask = 0;
+  if (set_smem_attr_once(gemm_bulk_kernel<1, false, false, true>, C::SMEM_BYTES, done_mask) != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * (kMaxGrid / 2));
+  cfg.blockDim = dim3(C::THREADS);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, gemm_bulk_kernel<1, false, false, true>, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    n = 0;
+  }
+  if (dev < 64) {
+    cached[dev] = n;
+    have[dev] = true;
+  }
+  return n;
+}
+
+// Whole tiles round-robin over the P0 persistent workers (CTAs, or CTA pairs);
+// when the last wave would be partial, it and one full wave are split along K
+// instead (stream-K), so every worker gets the same number of groups.
+void make_schedule(GemmParams& p, int P0) {
+  P0 = std::max(1, P0);
+  if (p.T >= P0) {
+    const int rem = p.T % P0;
+    p.T_sk = rem == 0 ? 0 : std::min(p.T, rem + P0);
+    p.T_dp = p.T - p.T_sk;
+    p.P = P0;
+  } else {
+    p.T_dp = 0;
+    p.T_sk = p.T;
+    const long long want = ((long long)p.T * p.G + 3) / 4;  // at least ~4 groups per worker
+    p.P = (int)std::max<long long>(1, std::min<long long>(P0, want));
+  }
+  p.I_sk = (uint32_t)p.T_sk * (uint32_t)p.G;  // T_sk <= 2 P0 - 1 <= 511, G <= 1024
+}
 }  // namespace
 
 cudaError_t launch_gemm(int M, int N, int K, int g, const int8_t* Xq, const uint16_t* sx,
@@ -449,24 +580,15 @@ cudaError_t launch_gemm(int M, int N, int K, int g, const int8_t* Xq, const uint
   p.G = K / kGroup;
   p.gpt = gpt_for_group(g);
   p.MT = (M + BN - 1) / BN;
-  p.NT = N / kTileN;
+  // The direct product of 128-token tiles runs on CTA pairs (M=256 MMAs, each
+  // SM staging half of every token tile) when N is a multiple of 256; then a
+  // tile is a pair tile of 256 weight rows.
+  const int pairs = std::min(num_sms, kMaxGrid) / 2;
+  const int cap = (BN == 128 && !zero_folded && N % (2 * kTileN) == 0 && pairs > 0) ? pair_capacity() : 0;
+  const bool pair = cap > 0;
+  p.NT = N / (pair ? 2 * kTileN : kTileN);
   p.T = p.MT * p.NT;
-  // Whole tiles round-robin over the persistent CTAs; when the last wave
-  // would be partial, it and one full wave are split along K instead
-  // (stream-K), so every CTA gets the same number of groups.
-  const int P0s = std::max(1, std::min(num_sms, kMaxGrid));
-  if (p.T >= P0s) {
-    const int rem = p.T % P0s;
-    p.T_sk = rem == 0 ? 0 : std::min(p.T, rem + P0s);
-    p.T_dp = p.T - p.T_sk;
-    p.P = P0s;
-  } else {
-    p.T_dp = 0;
-    p.T_sk = p.T;
-    const long long want = ((long long)p.T * p.G + 3) / 4;  // at least ~4 groups per CTA
-    p.P = (int)std::max<long long>(1, std::min<long long>(P0s, want));
-  }
-  p.I_sk = (uint32_t)p.T_sk * (uint32_t)p.G;  // T_sk <= 2 P0 - 1 <= 511, G <= 1024
+  make_schedule(p, pair ? std::min(pairs, cap) : std::min(num_sms, kMaxGrid));
   uint8_t* w = static_cast<uint8_t*>(ws);
   p.status = reinterpret_cast<int*>(w);
   p.sk_cnt = reinterpret_cast<int32_t*>(w + L.cnt_off);
@@ -519,6 +641,7 @@ cudaError_t launch_gemm(int M, int N, int K, int g, const int8_t* Xq, const uint
   c.K = K;
   c.BN = BN;
   c.MT = p.MT;
+  c.split = pair ? 1 : 0;
   const long long work = (long long)p.MT * BN * (K / 16);
   const int cblocks = (int)std::max<long long>(1, std::min<long long>((work + 255) / 256, (long long)P0 * 4));
   cudaLaunchConfig_t cfg = {};
@@ -530,7 +653,7 @@ cudaError_t launch_gemm(int M, int N, int K, int g, const int8_t* Xq, const uint
   cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, convert_kernel, c);
   if (e != cudaSuccess) return e;
-  return launch_bulk(p, zero_folded, s);
+  return pair ? launch_pair(p, s) : launch_bulk(p, zero_folded, s);
 }
 
 cudaError_t launch_w4ax(int M, int N, int K, int g, int n8, const uint8_t* Xa, const uint16_t* sxb,
@@ -548,18 +671,7 @@ cudaError_t launch_w4ax(int M, int N, int K, int g, int n8, const uint8_t* Xa, c
   p.NT = N / kTileN;
   p.T = p.MT * p.NT;
   const int P0 = std::max(1, std::min(num_sms, kMaxGrid));
-  if (p.T >= P0) {  // the schedule of launch_gemm
-    const int rem = p.T % P0;
-    p.T_sk = rem == 0 ? 0 : std::min(p.T, rem + P0);
-    p.T_dp = p.T - p.T_sk;
-    p.P = P0;
-  } else {
-    p.T_dp = 0;
-    p.T_sk = p.T;
-    const long long want = ((long long)p.T * p.G + 3) / 4;
-    p.P = (int)std::max<long long>(1, std::min<long long>(P0, want));
-  }
-  p.I_sk = (uint32_t)p.T_sk * (uint32_t)p.G;
+  make_schedule(p, P0);
   uint8_t* w = static_cast<uint8_t*>(ws);
   p.status = reinterpret_cast<int*>(w);
   p.sk_cnt = reinterpret_cast<int32_t*>(w + L.cnt_off);

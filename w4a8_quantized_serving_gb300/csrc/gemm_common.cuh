@@ -27,9 +27,10 @@ constexpr int kSmemBudget = 227 * 1024;  // per-CTA dynamic shared memory limit
 
 // tcgen05 instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B
 // fp16 (bits 7-9, 10-12 = 0), both K-major (bits 15, 16 = 0), N >> 3 in bits
-// 17-22, M >> 4 in bits 24-28; M = 128 (one weight tile).
-__host__ __device__ constexpr uint32_t mma_idesc(int n) {
-  return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kTileN >> 4) << 24);
+// 17-22, M >> 4 in bits 24-28; M = 128 (one weight tile), or 256 for the
+// CTA-pair MMA (one weight tile in each CTA).
+__host__ __device__ constexpr uint32_t mma_idesc(int n, int m = kTileN) {
+  return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
 // Exact dequant of a pair of 4-bit codes (QServe "subtraction after
@@ -122,10 +123,11 @@ struct Unit {
 struct UnitIter {
   int dp_next;
   uint32_t it, it_end;
-  __device__ __forceinline__ void init(const GemmParams& p) {
-    dp_next = blockIdx.x;
-    it = blockIdx.x * p.I_sk / (uint32_t)p.P;
-    it_end = (blockIdx.x + 1) * p.I_sk / (uint32_t)p.P;
+  // idx: this worker's index among the p.P workers (a CTA, or a CTA pair)
+  __device__ __forceinline__ void init(const GemmParams& p, uint32_t idx = blockIdx.x) {
+    dp_next = (int)idx;
+    it = idx * p.I_sk / (uint32_t)p.P;
+    it_end = (idx + 1) * p.I_sk / (uint32_t)p.P;
   }
   __device__ __forceinline__ bool next(const GemmParams& p, Unit& u) {
     if (dp_next < p.T_dp) {
@@ -178,13 +180,13 @@ __device__ __forceinline__ TileXY tile_xy(const GemmParams& p, int t) {
 // already recorded one.  The loop polls only the barrier for the first ~100k
 // cycles; the global timer and the abort word in global memory are read after
 // that, so a normal hand-off never waits behind a global load.
-__device__ __noinline__ inline bool wait_slow(uint32_t bar, uint32_t parity, const GemmParams& p,
-                                              bool honor_abort) {
+template <bool CL = false>
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const GemmParams& p, bool honor_abort) {
   volatile unsigned* abort_word = reinterpret_cast<volatile unsigned*>(p.status + 1);
   const long long c0 = clock64();
   uint64_t t0 = 0;
   for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (CL ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
     if ((i & 255) == 0 && clock64() - c0 > 100000) {
       const uint64_t now = global_timer_ns();
       if (t0 == 0) t0 = now;
@@ -198,10 +200,13 @@ __device__ __noinline__ inline bool wait_slow(uint32_t bar, uint32_t parity, con
   }
 }
 
+// CL: acquire at cluster scope, for barriers that the other CTA of a CTA pair
+// (or the pair's tensor-core operations) arrive on.
+template <bool CL = false>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const GemmParams& p,
                                          bool honor_abort = true) {
-  if (mbar_try_wait(bar, parity)) return true;
-  return wait_slow(bar, parity, p, honor_abort);
+  if (CL ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+  return wait_slow<CL>(bar, parity, p, honor_abort);
 }
 
 // Per-stage sequence words in shared memory: the producer publishes, with
@@ -257,9 +262,10 @@ __device__ __noinline__ inline bool spin_ok(const GemmParams& p, uint64_t& t0) {
 }
 
 // Lane 0 waits, the warp learns the outcome (keeps the warp converged).
+template <bool CL = false>
 __device__ __forceinline__ bool warp_wait_bar(uint32_t bar, uint32_t parity, const GemmParams& p) {
   int ok = 1;
-  if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, p);
+  if ((threadIdx.x & 31) == 0) ok = wait_bar<CL>(bar, parity, p);
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
@@ -269,8 +275,9 @@ __device__ __forceinline__ bool warp_wait_bar(uint32_t bar, uint32_t parity, con
 // st .sync.aligned, elect.sync); so a wait followed by one, with no
 // __syncwarp in between, takes this form or warp_wait_bar's.  The vote
 // returns the warp converged, with one outcome for all lanes.
+template <bool CL = false>
 __device__ __forceinline__ bool conv_wait_bar(uint32_t bar, uint32_t parity, const GemmParams& p) {
-  const bool ok = wait_bar(bar, parity, p);
+  const bool ok = wait_bar<CL>(bar, parity, p);
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -396,13 +403,27 @@ __device__ __forceinline__ void write_tile_out(const GemmParams& p, const int32_
 // address of group gi's B tile; the group's A-full barrier covers it too.
 // After each MMA group: commits to `bar_aempty[a]` and to `extra_commit(gi)`
 // (0 = none).
-template <int BN, int NACC, int NABUF, int ACOL0, int FOLD, typename BTile, typename ExtraCommit>
+// PAIR: the warp of the pair's leading CTA issues the pair's MMAs (M=256:
+// each CTA's weight tile from its own TMEM; N=BN tokens, the first BN/2 from
+// this CTA's B half, the rest from the other CTA's, at the same offset), its
+// waits are cluster-scope (the other CTA arrives on the A-full and
+// accumulator-empty barriers too), and every commit but the drain arrives on
+// the same barrier in both CTAs.
+template <int BN, int NACC, int NABUF, int ACOL0, int FOLD, bool PAIR = false, typename BTile,
+          typename ExtraCommit>
 __device__ __forceinline__ void mma_role(const GemmParams& p, uint32_t tmem, uint32_t bar_afull,
                                          uint32_t bar_aempty, uint32_t bar_accfull, uint32_t bar_accempty,
                                          uint32_t bar_drain, BTile b_tile, ExtraCommit extra_commit) {
-  constexpr uint32_t kIdesc = mma_idesc(BN);
+  constexpr uint32_t kIdesc = mma_idesc(BN, PAIR ? 2 * kTileN : kTileN);
+  constexpr uint32_t kBRows = PAIR ? BN / 2 : BN;  // rows of this CTA's B tile
+  auto commit = [](uint32_t bar) {
+    if constexpr (PAIR)
+      tc_commit_pair_mc(bar, 3);
+    else
+      tc_commit(bar);
+  };
   UnitIter iter;
-  iter.init(p);
+  iter.init(p, PAIR ? blockIdx.x >> 1 : blockIdx.x);
   Unit u;
   uint32_t gi = 0, chunk = 0;
   bool ok = true;
@@ -410,7 +431,7 @@ __device__ __forceinline__ void mma_role(const GemmParams& p, uint32_t tmem, uin
     for (int c0 = u.g0; c0 < u.g1; c0 += FOLD) {
       const int c1 = min(u.g1, c0 + FOLD);
       const int b = chunk % NACC;
-      if (!warp_wait_bar(bar_accempty + 8 * b, ((chunk / NACC) & 1) ^ 1, p)) {
+      if (!warp_wait_bar<PAIR>(bar_accempty + 8 * b, ((chunk / NACC) & 1) ^ 1, p)) {
         ok = false;
         break;
       }
@@ -418,7 +439,7 @@ __device__ __forceinline__ void mma_role(const GemmParams& p, uint32_t tmem, uin
       const uint32_t d_tmem = tmem + b * BN;
       for (int g = c0; g < c1; ++g, ++gi) {
         const int a = gi % NABUF;
-        if (!warp_wait_bar(bar_afull + 8 * a, (gi / NABUF) & 1, p)) {
+        if (!warp_wait_bar<PAIR>(bar_afull + 8 * a, (gi / NABUF) & 1, p)) {
           ok = false;
           break;
         }
@@ -428,25 +449,35 @@ __device__ __forceinline__ void mma_role(const GemmParams& p, uint32_t tmem, uin
         const uint32_t a_col = tmem + ACOL0 + a * 64;
         if (elect_one()) {
 #pragma unroll
-          for (int j = 0; j < 8; ++j)  // K step j: 64-channel half j / 4, 32-byte chunk j % 4
-            tc_mma_ts(d_tmem, a_col + 8 * j, b_lo + (j >> 2) * (BN * 8) + (j & 3) * 2, kDescSw128Hi, kIdesc,
-                       (g > c0 || j > 0) ? 1u : 0u);
-          tc_commit(bar_aempty + 8 * a);
+          for (int j = 0; j < 8; ++j) {  // K step j: 64-channel half j / 4, 32-byte chunk j % 4
+            const uint32_t bl = b_lo + (j >> 2) * (kBRows * 8) + (j & 3) * 2;
+            const uint32_t acc = (g > c0 || j > 0) ? 1u : 0u;
+            if constexpr (PAIR)
+              tc_mma_ts_pair(d_tmem, a_col + 8 * j, bl, kDescSw128Hi, kIdesc, acc);
+            else
+              tc_mma_ts(d_tmem, a_col + 8 * j, bl, kDescSw128Hi, kIdesc, acc);
+          }
+          commit(bar_aempty + 8 * a);
           const uint32_t xc = extra_commit(gi);
-          if (xc) tc_commit(xc);
+          if (xc) commit(xc);
         }
         __syncwarp();
       }
       if (!ok) break;
-      if (elect_one()) tc_commit(bar_accfull + 8 * b);
+      if (elect_one()) commit(bar_accfull + 8 * b);
       __syncwarp();
       ++chunk;
     }
   }
   // all MMAs issued by this warp complete before TMEM is released
-  if (elect_one()) tc_commit(bar_drain);
+  if (elect_one()) {
+    if constexpr (PAIR)
+      tc_commit_pair_mc(bar_drain, 1);  // this (the leading) CTA only
+    else
+      tc_commit(bar_drain);
+  }
   __syncwarp();
-  if ((threadIdx.x & 31) == 0) wait_bar(bar_drain, 0, p, false);
+  if ((threadIdx.x & 31) == 0) wait_bar<PAIR>(bar_drain, 0, p, false);
   __syncwarp();
 }
 
@@ -455,9 +486,11 @@ __device__ __forceinline__ void mma_role(const GemmParams& p, uint32_t tmem, uin
 // split tile's int32 partial sums are added into the workspace, and the last
 // contributor writes Y and leaves the workspace zeroed.  `run` holds tokens
 // tok0 .. tok0 + TOK - 1 of weight row `row` (output channel n; first token m0).
+// `sk` indexes the split tile's partial sums and count (for a CTA pair, each
+// CTA's half of a pair tile has its own).
 template <int BN, int NEPI, int TOK>
-__device__ __forceinline__ void finish_unit(const GemmParams& p, const Unit& u, int32_t (&run)[TOK], int m0, int n,
-                                            int tok0, int row, int etid, bool ok, volatile int* last_flag,
+__device__ __forceinline__ void finish_unit(const GemmParams& p, const Unit& u, int sk, int32_t (&run)[TOK], int m0,
+                                            int n, int tok0, int row, int etid, bool ok, volatile int* last_flag,
                                             bool tracer, int unit_no) {
   (void)tracer;
   (void)unit_no;
@@ -465,7 +498,6 @@ __device__ __forceinline__ void finish_unit(const GemmParams& p, const Unit& u, 
     if (ok) write_tile_out<TOK>(p, run, m0, n);
     return;
   }
-  const int sk = u.tile - p.T_dp;
   int32_t* part = p.sk_acc + (size_t)sk * BN * kTileN + (size_t)tok0 * kTileN;
   if (ok) {
 #pragma unroll
@@ -502,11 +534,15 @@ __device__ __forceinline__ void finish_unit(const GemmParams& p, const Unit& u, 
 // lane.  Per fold chunk: read the fp32 accumulator, convert to int32 (exact),
 // add.  At a unit's end: write Y (whole-K tile), or add the int32 partials
 // into the workspace and let the last contributor write Y and clear them.
+// PAIR: this CTA holds weight tile 2 nt + rank of pair tile nt, and releases
+// an accumulator on the leading CTA's barrier (where the pair's MMAs are
+// issued).
 template <int BN, int NEPI, int NACC, bool ZF = false, int TILE = kWTileBytes,
-          int FOLD = ZF ? kFoldGroupsZf : kFoldGroups>
+          int FOLD = ZF ? kFoldGroupsZf : kFoldGroups, bool PAIR = false>
 __device__ __forceinline__ void epilogue_role(const GemmParams& p, uint32_t tmem, int epi_warp0,
                                               uint32_t bar_accfull, uint32_t bar_accempty,
                                               volatile int* last_flag) {
+  static_assert(!(PAIR && ZF), "the pair kernel has no zero-point-folded form");
   constexpr int TOK = BN / (NEPI / 4);
   static_assert(TOK % 16 == 0, "epilogue loads 16 columns at a time");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -516,8 +552,9 @@ __device__ __forceinline__ void epilogue_role(const GemmParams& p, uint32_t tmem
   const int tok0 = (e >> 2) * TOK;
   const int etid = threadIdx.x - epi_warp0 * 32;
   const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+  const uint32_t rank = PAIR ? blockIdx.x & 1 : 0;
   UnitIter iter;
-  iter.init(p);
+  iter.init(p, PAIR ? blockIdx.x >> 1 : blockIdx.x);
   Unit u;
   uint32_t chunk = 0;
   int unit_no = 0;
@@ -525,7 +562,7 @@ __device__ __forceinline__ void epilogue_role(const GemmParams& p, uint32_t tmem
   while (iter.next(p, u)) {
     const TileXY xy = tile_xy(p, u.tile);
     const int nt = xy.nt, mt = xy.mt;
-    const int n = nt * kTileN + row;
+    const int n = (PAIR ? 2 * nt + (int)rank : nt) * kTileN + row;
     int32_t run[TOK];
 #pragma unroll
     for (int i = 0; i < TOK; ++i) run[i] = 0;
@@ -533,7 +570,7 @@ __device__ __forceinline__ void epilogue_role(const GemmParams& p, uint32_t tmem
       const int b = chunk % NACC;
       // zero points' share of the chunk, while its MMAs still run
       if constexpr (ZF) zero_point_share<TOK, TILE>(p, nt, c0, min(u.g1, c0 + FOLD), mt * BN + tok0, row, run);
-      if (ok) ok = conv_wait_bar(bar_accfull + 8 * b, (chunk / NACC) & 1, p);
+      if (ok) ok = conv_wait_bar<PAIR>(bar_accfull + 8 * b, (chunk / NACC) & 1, p);
       if (e == 0 && lane == 0) QOQ_TRACE_AT(p, 512 + (int)chunk, 0);
       if (ok) {
         tc_fence_after();
@@ -546,12 +583,18 @@ __device__ __forceinline__ void epilogue_role(const GemmParams& p, uint32_t tmem
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar_accempty + 8 * b);
+        if (lane == 0) {
+          if (PAIR && rank != 0)
+            mbar_arrive_remote(bar_accempty + 8 * b, 0);
+          else
+            mbar_arrive(bar_accempty + 8 * b);
+        }
         if (e == 0 && lane == 0) QOQ_TRACE_AT(p, 576 + (int)chunk, 0);
       }
     }
-    finish_unit<BN, NEPI, TOK>(p, u, run, mt * BN + tok0, n, tok0, row, etid, ok, last_flag, e == 0 && lane == 0,
-                                unit_no);
+    const int sk = PAIR ? 2 * (u.tile - p.T_dp) + (int)rank : u.tile - p.T_dp;
+    finish_unit<BN, NEPI, TOK>(p, u, sk, run, mt * BN + tok0, n, tok0, row, etid, ok, last_flag,
+                                e == 0 && lane == 0, unit_no);
     if (e == 0 && lane == 0) QOQ_TRACE_AT(p, 640 + unit_no, 0);
     ++unit_no;
   }

@@ -161,10 +161,14 @@ constexpr int kTraceSlots = 1024;
   } while (0)
 #endif
 
+// split: the CTA-pair layout, each [128][128] token x channel block stored as
+// two [64][128] halves (tokens 0..63, then 64..127), each [2][64][64] (the
+// 64-channel halves), so that each CTA of a pair copies its half in one piece.
 struct ConvertParams {
   const int8_t* Xq;
   uint16_t* xh;
   int M, K, BN, MT;
+  int split;
 };
 
 // W4Ax activations (mixed 8-bit / 4-bit 128-channel blocks, n8 leading 8-bit

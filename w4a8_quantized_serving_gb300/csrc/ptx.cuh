@@ -63,6 +63,46 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The same phase test with cluster-scope acquire, for barriers that the peer
+// CTA of a CTA pair (or its tensor-core operations) arrive on.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// ----------------------------------------------------------------- clusters --
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Every thread of every CTA of the cluster (an aligned, whole-CTA call).
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Arrive on the mbarrier at shared offset `bar` of CTA `cta` of this cluster.
+// The hand-offs it signals are of tensor memory, ordered by the tcgen05
+// fences around the arrive and the wait, so the release is at CTA scope: a
+// cluster-scope release would first wait for this thread's earlier global
+// stores (output tiles, split-K sums) to become visible, and stalled the
+// CTA-pair GEMM's epilogue and dequant warps (ncu: membar stalls 1.8 per
+// issued instruction, 38% longer at M=4096).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar, uint32_t cta) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(bar), "r"(cta));
+  asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(r) : "memory");
+}
+
 // ------------------------------------------------------------ bulk copies --
 
 // One contiguous global -> shared copy completing on an mbarrier (tx bytes).
@@ -129,6 +169,23 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
                : "memory");
 }
 
+// The CTA-pair forms (cta_group::2: one allocation at the same columns of
+// both CTAs' tensor memory, issued by one warp in each CTA; MMAs issued by one
+// thread of the pair with M = 256 rows, 128 in each CTA's tensor memory, and
+// B split by columns between the two CTAs' shared memory at the same offset).
+// A kernel uses either these or the cta_group::1 forms, never both.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -145,6 +202,15 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
                : "memory");
 }
 
+// Pair form: arrive on the barrier at shared offset `bar` of every CTA in
+// `cta_mask` when this thread's previously issued tcgen05 operations complete.
+__device__ __forceinline__ void tc_commit_pair_mc(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(cta_mask)
+      : "memory");
+}
+
 // D[tmem] (+)= A[tmem] * B[smem desc]^T, kind::f16 (fp16/bf16 in, fp32 accumulate).
 // The shared-memory descriptor is passed as its two 32-bit halves, so that a
 // caller stepping through a tile adds to the low half only.
@@ -155,6 +221,18 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint
       "setp.ne.b32 p, %5, 0;\n\t"
       "mov.b64 d, {%2, %3};\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], d, %4, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(desc_lo), "r"(desc_hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Pair form of tc_mma_ts (issued by one thread of the leading CTA).
+__device__ __forceinline__ void tc_mma_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint32_t desc_lo,
+                                                uint32_t desc_hi, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 d;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "mov.b64 d, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], d, %4, p;\n\t}\n" ::"r"(d_tmem),
       "r"(a_tmem), "r"(desc_lo), "r"(desc_hi), "r"(idesc), "r"(accumulate)
       : "memory");
 }
