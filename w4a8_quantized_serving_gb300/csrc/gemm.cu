@@ -48,13 +48,21 @@ struct BulkCfg {
   static constexpr int NDQ = 4 * NSLOT;
   static constexpr int NEPI = 16;   // 4 per TMEM lane quadrant, 32 tokens each
   static constexpr int EPI_WARP0 = 2 + NDQ;
-  static constexpr int THREADS = (2 + NDQ + NEPI) * 32;
+  // Copy-issuing warps: warp 0, and with two the last warp of the CTA.  A
+  // bulk copy takes a few hundred ns to issue while the SM is busy, so one
+  // issuing thread paces the pair kernel's ring (one stage per ~320 ns at
+  // M=128 before any wait); producer w serves the groups gi with gi % NPROD
+  // == w from its own sub-ring of SPS stages.
+  static constexpr int NPROD = PAIR ? 2 : 1;
+  static constexpr int PROD2_WARP = EPI_WARP0 + NEPI;
+  static constexpr int THREADS = (2 + NDQ + NEPI + (NPROD - 1)) * 32;
   static constexpr int NACC = 2;
   static constexpr int ACOL0 = NACC * BN;
   static constexpr int NABUF = (kTmemCols - ACOL0) / 64;
   static constexpr int B_BYTES = BROWS * kGroup * 2;
   static constexpr int STAGE_BYTES = B_BYTES + TILE;
-  static constexpr int STAGES = (kSmemBudget - 4096) / STAGE_BYTES;  // 4 KB: barriers, scale ring, alignment
+  static constexpr int STAGES = (kSmemBudget - 4096) / STAGE_BYTES / NPROD * NPROD;  // 4 KB: barriers, scale ring, alignment
+  static constexpr int SPS = STAGES / NPROD;  // stages per producer
   static constexpr int W_OFF = STAGES * B_BYTES;
   static constexpr int BAR_OFF = W_OFF + STAGES * TILE;
   static constexpr int NBARS = 2 * STAGES + 2 * NABUF + 2 * NACC + 1;
@@ -69,9 +77,22 @@ struct BulkCfg {
   static constexpr int SC_BAR_OFF = SC_OFF + SCR * 256;
   static constexpr int SMEM_BYTES = SC_BAR_OFF + 2 * SCR * 8 + 1024;  // + slack for 1024-B alignment
   static_assert(NABUF >= NSLOT + 1, "A buffers");
-  static_assert(STAGES >= 3, "pipeline depth");
+  static_assert(STAGES >= 3 && SPS >= 2, "pipeline depth");
+  static_assert(NPROD == 1 || SCR % NPROD == 0, "each producer owns the scale slots of its groups");
   static_assert(SMEM_BYTES <= kSmemBudget, "shared memory");
 };
+
+// Stage of group gi (the CTA's gi-th group): sub-ring gi % NPROD, lap k / SPS
+// of its k = gi / NPROD-th use.
+struct StageRef {
+  int s;
+  uint32_t lap;
+};
+template <class C>
+__device__ __forceinline__ StageRef stage_of(uint32_t gi) {
+  const uint32_t k = gi / C::NPROD;
+  return StageRef{(int)((gi % C::NPROD) * C::SPS + k % C::SPS), k / C::SPS};
+}
 
 // ZF: the zero-point-folded variant (see zero_point_share).  AX: the W4Ax
 // product (one accumulator per group, scaled per activation block; see
@@ -142,19 +163,34 @@ __global__ void __launch_bounds__(BulkCfg<GPT, PAIR>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + C::TMEM_SLOT_OFF);
 
-  if (warp == 0) {
+  if (warp == 0 || (C::NPROD > 1 && warp == C::PROD2_WARP)) {
     // ------------------------------------------------------------ producer --
     if (lane == 0) {
+      const uint32_t w = warp == 0 ? 0u : 1u;  // this producer's groups: gi % NPROD == w
       const uint64_t pol = policy_evict_last();  // weights and activations are both re-read
       UnitIter iter;
       iter.init(p, widx);
       Unit u;
       bool have = iter.next(p, u);
       int g = have ? u.g0 : 0;
+      uint32_t gi = 0;
       uint32_t issued_mask = 0, issued_par = 0;  // per stage: last issue and its parity
       constexpr uint32_t kStageTx = C::TILE + C::B_BYTES;
       // the current unit's tile coordinates (computed once per unit)
       TileXY xy = have ? tile_xy(p, u.tile) : TileXY{0, 0};
+      auto advance = [&]() {  // to this producer's next group
+        do {
+          ++gi;
+          if (++g >= u.g1) {
+            have = iter.next(p, u);
+            if (have) {
+              g = u.g0;
+              xy = tile_xy(p, u.tile);
+            }
+          }
+        } while (have && gi % C::NPROD != w);
+      };
+      if (have && gi % C::NPROD != w) advance();
       auto issue_w = [&](int s, int nt, int gg) {
         const int wt = PAIR ? 2 * nt + (int)rank : nt;  // this CTA's weight tile
         const uint8_t* src = p.packed + ((size_t)wt * p.G + gg) * C::TILE;
@@ -165,7 +201,8 @@ __global__ void __launch_bounds__(BulkCfg<GPT, PAIR>::THREADS, 1)
         const uint16_t* src = p.xh + ((size_t)mt * p.G + gg) * (BN * kGroup) + (size_t)rank * (C::BROWS * kGroup);
         bulk_g2s(sbase + s * C::B_BYTES, src, C::B_BYTES, bar_full + 8 * s, pol);
       };
-      // W4Ax: group number q's block scales into ring slot q % SCR
+      // W4Ax: group number q's block scales into ring slot q % SCR (with two
+      // producers, each owns the slots of its groups' parity)
       uint32_t sc_mask = 0, sc_par = 0;  // per slot: a copy in its latest lap; its parity
       auto issue_sc = [&](uint32_t qn, int mt, int gg) -> bool {
         if (!AX) return true;
@@ -181,55 +218,45 @@ __global__ void __launch_bounds__(BulkCfg<GPT, PAIR>::THREADS, 1)
       };
       // Weights do not depend on the preceding kernels: issue a few stages
       // before waiting on them.
+      constexpr int kPre = kPrefetchStages / C::NPROD < C::SPS ? kPrefetchStages / C::NPROD : C::SPS;
       int npre = 0;
-      int pre_mt[kPrefetchStages], pre_g[kPrefetchStages];
-      while (have && npre < kPrefetchStages) {
-        const int s = npre;
-        mbar_arrive_expect_tx(bar_full + 8 * s, kStageTx);
-        issue_w(s, xy.nt, g);
-        st_release_shared(seq + 4 * s, (uint32_t)npre + 1);
+      int pre_mt[kPre], pre_g[kPre], pre_s[kPre];
+      uint32_t pre_gi[kPre];
+      while (have && npre < kPre) {  // first lap of the sub-ring: no stage to wait for
+        const StageRef st = stage_of<C>(gi);
+        mbar_arrive_expect_tx(bar_full + 8 * st.s, kStageTx);
+        issue_w(st.s, xy.nt, g);
+        st_release_shared(seq + 4 * st.s, gi + 1);
         pre_mt[npre] = xy.mt;
         pre_g[npre] = g;
-        issued_mask |= 1u << s;
+        pre_s[npre] = st.s;
+        pre_gi[npre] = gi;
+        issued_mask |= 1u << st.s;
         ++npre;
-        if (++g >= u.g1) {
-          have = iter.next(p, u);
-          if (have) {
-            g = u.g0;
-            xy = tile_xy(p, u.tile);
-          }
-        }
+        advance();
       }
       grid_dep_wait();
       bool sc_ok = true;
       for (int i = 0; i < npre; ++i) {
-        issue_x(i, pre_mt[i], pre_g[i]);
-        if (sc_ok) sc_ok = issue_sc((uint32_t)i, pre_mt[i], pre_g[i]);
+        issue_x(pre_s[i], pre_mt[i], pre_g[i]);
+        if (sc_ok) sc_ok = issue_sc(pre_gi[i], pre_mt[i], pre_g[i]);
       }
-      uint32_t gi = npre;
       while (have && sc_ok) {
-        const int s = gi % C::STAGES;
-        const uint32_t ph = (gi / C::STAGES) & 1;
-        if (!wait_bar<PAIR>(bar_empty + 8 * s, ph ^ 1, p)) break;  // released by the pair's MMA too
+        const StageRef st = stage_of<C>(gi);
+        const uint32_t ph = st.lap & 1;
+        if (st.lap > 0 && !wait_bar<PAIR>(bar_empty + 8 * st.s, ph ^ 1, p)) break;  // released by the pair's MMA too
         if (!issue_sc(gi, xy.mt, g)) break;
         if (!(p.fault == 1 && gi == (uint32_t)C::STAGES + 1)) {  // test hook: skip one stage
-          mbar_arrive_expect_tx(bar_full + 8 * s, kStageTx);
-          issue_w(s, xy.nt, g);
-          issue_x(s, xy.mt, g);
-          st_release_shared(seq + 4 * s, gi + 1);
-          issued_mask |= 1u << s;
-          issued_par = (issued_par & ~(1u << s)) | (ph << s);
+          mbar_arrive_expect_tx(bar_full + 8 * st.s, kStageTx);
+          issue_w(st.s, xy.nt, g);
+          issue_x(st.s, xy.mt, g);
+          st_release_shared(seq + 4 * st.s, gi + 1);
+          issued_mask |= 1u << st.s;
+          issued_par = (issued_par & ~(1u << st.s)) | (ph << st.s);
         } else {
-          issued_mask &= ~(1u << s);
+          issued_mask &= ~(1u << st.s);
         }
-        ++gi;
-        if (++g >= u.g1) {
-          have = iter.next(p, u);
-          if (have) {
-            g = u.g0;
-            xy = tile_xy(p, u.tile);
-          }
-        }
+        advance();
       }
       // Let every copy still in flight land before the CTA may exit.
       for (int s = 0; s < C::STAGES; ++s)
@@ -244,8 +271,8 @@ __global__ void __launch_bounds__(BulkCfg<GPT, PAIR>::THREADS, 1)
     if (rank == 0)  // of a pair, the leading CTA issues
       mma_role<BN, C::NACC, C::NABUF, C::ACOL0, AX ? 1 : (ZF ? kFoldGroupsZf : kFoldGroups), PAIR>(
           p, tmem, bar_afull, bar_aempty, bar_accfull, bar_accempty, bar_drain,
-          [&](uint32_t gi, int) { return sbase + (uint32_t)((gi % C::STAGES) * C::B_BYTES); },
-          [&](uint32_t gi) { return bar_empty + 8 * (gi % C::STAGES); });
+          [&](uint32_t gi, int) { return sbase + (uint32_t)(stage_of<C>(gi).s * C::B_BYTES); },
+          [&](uint32_t gi) { return bar_empty + 8 * stage_of<C>(gi).s; });
   } else if (warp < C::EPI_WARP0) {
     // ------------------------------------------------------------- dequant --
     grid_dep_wait();
@@ -261,11 +288,12 @@ __global__ void __launch_bounds__(BulkCfg<GPT, PAIR>::THREADS, 1)
     while (ok && iter.next(p, u)) {
       for (int g = u.g0; g < u.g1; ++g, ++gi) {
         if ((int)(gi % C::NSLOT) != slot) continue;
-        const int s = gi % C::STAGES;
+        const StageRef st = stage_of<C>(gi);
+        const int s = st.s;
         const int a = gi % C::NABUF;
         // every lane waits, then the warp votes: it reaches the tensor memory
         // stores below converged (see conv_wait_bar)
-        const bool got = wait_seq(seq + 4 * s, gi + 1, p) && wait_bar(bar_full + 8 * s, (gi / C::STAGES) & 1, p) &&
+        const bool got = wait_seq(seq + 4 * s, gi + 1, p) && wait_bar(bar_full + 8 * s, st.lap & 1, p) &&
                          wait_bar<PAIR>(bar_aempty + 8 * a, ((gi / C::NABUF) & 1) ^ 1, p);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
