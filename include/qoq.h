@@ -326,15 +326,25 @@ qoq_status qoq_w4ax_gemm(int M, int N, int K, int g, int n8, const uint8_t* Xa, 
  * `stream`, the part that must start at zero (a small extra kernel), then
  * runs the GEMM in it.  Calls that can overlap on the GPU (other streams,
  * other host threads) race on the array and give wrong results: serialise
- * them.  A device-side wait timeout is not reported, since
- * qoq_last_device_status needs a workspace pointer.  Y is then undefined, and
- * the next call starts from a cleared array.
+ * them.  A device-side wait timeout leaves Y undefined; the next call still
+ * starts from a cleared array, and qoq_no_alloc_last_status reports it.
  */
 #define QOQ_NO_ALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 qoq_status qoq_w4a8_gemm_no_alloc(int M, int N, int K, int g, const int8_t* Xq,
                                   const uint16_t* sx_f16, const uint8_t* packed,
                                   const uint16_t* s1_f16, uint16_t* Y_f16, int32_t* acc_debug,
                                   qoq_stream_t stream);
+
+/*
+ * The device status of the qoq_w4a8_gemm_no_alloc calls on the current
+ * device since the previous read: synchronizes `stream` (the stream those
+ * calls ran on), returns QOQ_OK, QOQ_ERR_DEVICE_TIMEOUT if any of them ran out
+ * of a device-side wait limit (sticky: each call's clearing step keeps its
+ * predecessor's status), or QOQ_ERR_CUDA (a CUDA error, e.g. one surfaced by
+ * the synchronization), and resets the status.  Like the calls themselves,
+ * not safe against no-alloc calls running concurrently.
+ */
+qoq_status qoq_no_alloc_last_status(qoq_stream_t stream);
 
 /*
  * Inverse of the packing layout, for testing: recovers the logical codes.

@@ -104,3 +104,36 @@ def test_no_alloc_matches_workspace_entry_point(M, N, K):
         assert np.array_equal(acc.cpu().numpy(), accr.cpu().numpy()), f"call {call}: acc differs"
         ok, rel, ab = gc.y_close(gc.f16_bits(Y), gc.f16_bits(Yr))
         assert ok, f"call {call}: Y differs (max rel {rel}, max abs {ab})"
+
+
+@pytest.mark.gpu
+@pytest.mark.skipif(not gpu_available(), reason="needs a CUDA GPU")
+def test_no_alloc_timeout_is_reported_after_later_calls():
+    """A no-alloc call that runs out of a device-side wait limit (test hook:
+    the producer skips one stage, 5 ms limit) is reported by
+    qoq_no_alloc_last_status even after a later call has cleared the array:
+    the status is sticky until read, the read resets it, and the later call
+    is bit-exact against the workspace entry point."""
+    import torch
+
+    mod = q()
+    M, N, K = 16, 128 * 152, 8192
+    W = gc.to_dev_f16(synth.weights(N, K, 75))
+    packed, s1 = mod.qoq_pack_weights(W)
+    Xq, sx = mod.qoq_quant_act(gc.to_dev_f16(synth.activations(M, K, 76)))
+    assert mod.qoq_no_alloc_last_status() == 0  # nothing pending from earlier tests
+    try:
+        mod.qoq_set_debug(5_000_000, 1)
+        mod.qoq_w4a8_gemm_no_alloc(Xq, sx, packed, s1, N)
+    finally:
+        mod.qoq_set_debug(0, 0)
+    acc = torch.full((M, N), -1, dtype=torch.int32, device="cuda")
+    mod.qoq_w4a8_gemm_no_alloc(Xq, sx, packed, s1, N, acc_debug=acc)  # clears the array, keeps the status
+    assert mod.qoq_no_alloc_last_status() == 7  # QOQ_ERR_DEVICE_TIMEOUT
+    assert mod.qoq_no_alloc_last_status() == 0  # the read reset it
+    ref = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    ws = torch.zeros(mod.qoq_gemm_workspace_bytes(M, N, K), dtype=torch.uint8, device="cuda")
+    mod.qoq_w4a8_gemm(Xq, sx, packed, s1, N, acc_debug=ref, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(acc, ref)
+    assert mod.qoq_last_device_status(ws) == 0

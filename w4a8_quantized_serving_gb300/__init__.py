@@ -13,7 +13,7 @@ _EXPORTS = (
     "QOQ_ERRORS", "QoQError", "QoQLinear", "build", "library_path", "lib",
     "qoq_gemm_workspace_bytes", "qoq_last_device_status", "qoq_pack_weights",
     "qoq_norm_quant_act", "qoq_packed_weight_bytes", "qoq_quant_act", "qoq_set_debug", "qoq_status_str",
-    "qoq_unpack_weights_debug", "qoq_version", "qoq_w4a8_gemm", "qoq_w4a8_gemm_no_alloc",
+    "qoq_unpack_weights_debug", "qoq_version", "qoq_w4a8_gemm", "qoq_w4a8_gemm_no_alloc", "qoq_no_alloc_last_status",
     "qoq_w4a8_gemm_zero_folded", "qoq_w4ax_act_bytes", "qoq_quant_act_w4ax", "qoq_w4ax_workspace_bytes",
     "qoq_w4ax_gemm", "workspace_for",
 )

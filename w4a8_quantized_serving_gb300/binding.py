@@ -22,7 +22,7 @@ QOQ_ERRORS = {
 EXPORTED = (
     "qoq_status_str", "qoq_version", "qoq_packed_weight_bytes", "qoq_gemm_workspace_bytes",
     "qoq_pack_weights", "qoq_quant_act", "qoq_norm_quant_act", "qoq_w4a8_gemm", "qoq_unpack_weights_debug",
-    "qoq_last_device_status", "qoq_set_debug", "qoq_w4a8_gemm_no_alloc", "qoq_w4a8_gemm_zero_folded",
+    "qoq_last_device_status", "qoq_no_alloc_last_status", "qoq_set_debug", "qoq_w4a8_gemm_no_alloc", "qoq_w4a8_gemm_zero_folded",
     "qoq_w4ax_act_bytes", "qoq_quant_act_w4ax", "qoq_w4ax_workspace_bytes", "qoq_w4ax_gemm",
 )
 
@@ -82,6 +82,8 @@ def lib() -> ctypes.CDLL:
             L.qoq_w4a8_gemm_zero_folded.restype = i32
             L.qoq_w4a8_gemm_no_alloc.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P]
             L.qoq_w4a8_gemm_no_alloc.restype = i32
+            L.qoq_no_alloc_last_status.argtypes = [P]
+            L.qoq_no_alloc_last_status.restype = i32
             L.qoq_unpack_weights_debug.argtypes = [i32, i32, i32, P, P, P, P, P]
             L.qoq_unpack_weights_debug.restype = i32
             L.qoq_last_device_status.argtypes = [P, P]
@@ -338,6 +340,12 @@ def qoq_last_device_status(workspace, stream=None) -> int:
     """Synchronize and return (then clear) the last GEMM's device status code."""
     torch = _torch()
     return int(lib().qoq_last_device_status(_dev(workspace, torch.uint8, "workspace"), _stream(stream)))
+
+
+def qoq_no_alloc_last_status(stream=None) -> int:
+    """Synchronize and return (then reset) the sticky device status of the
+    qoq_w4a8_gemm_no_alloc calls since the previous read."""
+    return int(lib().qoq_no_alloc_last_status(_stream(stream)))
 
 
 class QoQLinear:

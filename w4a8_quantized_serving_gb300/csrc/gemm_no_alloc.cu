@@ -28,6 +28,10 @@
 namespace {
 
 static __device__ __align__(256) unsigned char g_no_alloc_scratch[QOQ_NO_ALLOC_SCRATCH_BYTES];
+// Sticky device status of the calls since the last qoq_no_alloc_last_status:
+// each call's clear kernel folds in the status its predecessor left in the
+// header before clearing it.
+static __device__ int g_no_alloc_sticky;
 
 constexpr int kMaxDevices = 64;
 
@@ -74,7 +78,8 @@ qoq_status scratch_address(void** out) {
 }
 
 // Zeroes the part of the workspace that the GEMM requires to start at zero:
-// the header's status and abort words, and the 16-byte words [lo16, hi16)
+// the header's status and abort words (after folding a non-zero status of the
+// previous call into g_no_alloc_sticky), and the 16-byte words [lo16, hi16)
 // (split-K counters and partial sums of 128-token tiles).  The decode
 // kernel's hand-off epoch and CTA exit counter (header words 2 and 3) are
 // kept: every launch leaves the counter at zero and advances the epoch, so
@@ -84,7 +89,11 @@ __global__ void __launch_bounds__(256) no_alloc_clear_kernel(size_t lo16, size_t
   uint4* p = reinterpret_cast<uint4*>(g_no_alloc_scratch);
   const size_t stride = (size_t)gridDim.x * blockDim.x;
   const size_t tid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (tid == 0) *reinterpret_cast<uint2*>(g_no_alloc_scratch) = make_uint2(0u, 0u);  // status and abort words
+  if (tid == 0) {
+    const int prev = *reinterpret_cast<volatile int*>(g_no_alloc_scratch);  // stream-ordered after that call
+    if (prev != 0) g_no_alloc_sticky = prev;
+    *reinterpret_cast<uint2*>(g_no_alloc_scratch) = make_uint2(0u, 0u);  // status and abort words
+  }
   for (size_t i = lo16 + tid; i < hi16; i += stride) p[i] = make_uint4(0u, 0u, 0u, 0u);
 }
 
@@ -132,4 +141,24 @@ extern "C" qoq_status qoq_w4a8_gemm_no_alloc(int M, int N, int K, int g, const i
 
   return qoq_w4a8_gemm(M, N, K, g, Xq, sx_f16, packed, s1_f16, Y_f16, acc_debug, scratch,
                        QOQ_NO_ALLOC_SCRATCH_BYTES, stream);
+}
+
+extern "C" qoq_status qoq_no_alloc_last_status(qoq_stream_t stream) {
+  void* scratch = nullptr;
+  const qoq_status st = scratch_address(&scratch);
+  if (st != QOQ_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  int sticky = 0, last = 0;
+  if (e == cudaSuccess) e = cudaMemcpyFromSymbol(&sticky, g_no_alloc_sticky, sizeof(int));
+  if (e == cudaSuccess) e = cudaMemcpy(&last, scratch, sizeof(int), cudaMemcpyDeviceToHost);  // the latest call's
+  const int zero = 0;
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_no_alloc_sticky, &zero, sizeof(int));
+  if (e == cudaSuccess) e = cudaMemcpy(scratch, &zero, sizeof(int), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return QOQ_ERR_CUDA;
+  }
+  const int code = sticky != 0 ? sticky : last;
+  return code == 0 ? QOQ_OK : (code == QOQ_ERR_DEVICE_TIMEOUT ? QOQ_ERR_DEVICE_TIMEOUT : QOQ_ERR_CUDA);
 }
