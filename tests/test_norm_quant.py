@@ -42,8 +42,10 @@ def _edge_rows(X):
 
 
 @pytest.mark.parametrize("kind", ["rms", "layer"])
-@pytest.mark.parametrize("M,K", [(1, 128), (7, 512), (16, 4096), (33, 1152), (5, 16384), (3, 65536), (2, 131072)])
+@pytest.mark.parametrize("M,K", [(1, 128), (7, 512), (16, 4096), (33, 1152), (5, 16384), (3, 65536), (2, 131072),
+                                 (1100, 1152), (1024, 4096)])
 def test_norm_quant_bit_exact(kind, M, K):
+    """Shapes from one row to the M >= 1024 prefill range, K up to 131072."""
     rng = np.random.default_rng(M * 1000 + K)
     X = (synth.activations(M, K, 40 + M) * 0.5).astype(np.float16)
     X = _edge_rows(X)
