@@ -37,7 +37,8 @@ def _edge_rows(K: int, seed: int) -> np.ndarray:
 
 # ------------------------------------------------------------------ act quant --
 
-@pytest.mark.parametrize("M,K", [(1, 128), (7, 256), (8, 512), (16, 4096), (129, 384), (33, 8192)])
+@pytest.mark.parametrize("M,K", [(1, 128), (7, 256), (8, 512), (16, 4096), (129, 384), (33, 8192), (300, 8192),
+                                 (80, 65536)])
 def test_act_quant_bit_exact(M, K):
     X = synth.activations(M, K, 100 + M)
     if M >= 8:
