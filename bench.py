@@ -319,6 +319,163 @@ def roofline_of(M: int, N: int, K: int, g: int, gemm_ms: float, steps: int, peak
     return roof
 
 
+_PROBE = None
+
+
+def probe_lib():
+    """libqoq_probe.so (the streaming-read probe, csrc/probe_stream.cu), built
+    beside libqoq.so; measurement support, not part of the W4A8 path."""
+    global _PROBE
+    if _PROBE is None:
+        import ctypes
+
+        from w4a8_quantized_serving_gb300.csrc import build as _b
+
+        if not os.path.exists(_b.PROBE_LIB):
+            raise SystemExit(f"{_b.PROBE_LIB} not found (run __graft_entry__.build())")
+        L = ctypes.CDLL(_b.PROBE_LIB)
+        P, sz, i32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+        L.qoq_probe_stream_read.argtypes = [P, sz, P, i32, i32, P]
+        L.qoq_probe_stream_read.restype = i32
+        L.qoq_probe_stream_ring.argtypes = [P, sz, P, P, i32, i32, i32, P]
+        L.qoq_probe_stream_ring.restype = i32
+        _PROBE = L
+    return _PROBE
+
+
+def stream_floor(torch, dev, nbytes: int, steps: int, repeats: int, form: str = "read", dependent: bool = True,
+                 ctas_per_sm: int = 2, chunk: int = 8192, producers: int = 2) -> dict:
+    """Time per launch of a chain of `steps` streaming reads of `nbytes` each
+    (rounded up to 16), timed like the GEMM call: a CUDA graph of the chain,
+    `repeats` replays between events, the median; consecutive launches read
+    distinct buffers of a pool of at least 8 and larger than 3x L2, each
+    launch a programmatic dependent of the one before.
+    form "read": 16-byte loads from ctas_per_sm CTAs per SM, waiting for the
+    preceding launch before the first read if `dependent`.
+    form "ring": the decode GEMM's way (one CTA per SM, `producers` threads
+    bulk-copying `chunk`-byte pieces into a 192 KB shared-memory ring,
+    consumer warps); `dependent` then means the first lap is copied before the
+    wait and consumed after it, as the GEMM does with its weights (else
+    nothing is read before the wait).
+    The HBM time one launch of that size needs on this GPU."""
+    L = probe_lib()
+    nbytes = (int(nbytes) + 15) // 16 * 16
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    nbuf = max(8, int(np.ceil(3 * l2 / nbytes)))
+    bufs = [torch.randint(0, 256, (nbytes,), dtype=torch.uint8, device=dev) for _ in range(nbuf)]
+    sink = torch.zeros(1, dtype=torch.int64, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def chain(n: int):
+        st = torch.cuda.current_stream().cuda_stream
+        for i in range(n):
+            if form == "ring":
+                e = L.qoq_probe_stream_ring(bufs[i % nbuf].data_ptr(), nbytes, sink.data_ptr(), err.data_ptr(),
+                                            chunk, producers, 1 if dependent else 0, st)
+            else:
+                e = L.qoq_probe_stream_read(bufs[i % nbuf].data_ptr(), nbytes, sink.data_ptr(), ctas_per_sm,
+                                            1 if dependent else 0, st)
+            if e != 0:
+                raise RuntimeError(f"stream probe ({form}): cudaError {e}")
+
+    chain(3)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        chain(steps)
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    out = []
+    for _ in range(repeats):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        graph.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        out.append(e0.elapsed_time(e1) / steps)
+    if int(err.item()) != 0:
+        raise RuntimeError(f"stream probe ({form}): a wait inside the kernel gave up")
+    del graph, bufs
+    ms = statistics.median(out)
+    r = {"form": form, "bytes": nbytes, "ms_per_launch": ms, "gb_per_s": nbytes / (ms * 1e-3) / 1e9,
+         "regions_ms_per_launch": [round(v, 6) for v in out], "dependent": dependent}
+    if form == "read":
+        r["ctas_per_sm"] = ctas_per_sm
+    else:
+        r["chunk_bytes"], r["producers"] = chunk, producers
+    return r
+
+
+def hbm_floor_of(torch, dev, nbytes: int, gemm_ms: float, args, peaks: dict) -> dict:
+    """Two streaming-read chains at the GEMM call's algorithmic bytes, beside
+    the GEMM call's own time per launch: plain loads that wait for the
+    preceding launch first ("read"), and the GEMM's own copy structure with its
+    first lap copied before that wait ("ring")."""
+    out = {}
+    for form in ("read", "ring"):
+        fl = stream_floor(torch, dev, nbytes, args.steps, args.repeats, form=form, dependent=True)
+        fl["frac_of_peak"] = fl["gb_per_s"] / peaks["hbm_gbs"]
+        fl["gemm_ms_over_floor"] = gemm_ms / fl["ms_per_launch"]
+        out[form] = fl
+    out["kernel"] = ("libqoq_probe.so: one read of the GEMM call's algorithmic bytes per launch, each launch a "
+                     "programmatic dependent of the one before, timed like the GEMM call; 'read': 16-byte loads "
+                     "after the wait for the preceding launch; 'ring': the decode GEMM's copy structure (one CTA "
+                     "per SM, two producer threads, 8 KB bulk copies into a 192 KB ring), first lap copied before "
+                     "that wait")
+    return out
+
+
+def run_stream_sweep(args) -> None:
+    """--stream-sweep: the streaming-read chains over launch sizes from 1 MiB
+    to 1 GiB (and the algorithmic bytes of the two HBM-bound workloads): plain
+    loads, dependent and independent, also over 1, 2 and 4 CTAs per SM at the
+    decode size; the GEMM-like ring (two producers, 8 KB copies) with and
+    without its first lap copied before the wait, and at the decode size and
+    1 GiB with one producer or 16 KB copies.  One JSON line."""
+    import torch
+
+    rank, world, local = dist_env()
+    if rank != 0:
+        return
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks, peak_src = load_peaks()
+    decode = synth.WORKLOADS[1]
+    dec_bytes = algorithmic_bytes(decode["M"], decode["N"], decode["K"])["gemm"]
+    tiny = synth.WORKLOADS[0]
+    sizes = sorted({1 << 20, 1 << 22, 1 << 24, dec_bytes, 1 << 26, 1 << 28, 1 << 30,
+                    algorithmic_bytes(tiny["M"], tiny["N"], tiny["K"])["gemm"]})
+    sampler = ClockSampler(local)
+    sampler.start()
+    rows = []
+    for nb in sizes:
+        for dep in (True, False):
+            r = stream_floor(torch, dev, nb, args.steps, args.repeats, dependent=dep)
+            r["frac_of_peak"] = r["gb_per_s"] / peaks["hbm_gbs"]
+            rows.append(r)
+    for cps in (1, 4):
+        r = stream_floor(torch, dev, dec_bytes, args.steps, args.repeats, dependent=True, ctas_per_sm=cps)
+        r["frac_of_peak"] = r["gb_per_s"] / peaks["hbm_gbs"]
+        rows.append(r)
+    for nb in sizes:
+        for pre in (True, False):
+            r = stream_floor(torch, dev, nb, args.steps, args.repeats, form="ring", dependent=pre)
+            r["frac_of_peak"] = r["gb_per_s"] / peaks["hbm_gbs"]
+            rows.append(r)
+    for nb in (dec_bytes, 1 << 30):  # the copy size and the number of issuing threads
+        for chunk, prod in ((8192, 1), (16384, 1), (16384, 2)):
+            r = stream_floor(torch, dev, nb, args.steps, args.repeats, form="ring", dependent=True, chunk=chunk,
+                             producers=prod)
+            r["frac_of_peak"] = r["gb_per_s"] / peaks["hbm_gbs"]
+            rows.append(r)
+    clocks = sampler.stop()
+    print(json.dumps({"stream_sweep": rows, "peak_hbm_gbs": peaks["hbm_gbs"], "peak_source": peak_src,
+                      "steps": args.steps, "repeats": args.repeats, "clocks": clocks}), flush=True)
+
+
 def bench_workload(q, torch, c: dict, args, dev, stream, dist, rank: int) -> dict:
     """Every GPU measurement of one workload: the step, the GEMM call alone and
     the step's quantizer alone (each a CUDA graph of K steps, timed over
@@ -651,6 +808,11 @@ def run_ours(args, c: dict) -> None:
         "pack_ms": r["pack_ms"],
     }
 
+    # a launch that only reads the GEMM call's algorithmic bytes, timed the
+    # same way: the HBM time one launch of this size needs here
+    if roof["bound"] == "hbm" and not args.no_floor:
+        line["hbm_floor"] = hbm_floor_of(torch, dev, nbytes["gemm"], r["gemm_ms"], args, peaks)
+
     # the other workloads of the metric, measured the same way
     if not args.no_per_config:
         per = {}
@@ -661,6 +823,8 @@ def run_ours(args, c: dict) -> None:
             if idx == args.config:
                 entry = config_summary(cc, r, args, world, peaks, peak_src)
                 entry["clocks"] = clocks
+                if "hbm_floor" in line:
+                    entry["hbm_floor"] = line["hbm_floor"]
             else:
                 smp = ClockSampler(local)
                 smp.start()
@@ -668,6 +832,10 @@ def run_ours(args, c: dict) -> None:
                 cl = smp.stop()
                 entry = config_summary(cc, rr, args, world, peaks, peak_src)
                 entry["clocks"] = cl
+                if entry["roofline"]["bound"] == "hbm" and not args.no_floor:
+                    entry["hbm_floor"] = hbm_floor_of(
+                        torch, dev, algorithmic_bytes(cc["M"], cc["N"], cc["K"], cc.get("g", 128))["gemm"],
+                        entry["ms_per_launch"], args, peaks)
             if rank == 0 and world == 1 and not args.no_cpu_baseline:
                 entry["cpu_baseline"] = oracle_step_timing(cc, args.cpu_budget_per_config, threads=0,
                                                            n_sample=oracle_sample_channels(cc, 2e10))
@@ -709,6 +877,10 @@ def main() -> None:
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true", help="measure the headline workload only")
     ap.add_argument("--no-graph", action="store_true", help="time direct launches instead of a CUDA graph")
+    ap.add_argument("--no-floor", action="store_true",
+                    help="skip the streaming-read chain timed beside HBM-bound workloads")
+    ap.add_argument("--stream-sweep", action="store_true",
+                    help="only time the streaming-read chain over launch sizes (one JSON line)")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per GEMM launch from an ncu capture of the current library, if known")
     args = ap.parse_args()
@@ -717,7 +889,9 @@ def main() -> None:
     c = dict(synth.WORKLOADS[args.config])
     if args.g != 128:
         c["g"] = args.g
-    if args.impl == "reference":
+    if args.stream_sweep:
+        run_stream_sweep(args)
+    elif args.impl == "reference":
         run_reference(args, c)
     else:
         run_ours(args, c)

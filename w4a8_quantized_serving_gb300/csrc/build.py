@@ -3,7 +3,8 @@
 Each .cu file compiles to an object in parallel, then nvcc links the shared
 library (CUDA runtime linked statically, so the library loads without a GPU
 and without libcudart on the loader path).  Output:
-w4a8_quantized_serving_gb300/_build/libqoq.so.
+w4a8_quantized_serving_gb300/_build/libqoq.so, and beside it libqoq_probe.so,
+the benchmark's streaming-read probe (not part of the W4A8 path).
 """
 from __future__ import annotations
 
@@ -19,6 +20,8 @@ ROOT = os.path.dirname(PKG)
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libqoq.so")
 SOURCES = ["api.cu", "act_quant.cu", "pack.cu", "gemm.cu", "gemm_decode.cu", "gemm_no_alloc.cu"]
+PROBE_LIB = os.path.join(BUILD, "libqoq_probe.so")
+PROBE_SOURCES = ["probe_stream.cu"]
 HEADERS = ["internal.h", "ptx.cuh", "gemm_common.cuh", os.path.join("..", "..", "include", "qoq.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O3",
@@ -56,15 +59,20 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
             os.replace(obj + ".tmp", obj)
         return obj
 
-    with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(compile_one, SOURCES))
-    if force or _stale(LIB, objs):
-        tmp = LIB + f".{os.getpid()}.tmp"
-        cmd = [nv, *ARCH, "-shared", "-o", tmp, *objs]
-        if verbose:
-            print(" ".join(cmd), flush=True)
-        subprocess.check_call(cmd)
-        os.replace(tmp, LIB)
+    with ThreadPoolExecutor(max_workers=len(SOURCES) + len(PROBE_SOURCES)) as ex:
+        objs = list(ex.map(compile_one, SOURCES + PROBE_SOURCES))
+
+    def link(target: str, parts: list[str]) -> None:
+        if force or _stale(target, parts):
+            tmp = target + f".{os.getpid()}.tmp"
+            cmd = [nv, *ARCH, "-shared", "-o", tmp, *parts]
+            if verbose:
+                print(" ".join(cmd), flush=True)
+            subprocess.check_call(cmd)
+            os.replace(tmp, target)
+
+    link(LIB, objs[: len(SOURCES)])
+    link(PROBE_LIB, objs[len(SOURCES):])
     return LIB
 
 
