@@ -21,9 +21,11 @@ parity n & 1, which is what the kernel's parity expressions evaluate to.
     its last group of the chunk, on the chunk's accumulator barrier;
   * epilogue: waits for each chunk's accumulator and releases it.
 
-Every parity wait must pass exactly on the phase it means, and no schedule may
-deadlock.  A planted mistake -- a slot skipping the accumulator wait in chunks
-where it has no group -- must show up as a wait passing a lap early.
+Every parity wait must pass exactly on the phase it means, every stage must
+still hold a group's bytes when its slot reads them, and no schedule may
+deadlock.  Two planted mistakes must show: a slot skipping the accumulator
+wait in chunks where it has no group (a wait passes a lap early), and a slot
+releasing a stage before reading it (the stage is refilled under it).
 """
 import random
 
@@ -73,7 +75,7 @@ def schedule(M, N, K, P0=152):
     return G, T, 0, max(1, min(P0, (T * G + 3) // 4))
 
 
-def run(units, nslot, stages, skip_idle_wait=False, hold=(), seed=0):
+def run(units, nslot, stages, skip_idle_wait=False, hold=(), seed=0, early_release=False):
     """Returns (deadlocked, list of wrong passes)."""
     rng = random.Random(seed)
     sps = stages // nslot
@@ -93,6 +95,7 @@ def run(units, nslot, stages, skip_idle_wait=False, hold=(), seed=0):
             gi += n
     place = {g: ((g % nslot) * sps + (g // nslot) % sps, (g // nslot) // sps) for g in range(gi)}
     inflight, issued = [], set()
+    content = {}  # stage -> the pair whose bytes it holds (set as a copy lands)
 
     def producer():
         for g in range(gi):
@@ -116,9 +119,13 @@ def run(units, nslot, stages, skip_idle_wait=False, hold=(), seed=0):
             for k, g in enumerate(mine):
                 yield "issued", g
                 s, lap = place[g]
+                if early_release:  # planted: the stage is released before it is read
+                    yield "arrive", ("empty", s), 4
                 yield "wait", ("full", s), lap
+                yield "check", s, g  # the stage still holds this group's bytes when it is read
                 yield "wait", ("mmadone", j), nown - 1
-                yield "arrive", ("empty", s), 4
+                if not early_release:
+                    yield "arrive", ("empty", s), 4
                 yield "arrive", ("mmadone", j), 1
                 if k == len(mine) - 1:
                     yield "arrive", ("accfull", b), 1
@@ -138,7 +145,8 @@ def run(units, nslot, stages, skip_idle_wait=False, hold=(), seed=0):
         moved = False
         free = [i for i, (_, g) in enumerate(inflight) if g not in hold]
         if free and rng.random() < 0.5:
-            s, _ = inflight.pop(free[rng.randrange(len(free))])
+            s, k = inflight.pop(free[rng.randrange(len(free))])
+            content[s] = k
             bars["full", s].arrive(1)
             moved = True
         for r in rng.sample(range(len(roles)), len(roles)):
@@ -159,6 +167,10 @@ def run(units, nslot, stages, skip_idle_wait=False, hold=(), seed=0):
             elif op[0] == "arrive":
                 bars[op[1]].arrive(op[2])
                 current[r], moved = None, True
+            elif op[0] == "check":
+                if content.get(op[1]) != op[2]:
+                    wrong.append((("stage", op[1]), op[2], content.get(op[1])))
+                current[r], moved = None, True
             elif bars[op[1]].passes(op[2] & 1):  # a wait for phase n tests parity n & 1
                 bar = bars[op[1]]
                 if bar.done != op[2] + 1:  # passed on a phase other than the one meant
@@ -167,7 +179,8 @@ def run(units, nslot, stages, skip_idle_wait=False, hold=(), seed=0):
         if not moved:
             if not inflight:
                 return True, wrong
-            s, _ = inflight.pop(0)  # only held copies are left: land the oldest
+            s, k = inflight.pop(0)  # only held copies are left: land the oldest
+            content[s] = k
             bars["full", s].arrive(1)
     return False, wrong
 
@@ -204,6 +217,21 @@ def test_model_catches_a_skipped_accumulator_wait():
     units = [(t, 0, 1) for t in range(12)]
     found = any(run(units, nslot, stages, skip_idle_wait=True, hold=(h,), seed=s)[1]
                 for s in range(8) for h in range(6))
+    assert found
+    assert not any(run(units, nslot, stages, hold=(h,), seed=s)[1] for s in range(8) for h in range(6))
+
+
+def test_model_catches_a_stage_released_before_it_is_read():
+    """A slot that released a stage before reading it would let the producer
+    refill the stage under it: the model must see the stage holding another
+    group's bytes when the slot reads it."""
+    nslot, stages = config(16)
+    units = [(0, 0, 32), (1, 0, 32)]
+    found = False
+    for s in range(8):
+        for h in range(6):
+            dead, wrong = run(units, nslot, stages, hold=(h,), seed=s, early_release=True)
+            found |= dead or bool(wrong)
     assert found
     assert not any(run(units, nslot, stages, hold=(h,), seed=s)[1] for s in range(8) for h in range(6))
 
