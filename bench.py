@@ -448,6 +448,8 @@ def run_stream_sweep(args) -> None:
     tiny = synth.WORKLOADS[0]
     sizes = sorted({1 << 20, 1 << 22, 1 << 24, dec_bytes, 1 << 26, 1 << 28, 1 << 30,
                     algorithmic_bytes(tiny["M"], tiny["N"], tiny["K"])["gemm"]})
+    if args.stream_bytes:
+        sizes = [int(b) for b in args.stream_bytes.split(",")]
     sampler = ClockSampler(local)
     sampler.start()
     rows = []
@@ -456,7 +458,7 @@ def run_stream_sweep(args) -> None:
             r = stream_floor(torch, dev, nb, args.steps, args.repeats, dependent=dep)
             r["frac_of_peak"] = r["gb_per_s"] / peaks["hbm_gbs"]
             rows.append(r)
-    for cps in (1, 4):
+    for cps in (1, 4) if not args.stream_bytes else ():
         r = stream_floor(torch, dev, dec_bytes, args.steps, args.repeats, dependent=True, ctas_per_sm=cps)
         r["frac_of_peak"] = r["gb_per_s"] / peaks["hbm_gbs"]
         rows.append(r)
@@ -465,7 +467,7 @@ def run_stream_sweep(args) -> None:
             r = stream_floor(torch, dev, nb, args.steps, args.repeats, form="ring", dependent=pre)
             r["frac_of_peak"] = r["gb_per_s"] / peaks["hbm_gbs"]
             rows.append(r)
-    for nb in (dec_bytes, 1 << 30):  # the copy size and the number of issuing threads
+    for nb in (dec_bytes, 1 << 30) if not args.stream_bytes else ():  # the copy size and the number of issuing threads
         for chunk, prod in ((8192, 1), (16384, 1), (16384, 2)):
             r = stream_floor(torch, dev, nb, args.steps, args.repeats, form="ring", dependent=True, chunk=chunk,
                              producers=prod)
@@ -881,6 +883,8 @@ def main() -> None:
                     help="skip the streaming-read chain timed beside HBM-bound workloads")
     ap.add_argument("--stream-sweep", action="store_true",
                     help="only time the streaming-read chain over launch sizes (one JSON line)")
+    ap.add_argument("--stream-bytes", default="",
+                    help="with --stream-sweep: only these launch sizes (comma-separated bytes)")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per GEMM launch from an ncu capture of the current library, if known")
     args = ap.parse_args()
