@@ -339,6 +339,8 @@ def probe_lib():
         L.qoq_probe_stream_read.restype = i32
         L.qoq_probe_stream_ring.argtypes = [P, sz, P, P, i32, i32, i32, P]
         L.qoq_probe_stream_ring.restype = i32
+        L.qoq_probe_mma_issue.argtypes = [i32, i32, i32, P, P]
+        L.qoq_probe_mma_issue.restype = i32
         _PROBE = L
     return _PROBE
 
@@ -476,6 +478,46 @@ def run_stream_sweep(args) -> None:
     clocks = sampler.stop()
     print(json.dumps({"stream_sweep": rows, "peak_hbm_gbs": peaks["hbm_gbs"], "peak_source": peak_src,
                       "steps": args.steps, "repeats": args.repeats, "clocks": clocks}), flush=True)
+
+
+def mma_issue_probe(torch, dev, pair: bool, n: int, iters: int = 2048, reps: int = 3) -> dict:
+    """One thread issuing `iters` tcgen05.mma of the GEMM's shape back to back
+    (csrc/probe_mma.cu): cycles per issue over the whole run, cycles per MMA
+    until all completed, and the spacing of the first 64 issues (median of the
+    first 8 and of issues 48-63).  The last of `reps` launches is reported."""
+    L = probe_lib()
+    out = torch.zeros(68, dtype=torch.int64, device=dev)
+    h = None
+    for _ in range(reps):
+        e = L.qoq_probe_mma_issue(1 if pair else 0, n, iters, out.data_ptr(), torch.cuda.current_stream().cuda_stream)
+        if e != 0:
+            raise RuntimeError(f"qoq_probe_mma_issue: cudaError {e}")
+        torch.cuda.synchronize()
+        h = out.cpu().numpy().astype(np.int64)
+    stamps = h[4:4 + 64]
+    gaps = np.diff(np.concatenate([[0], stamps]))
+    return {"cta_group": 2 if pair else 1, "M": 256 if pair else 128, "N": n, "iters": int(h[3]),
+            "completed": bool(h[2]), "issue_cycles_per_mma": float(h[0]) / iters,
+            "complete_cycles_per_mma": float(h[1]) / iters,
+            "first_issue_gaps": [int(x) for x in gaps[:16]],
+            "gap_median_first8": float(np.median(gaps[1:9])), "gap_median_48_63": float(np.median(gaps[48:64]))}
+
+
+def run_mma_probe(args) -> None:
+    """--mma-probe: the issue probe for N=128 and N=256, one CTA and a CTA pair;
+    one JSON line."""
+    import torch
+
+    rank, world, local = dist_env()
+    if rank != 0:
+        return
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    sampler = ClockSampler(local)
+    sampler.start()
+    rows = [mma_issue_probe(torch, dev, pair, n) for pair in (False, True) for n in (128, 256)]
+    clocks = sampler.stop()
+    print(json.dumps({"mma_issue_probe": rows, "clocks": clocks}), flush=True)
 
 
 def bench_workload(q, torch, c: dict, args, dev, stream, dist, rank: int) -> dict:
@@ -883,6 +925,8 @@ def main() -> None:
                     help="skip the streaming-read chain timed beside HBM-bound workloads")
     ap.add_argument("--stream-sweep", action="store_true",
                     help="only time the streaming-read chain over launch sizes (one JSON line)")
+    ap.add_argument("--mma-probe", action="store_true",
+                    help="only run the tcgen05.mma issue-rate probe (one JSON line)")
     ap.add_argument("--stream-bytes", default="",
                     help="with --stream-sweep: only these launch sizes (comma-separated bytes)")
     ap.add_argument("--traffic", type=float, default=None,
@@ -893,7 +937,9 @@ def main() -> None:
     c = dict(synth.WORKLOADS[args.config])
     if args.g != 128:
         c["g"] = args.g
-    if args.stream_sweep:
+    if args.mma_probe:
+        run_mma_probe(args)
+    elif args.stream_sweep:
         run_stream_sweep(args)
     elif args.impl == "reference":
         run_reference(args, c)

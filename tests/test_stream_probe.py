@@ -1,4 +1,5 @@
-"""The benchmark's streaming-read probe (csrc/probe_stream.cu, libqoq_probe.so).
+"""The benchmark's probes (libqoq_probe.so): the streaming-read probe
+(csrc/probe_stream.cu) and the tcgen05.mma issue-rate probe (csrc/probe_mma.cu).
 
 It sets the GEMM call's HBM figure beside what a launch that only reads the
 same bytes takes, so it must really read every byte once: the GPU cases check
@@ -29,15 +30,19 @@ def probe():
     L.qoq_probe_stream_ring.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p,
                                         ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
     L.qoq_probe_stream_ring.restype = ctypes.c_int
+    L.qoq_probe_mma_issue.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
+    L.qoq_probe_mma_issue.restype = ctypes.c_int
     return L
 
 
 def test_probe_is_built_beside_the_library_and_not_into_it():
     from w4a8_quantized_serving_gb300.csrc import build as cbuild
 
-    assert "probe_stream.cu" in cbuild.PROBE_SOURCES and "probe_stream.cu" not in cbuild.SOURCES
+    for src in ("probe_stream.cu", "probe_mma.cu"):
+        assert src in cbuild.PROBE_SOURCES and src not in cbuild.SOURCES
     L = probe()
-    assert hasattr(L, "qoq_probe_stream_read") and hasattr(L, "qoq_probe_stream_ring")
+    for name in ("qoq_probe_stream_read", "qoq_probe_stream_ring", "qoq_probe_mma_issue"):
+        assert hasattr(L, name)
 
 
 def test_probe_rejects_bad_arguments_on_the_host():
@@ -62,6 +67,10 @@ def test_probe_rejects_bad_arguments_on_the_host():
     assert ring(FAKE, 64, sink, err + 2, 8192, 2, 1, None) == CUDA_ERROR_INVALID_VALUE
     for chunk, prod in ((4096, 1), (12288, 1), (8192, 0), (8192, 3)):
         assert ring(FAKE, 64, sink, err, chunk, prod, 1, None) == CUDA_ERROR_INVALID_VALUE
+    mma = L.qoq_probe_mma_issue
+    for pair, n, iters, out in ((2, 128, 64, FAKE), (0, 64, 64, FAKE), (0, 128, 1, FAKE), (0, 128, (1 << 20) + 1, FAKE),
+                                (0, 128, 64, None), (1, 256, 64, FAKE + 4)):
+        assert mma(pair, n, iters, out, None) == CUDA_ERROR_INVALID_VALUE
 
 
 @pytest.mark.gpu
@@ -136,3 +145,25 @@ def test_probe_chain_in_a_graph_times_like_the_bench():
     fl = bench.hbm_floor_of(torch, torch.device("cuda", 0), 76304, 0.01,
                             types.SimpleNamespace(steps=8, repeats=2), peaks)
     assert fl["read"]["dependent"] and fl["ring"]["gemm_ms_over_floor"] > 0
+
+
+@pytest.mark.gpu
+@pytest.mark.skipif(not gpu_available(), reason="needs a GPU")
+@pytest.mark.parametrize("pair", [False, True])
+@pytest.mark.parametrize("n", [128, 256])
+def test_mma_issue_probe_completes_with_plausible_rates(pair, n):
+    """Every launch completes (its bounded wait did not give up), the issue
+    stamps rise, and the rates lie between a few and a few thousand cycles."""
+    import importlib.util
+
+    import torch
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    spec = importlib.util.spec_from_file_location("bench_under_test", os.path.join(root, "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    r = bench.mma_issue_probe(torch, torch.device("cuda", 0), pair, n, iters=512, reps=2)
+    assert r["completed"] and r["iters"] == 512
+    assert 4 < r["issue_cycles_per_mma"] < 5000
+    assert r["issue_cycles_per_mma"] <= r["complete_cycles_per_mma"] + 1
+    assert all(g > 0 for g in r["first_issue_gaps"])

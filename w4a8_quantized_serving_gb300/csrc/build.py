@@ -21,7 +21,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libqoq.so")
 SOURCES = ["api.cu", "act_quant.cu", "pack.cu", "gemm.cu", "gemm_decode.cu", "gemm_no_alloc.cu"]
 PROBE_LIB = os.path.join(BUILD, "libqoq_probe.so")
-PROBE_SOURCES = ["probe_stream.cu"]
+PROBE_SOURCES = ["probe_stream.cu", "probe_mma.cu"]
 HEADERS = ["internal.h", "ptx.cuh", "gemm_common.cuh", os.path.join("..", "..", "include", "qoq.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O3",
