@@ -504,8 +504,8 @@ def mma_issue_probe(torch, dev, pair: bool, n: int, iters: int = 2048, reps: int
 
 
 def run_mma_probe(args) -> None:
-    """--mma-probe: the issue probe for N=128 and N=256, one CTA and a CTA pair;
-    one JSON line."""
+    """--mma-probe: the issue probe for N=16 .. 256 on one CTA and N=128, 256 on
+    a CTA pair; one JSON line."""
     import torch
 
     rank, world, local = dist_env()
@@ -515,7 +515,8 @@ def run_mma_probe(args) -> None:
     dev = torch.device("cuda", local)
     sampler = ClockSampler(local)
     sampler.start()
-    rows = [mma_issue_probe(torch, dev, pair, n) for pair in (False, True) for n in (128, 256)]
+    rows = [mma_issue_probe(torch, dev, False, n) for n in (16, 32, 64, 128, 256)]
+    rows += [mma_issue_probe(torch, dev, True, n) for n in (128, 256)]
     clocks = sampler.stop()
     print(json.dumps({"mma_issue_probe": rows, "clocks": clocks}), flush=True)
 

@@ -5,8 +5,8 @@
 // One thread issues `iters` MMAs of the GEMM's shape back to back (kind::f16,
 // K=16, M=128 per CTA -- 256 for a CTA pair, cta_group::2 -- and N tokens; A
 // from tensor memory, B a zero tile in shared memory, one accumulator), reads
-// the SM clock after each of the first 64 issues, then commits and waits for
-// them all to complete.  When the issue spacing stays at the thread's own
+// the SM clock before each of issues 2 .. 65, then commits and waits for them
+// all to complete.  When the issue spacing stays at the thread's own
 // rate while the tensor pipe needs less time per MMA, one issuing thread
 // cannot keep the pipe busy; when the spacing grows to the pipe's time per
 // MMA after a few issues, the thread runs ahead and later issues wait for
@@ -127,13 +127,14 @@ cudaError_t launch_probe(unsigned long long* out, int iters, cudaStream_t s) {
 
 // out: 68 unsigned 64-bit words in device memory (8-byte aligned), written as
 // described at the head of this file.  pair: 0 (one CTA, cta_group::1) or 1
-// (a cluster of two, cta_group::2); n: 128 or 256 (the MMA's N); iters: 2 ..
-// 1 << 20.  Returns a cudaError_t: cudaErrorInvalidValue for other arguments
-// (before any launch); cudaErrorNoDevice off an sm_103 device; otherwise the
-// launch's status.
+// (a cluster of two, cta_group::2); n: the MMA's N, 16, 32, 64, 128 or 256
+// for one CTA (the decode kernel's token tiles are 16, 32 or 64), 128 or 256
+// for a pair; iters: 2 .. 1 << 20.  Returns a cudaError_t:
+// cudaErrorInvalidValue for other arguments (before any launch);
+// cudaErrorNoDevice off an sm_103 device; otherwise the launch's status.
 extern "C" int qoq_probe_mma_issue(int pair, int n, int iters, unsigned long long* out, void* stream) {
-  if (!out || ((uintptr_t)out & 7u) || (pair != 0 && pair != 1) || (n != 128 && n != 256) || iters < 2 ||
-      iters > (1 << 20))
+  const bool n_ok = n == 128 || n == 256 || (!pair && (n == 16 || n == 32 || n == 64));
+  if (!out || ((uintptr_t)out & 7u) || (pair != 0 && pair != 1) || !n_ok || iters < 2 || iters > (1 << 20))
     return cudaErrorInvalidValue;
   int dev = 0, major = 0, minor = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
@@ -144,6 +145,12 @@ extern "C" int qoq_probe_mma_issue(int pair, int n, int iters, unsigned long lon
   cudaError_t e;
   if (pair)
     e = n == 128 ? launch_probe<true, 128>(out, iters, s) : launch_probe<true, 256>(out, iters, s);
+  else if (n == 16)
+    e = launch_probe<false, 16>(out, iters, s);
+  else if (n == 32)
+    e = launch_probe<false, 32>(out, iters, s);
+  else if (n == 64)
+    e = launch_probe<false, 64>(out, iters, s);
   else
     e = n == 128 ? launch_probe<false, 128>(out, iters, s) : launch_probe<false, 256>(out, iters, s);
   return (int)e;
