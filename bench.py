@@ -759,11 +759,14 @@ def config_summary(c: dict, r: dict, args, world: int, peaks: dict, peak_src: st
     G = c.get("g", 128)
     ops = 2.0 * M * N * K
     roof = roofline_of(M, N, K, G, r["gemm_ms"], args.steps, peaks, peak_src, r["n8"])
+    roof_out = {k: roof[k] for k in ("bound", "achieved", "peak", "unit", "frac", "peak_source")}
+    if G == 128 and r["n8"] is None and args.variant == "direct":
+        roof_out["traffic"], roof_out["traffic_source"] = recorded_traffic(c["name"])
+        roof_out["algorithmic_bytes_per_launch"] = roof["algorithmic_bytes_per_launch"]
     return {
         "workload": c["name"], "M": M, "N": N, "K": K, "g": G,
         "value": job_tops(world, ops, r["ms_per_step"]), "unit": UNIT, "ms_per_step": r["ms_per_step"],
-        "ms_per_launch": r["gemm_ms"], "roofline": {k: roof[k] for k in ("bound", "achieved", "peak", "unit",
-                                                                          "frac", "peak_source")},
+        "ms_per_launch": r["gemm_ms"], "roofline": roof_out,
         "gemm_tops": roof["tops_effective"], "gemm_gb_per_s": roof["gb_per_s_algorithmic"],
         "quantizer_ms": r["act_ms"],
         "e2e": {"value": job_tops(world, ops, r["e2e_ms"]), "unit": UNIT, "ms_per_step": r["e2e_ms"],
